@@ -1,0 +1,483 @@
+"""Pins for the CPU oracle: checks against things other than the oracle itself.
+
+Each ``pin_*`` function raises AssertionError (or OracleError) when the oracle
+disagrees with:
+  * hand-worked fixtures under tests/golden/ (each cites the page it follows);
+  * a sort-based brute force of the dispatch layout, written independently of
+    the oracle's counting sort;
+  * closed forms (identity expert: x_out = x * sum of contributing weights);
+  * invariants (counts, bijection of assist_info onto the routed picks);
+  * exact rational arithmetic with IEEE round-to-nearest-even (quantiser);
+  * library routines (numpy float16 and torch bfloat16 conversions, torch
+    fp64 matmul and silu for the SwiGLU expert).
+They are plain functions so that tests/test_oracle_mutants.py can rerun them
+against deliberately broken builds of the oracle.
+"""
+from __future__ import annotations
+
+import json
+import math
+import os
+import struct
+from fractions import Fraction
+
+import numpy as np
+
+import workloads as WL
+from oracle import oracle as O
+
+GOLDEN = os.path.join(os.path.dirname(os.path.abspath(__file__)), "golden")
+
+
+def golden(name: str) -> dict:
+    with open(os.path.join(GOLDEN, name), encoding="utf-8") as f:
+        return json.load(f)
+
+
+# ------------------------------------------------------------------ helpers
+
+def brute_force_layout(wl: WL.Workload, inp: dict):
+    """Dispatch layout by sorting: every routed pick becomes the key
+    (rank d, local expert le, source s, token t, topk k); sorted keys give the
+    rows of each rank, and counting keys per (le, s) gives the segment sizes."""
+    W, bs, K, E = wl.ep_world_size, wl.bs, wl.topk, wl.moe_expert_num
+    L = E // W
+    ids = inp["expert_ids"]
+    mask = inp.get("active_mask")
+    keys = []
+    for s in range(W):
+        for t in range(bs):
+            for k in range(K):
+                if mask is not None:
+                    act = mask[s, t] if mask.ndim == 2 else mask[s, t, k]
+                    if not act:
+                        continue
+                e = int(ids[s, t, k])
+                if 0 <= e < E:
+                    keys.append((e // L, e % L, s, t, k))
+    keys.sort()
+    rows = [[] for _ in range(W)]
+    seg = np.zeros((W, L * W), dtype=np.int64)
+    for d, le, s, t, k in keys:
+        rows[d].append((s, t, k))
+        seg[d, le * W + s] += 1
+    return rows, seg
+
+
+def contributing_weight_sum(wl: WL.Workload, inp: dict) -> np.ndarray:
+    """Sum over picks that are active and routed or copy (int64 / float64)."""
+    ids = inp["expert_ids"].astype(np.int64)
+    E, Z, C = wl.moe_expert_num, wl.zero_expert_num, wl.copy_expert_num
+    contrib = (ids >= 0) & (ids < E)
+    contrib |= (ids >= E + Z) & (ids < E + Z + C)
+    mask = inp.get("active_mask")
+    if mask is not None:
+        m = mask.astype(bool)
+        contrib &= m[..., None] if m.ndim == 2 else m
+    w = inp["expert_scales"]
+    if w.dtype == np.int32:
+        return (w.astype(np.int64) * contrib).sum(-1)
+    return (w.astype(np.float64) * contrib).sum(-1)
+
+
+def rn_f32(q: Fraction) -> Fraction:
+    """Round a rational to the nearest fp32 value, ties to even (normal range)."""
+    if q == 0:
+        return Fraction(0)
+    sign = -1 if q < 0 else 1
+    a = abs(q)
+    e = math.floor(math.log2(a.numerator) - math.log2(a.denominator))
+    while Fraction(2) ** e > a:
+        e -= 1
+    while Fraction(2) ** (e + 1) <= a:
+        e += 1
+    assert e >= -126, "subnormal results are outside this helper"
+    ulp = Fraction(2) ** (e - 23)
+    n = a / ulp
+    fl = n.numerator // n.denominator
+    r = n - fl
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return sign * fl * ulp
+
+
+def round_half_even(q: Fraction) -> int:
+    fl = math.floor(q)
+    r = q - fl
+    if r > Fraction(1, 2) or (r == Fraction(1, 2) and fl % 2 == 1):
+        fl += 1
+    return int(fl)
+
+
+def f32_bits(v: float) -> int:
+    return struct.unpack("<I", struct.pack("<f", v))[0]
+
+
+def quantize_exact(values) -> tuple:
+    """quantMode 2 by exact rational arithmetic: returns (q list, scale)."""
+    xs = [Fraction(float(v)) for v in values]
+    amax = max(abs(v) for v in xs)
+    if amax == 0:
+        return [0] * len(xs), Fraction(0)
+    scale = rn_f32(amax / 127)
+    q = []
+    for v in xs:
+        r = round_half_even(rn_f32(v / scale)) if v != 0 else 0
+        q.append(max(-127, min(127, r)))
+    return q, scale
+
+
+# -------------------------------------------------------------------- pins
+
+def pin_dispatch_combine_hand():
+    g = golden("dispatch_hand.json")
+    for case in g["cases"]:
+        wl = WL.Workload(case["name"], case["W"], case["bs"], case["h"], case["K"], case["E"],
+                         WL.X_INT32, zero_expert_num=case["Z"], copy_expert_num=case["C"],
+                         mask_kind=case["mask_kind"])
+        inp = {
+            "x": np.array(case["x"], dtype=np.int32),
+            "expert_ids": np.array(case["expert_ids"], dtype=np.int32),
+            "expert_scales": np.array(case["expert_scales"], dtype=np.int32),
+            "active_mask": (None if case["active_mask"] is None
+                            else np.array(case["active_mask"], dtype=np.uint8)),
+        }
+        assert O.capacity(wl) == case["capacity"], case["name"]
+        d = O.dispatch(wl, inp)
+        assert d["ep_recv_count"].tolist() == case["ep_recv_count"], case["name"]
+        for r in range(wl.ep_world_size):
+            n = len(case["assist_info"][r])
+            assert d["assist_info"][r, :n].tolist() == case["assist_info"][r], (case["name"], r)
+            assert d["expand_x"][r, :n].tolist() == case["expand_x"][r], (case["name"], r)
+        x_out = O.combine(wl, d["expand_x"], d["assist_info"], d["ep_recv_count"], inp)
+        assert x_out.tolist() == case["x_out"], case["name"]
+    for cc in g["capacity_cases"]:
+        wl = WL.Workload("cap", cc["W"], cc["bs"], 16, cc["K"], cc["E"], WL.X_INT32)
+        assert O.capacity(wl) == cc["A"], cc
+
+
+def pin_layout_bruteforce(wl: WL.Workload, inp: dict):
+    d = O.dispatch(wl, inp)
+    rows, seg = brute_force_layout(wl, inp)
+    assert np.array_equal(d["ep_recv_count"], np.cumsum(seg, axis=1)), "ep_recv_count"
+    for r in range(wl.ep_world_size):
+        n = len(rows[r])
+        got = [tuple(v) for v in d["assist_info"][r, :n].tolist()]
+        assert got == rows[r], f"assist_info of rank {r}"
+    return d
+
+
+def pin_invariants(wl: WL.Workload, inp: dict, d: dict):
+    W, bs, K = wl.ep_world_size, wl.bs, wl.topk
+    L = wl.moe_expert_num // W
+    ep = d["ep_recv_count"].astype(np.int64)
+    assert (np.diff(ep, axis=1) >= 0).all() and (ep[:, 0] >= 0).all(), "running counts"
+    ids = inp["expert_ids"]
+    mask = inp.get("active_mask")
+    active = np.ones((W, bs, K), dtype=bool)
+    if mask is not None:
+        active = np.broadcast_to(mask.astype(bool)[..., None], active.shape) if mask.ndim == 2 \
+            else mask.astype(bool)
+    routed = active & (ids >= 0) & (ids < wl.moe_expert_num)
+    assert int(ep[:, -1].sum()) == int(routed.sum()), "sum of counts = routed picks"
+    seen = np.zeros((W, bs, K), dtype=np.int64)
+    for r in range(W):
+        n = int(ep[r, -1])
+        assert n <= O.capacity(wl)
+        for row in range(n):
+            s, t, k = d["assist_info"][r, row]
+            seen[s, t, k] += 1
+            e = int(ids[s, t, k])
+            assert e // L == r, "row lands on the rank that owns its expert"
+            j = int(np.searchsorted(ep[r], row, side="right"))
+            assert j == (e % L) * W + s, "row lies in segment (local expert, source)"
+            if wl.quant_mode == 0:
+                assert np.array_equal(d["expand_x"][r, row], inp["x"][s, t]), "payload row"
+            if d.get("expand_scales") is not None:
+                assert d["expand_scales"][r, row] == inp["expert_scales"][s, t, k]
+    assert np.array_equal(seen, routed.astype(np.int64)), "assist_info is a bijection onto routed picks"
+
+
+def pin_combine_closed_form_int(wl: WL.Workload, inp: dict, d: dict):
+    """Identity expert: x_out = x * (sum of contributing weights), exactly."""
+    assert wl.x_dtype == WL.X_INT32
+    x_out = O.combine(wl, d["expand_x"], d["assist_info"], d["ep_recv_count"], inp)
+    want = inp["x"].astype(np.int64) * contributing_weight_sum(wl, inp)[..., None]
+    assert np.array_equal(x_out.astype(np.int64), want), "closed form x * sum(w)"
+
+
+def pin_combine_gather(wl: WL.Workload, inp: dict, d: dict, seed: int = 7):
+    """Non-identity expert: give every expert-output row its own random values;
+    x_out must be the weighted sum of the rows the brute-force layout assigns."""
+    assert wl.x_dtype == WL.X_INT32
+    rng = np.random.default_rng(seed)
+    y = rng.integers(-50, 51, size=d["expand_x"].shape, dtype=np.int32)
+    rows, _ = brute_force_layout(wl, inp)
+    x_out = O.combine(wl, y, d["assist_info"], d["ep_recv_count"], inp)
+    W, bs, K, h = wl.ep_world_size, wl.bs, wl.topk, wl.h
+    E, Z, C = wl.moe_expert_num, wl.zero_expert_num, wl.copy_expert_num
+    want = np.zeros((W, bs, h), dtype=np.int64)
+    where = {}
+    for r in range(W):
+        for row, key in enumerate(rows[r]):
+            where[key] = (r, row)
+    mask = inp.get("active_mask")
+    for s in range(W):
+        for t in range(bs):
+            for k in range(K):
+                if mask is not None and not (mask[s, t] if mask.ndim == 2 else mask[s, t, k]):
+                    continue
+                e = int(inp["expert_ids"][s, t, k])
+                w = int(inp["expert_scales"][s, t, k])
+                if e < E:
+                    r, row = where[(s, t, k)]
+                    want[s, t] += w * y[r, row].astype(np.int64)
+                elif E + Z <= e < E + Z + C:
+                    want[s, t] += w * inp["x"][s, t].astype(np.int64)
+    assert np.array_equal(x_out.astype(np.int64), want), "gather by assist_info"
+
+
+def pin_combine_closed_form_float(wl: WL.Workload, inp: dict, d: dict):
+    """Identity expert, float data: x_out = round(x * sum(w)) up to fp32
+    accumulation error (a few fp32 ulps before the final rounding)."""
+    x_out = O.combine(wl, d["expand_x"], d["assist_info"], d["ep_recv_count"], inp)
+    if wl.x_dtype == WL.X_FP16:
+        xf = inp["x"].astype(np.float64)
+        got = x_out.astype(np.float64)
+        ulp_rel = 2.0 ** -10
+    else:
+        xf = WL.bf16_bits_to_fp32(inp["x"]).astype(np.float64)
+        got = WL.bf16_bits_to_fp32(x_out).astype(np.float64)
+        ulp_rel = 2.0 ** -7
+    want = xf * contributing_weight_sum(wl, inp)[..., None]
+    err = np.abs(got - want)
+    bound = np.abs(want) * ulp_rel + 1e-6 * np.abs(xf) * wl.topk + 2.0 ** -24
+    assert (err <= bound).all(), f"max err {err.max()}"
+
+
+def pin_combine_order_hand():
+    g = golden("combine_order_hand.json")
+    wl = WL.Workload("order", g["W"], g["bs"], g["h"], g["K"], g["E"], WL.X_FP16,
+                     copy_expert_num=g["C"])
+    inp = {
+        "x": np.array(g["x_fp16_bits"], dtype=np.uint16).view(np.float16),
+        "expert_ids": np.array(g["expert_ids"], dtype=np.int32),
+        "expert_scales": np.array([[[int(b, 16) for b in tk] for tk in r] for r in g["expert_scales_f32_bits"]],
+                                  dtype=np.uint32).view(np.float32),
+        "active_mask": None,
+    }
+    d = O.dispatch(wl, inp)
+    x_out = O.combine(wl, d["expand_x"], d["assist_info"], d["ep_recv_count"], inp)
+    assert x_out.view(np.uint16).tolist() == g["x_out_fp16_bits"], x_out.view(np.uint16).tolist()
+
+
+def pin_quant_hand():
+    g = golden("quant_hand.json")
+    for case in g["cases"]:
+        for dt in ("float16", "bfloat16"):
+            x = np.array(case["x"], dtype=np.float32)
+            row = x.astype(np.float16) if dt == "float16" else WL.fp32_to_bf16_bits(x)
+            q, scale = O.quantize_row(row, dt)
+            assert q.tolist() == case["q"], (case["name"], dt, q.tolist())
+            assert f32_bits(scale) == int(case["scale_bits"], 16), (case["name"], dt, hex(f32_bits(scale)))
+
+
+def pin_quant_exact(n_rows: int = 40, h: int = 48, seed: int = 11):
+    """Random fp16 / bf16 rows (including exact .5 ties at scale 1) against
+    exact rational arithmetic with IEEE rounding."""
+    rng = np.random.default_rng(seed)
+    for i in range(n_rows):
+        dt = "float16" if i % 2 == 0 else "bfloat16"
+        kind = i % 4
+        if kind < 2:
+            x = (rng.standard_normal(h) * (10.0 ** rng.integers(-3, 3))).astype(np.float32)
+        else:
+            # amax 127 makes the scale exactly 1: half-integers are exact ties
+            x = (rng.integers(-254, 255, size=h) / 2.0).astype(np.float32)
+            x[0] = 127.0
+        row = x.astype(np.float16) if dt == "float16" else WL.fp32_to_bf16_bits(x)
+        vals = row.astype(np.float64) if dt == "float16" else WL.bf16_bits_to_fp32(row).astype(np.float64)
+        q, scale = O.quantize_row(row, dt)
+        want_q, want_scale = quantize_exact(vals)
+        assert q.tolist() == want_q, (i, dt)
+        assert Fraction(scale) == want_scale, (i, dt)
+
+
+def pin_quant_dispatch(wl: WL.Workload, inp: dict):
+    """quantMode 2 through dispatch: each routed row holds its token's int8 row
+    and scale, and |x - q*scale| <= scale/2 (plus the scale's own rounding)."""
+    d = O.dispatch(wl, inp)
+    ep = d["ep_recv_count"]
+    xf = (inp["x"].astype(np.float64) if wl.x_dtype == WL.X_FP16
+          else WL.bf16_bits_to_fp32(inp["x"]).astype(np.float64))
+    for r in range(wl.ep_world_size):
+        for row in range(int(ep[r, -1])):
+            s, t, k = d["assist_info"][r, row]
+            q = d["expand_x"][r, row].astype(np.int64)
+            sc = float(d["dynamic_scales"][r, row])
+            assert np.abs(q).max() <= 127
+            amax = np.abs(xf[s, t]).max()
+            if amax == 0:
+                assert sc == 0 and not q.any()
+                continue
+            assert abs(q[np.argmax(np.abs(xf[s, t]))]) == 127
+            assert np.all(np.abs(xf[s, t] - q * sc) <= sc * 0.5 * (1 + 1e-5) + amax * 2e-7)
+    return d
+
+
+def pin_plane_hand():
+    g = golden("plane_hand.json")
+    for sc in g["scenarios"]:
+        wl = WL.Workload("plane", sc["W"], 1, sc["h"], 1, sc["E"], sc["x_dtype"])
+        ep = np.array(sc["ep_recv_count"], dtype=np.int32)
+        # the fixture's segment sizes and running counts agree
+        seg = np.array(sc["segment_rows"], dtype=np.int64).reshape(sc["W"], -1)
+        assert np.array_equal(np.cumsum(seg, axis=1), ep), sc["name"]
+        got_c = O.combine_plane(wl, ep, sc["bulk_min_bytes"])
+        assert got_c.tolist() == sc["combine_plane"], (sc["name"], got_c.tolist())
+        got_d = O.dispatch_plane(wl, ep, sc["bulk_min_bytes"])
+        assert got_d.tolist() == sc["dispatch_plane"], (sc["name"], got_d.tolist())
+
+
+def pin_conversions(n: int = 20000, seed: int = 3):
+    """fp32 -> fp16 / bf16 round-to-nearest-even against numpy and torch."""
+    import torch
+    rng = np.random.default_rng(seed)
+    vals = np.concatenate([
+        rng.standard_normal(n).astype(np.float32) * np.float32(10.0) ** rng.integers(-8, 5, n).astype(np.float32),
+        # exact ties between bf16 neighbours and between fp16 neighbours
+        (np.arange(1, 200, dtype=np.uint32) << 16 | 0x8000).view(np.float32),
+        np.float32(1.0) + np.float32(2.0 ** -11) * np.arange(1, 64, 2, dtype=np.float32),
+        np.array([0.0, -0.0, 65504.0, 65520.0, 6e-8, 3e-8, 1e-40], dtype=np.float32),
+    ]).astype(np.float32)
+    L = O.lib()
+    want_h = vals.astype(np.float16).view(np.uint16)
+    want_b = torch.from_numpy(vals.copy()).to(torch.bfloat16).view(torch.int16).numpy().view(np.uint16)
+    got_h = np.array([L.orc_f32_to_fp16(float(v)) for v in vals], dtype=np.uint16)
+    got_b = np.array([L.orc_f32_to_bf16(float(v)) for v in vals], dtype=np.uint16)
+    assert np.array_equal(got_h, want_h), "fp16 rounding"
+    assert np.array_equal(got_b, want_b), "bf16 rounding"
+    back_h = np.array([L.orc_fp16_to_f32(int(b)) for b in want_h[:2000]], dtype=np.float32)
+    assert np.array_equal(back_h, want_h[:2000].view(np.float16).astype(np.float32))
+    back_b = np.array([L.orc_bf16_to_f32(int(b)) for b in want_b[:2000]], dtype=np.float32)
+    assert np.array_equal(back_b, WL.bf16_bits_to_fp32(want_b[:2000]))
+
+
+def pin_swiglu_torch(seed: int = 5):
+    """SwiGLU expert rows against torch fp64 matmul and silu (library routines)."""
+    import torch
+    rng = np.random.default_rng(seed)
+    E, h, I, n = 3, 16, 8, 7
+    wg = WL.fp32_to_bf16_bits(rng.standard_normal((E, h, I)).astype(np.float32) * np.float32(0.3))
+    wu = WL.fp32_to_bf16_bits(rng.standard_normal((E, h, I)).astype(np.float32) * np.float32(0.3))
+    wd = WL.fp32_to_bf16_bits(rng.standard_normal((E, I, h)).astype(np.float32) * np.float32(0.3))
+    x = WL.fp32_to_bf16_bits(rng.standard_normal((n, h)).astype(np.float32))
+    ex = rng.integers(0, E, size=n).astype(np.int32)
+    y = O.swiglu_rows(x, ex, wg, wu, wd)
+    t = lambda a: torch.from_numpy(WL.bf16_bits_to_fp32(a).astype(np.float64))
+    X, G, U, D = t(x), t(wg), t(wu), t(wd)
+    for i in range(n):
+        e = int(ex[i])
+        a = X[i] @ G[e]
+        b = X[i] @ U[e]
+        want = (torch.nn.functional.silu(a) * b) @ D[e]
+        assert np.allclose(y[i], want.numpy(), rtol=1e-12, atol=1e-12), i
+
+
+def pin_ffn_tokens_compose(seed: int = 9):
+    """The FFN variant for a token = sum_k w_k * expert_{e_k}(x) + copy terms:
+    checked by composing swiglu_rows over the token's picks by hand."""
+    wl = WL.Workload("ffn_tiny", 2, 3, 16, 2, 4, WL.X_BF16, copy_expert_num=1,
+                     zero_expert_num=1, special_p=0.3, ffn_intermediate=8, seed=seed)
+    inp = WL.make_inputs(wl)
+    toks = np.arange(wl.ep_world_size * wl.bs)
+    got = O.moe_ffn_tokens(wl, inp, toks)
+    xs = inp["x"].reshape(-1, wl.h)
+    ids = inp["expert_ids"].reshape(-1, wl.topk)
+    ws = inp["expert_scales"].reshape(-1, wl.topk).astype(np.float64)
+    for i in toks:
+        want = np.zeros(wl.h)
+        for k in range(wl.topk):
+            e = int(ids[i, k])
+            if e < wl.moe_expert_num:
+                want += ws[i, k] * O.swiglu_rows(xs[i:i + 1], np.array([e]), inp["w_gate"], inp["w_up"],
+                                                 inp["w_down"])[0]
+            elif e >= wl.moe_expert_num + wl.zero_expert_num:
+                want += ws[i, k] * WL.bf16_bits_to_fp32(xs[i]).astype(np.float64)
+        assert np.allclose(got[i], want, rtol=1e-12, atol=1e-14), i
+
+
+def pin_errors():
+    """Rejections the pages state: id ranges, the 1D mask order, config ranges."""
+    base = WL.Workload("err", 2, 4, 16, 2, 4, WL.X_INT32, zero_expert_num=1, copy_expert_num=1)
+    inp = WL.make_inputs(base)
+
+    def status(wl, inp):
+        return O.dispatch(wl, inp, raise_on_error=False)["status"]
+
+    assert status(base, inp) == 0
+    bad = dict(inp, expert_ids=inp["expert_ids"].copy())
+    bad["expert_ids"][1, 2, 1] = 6  # E + Z + C = 6 is out of range
+    assert status(base, bad) == 4
+    bad["expert_ids"][1, 2, 1] = -1
+    assert status(base, bad) == 4
+    dup = dict(inp, expert_ids=inp["expert_ids"].copy())
+    dup["expert_ids"][0, 0, :] = 3  # the same routed expert twice in one token
+    assert status(base, dup) == 4
+    dup["expert_ids"][0, 0, :] = 5  # the same copy expert twice is allowed
+    assert status(base, dup) == 0
+    m1 = base.with_(mask_kind=1)
+    good = dict(inp, active_mask=np.array([[1, 1, 0, 0], [1, 1, 1, 1]], dtype=np.uint8))
+    assert status(m1, good) == 0
+    badm = dict(inp, active_mask=np.array([[1, 0, 1, 0], [1, 1, 1, 1]], dtype=np.uint8))
+    assert status(m1, badm) == 5
+    # a masked pick's id is not looked at
+    masked = dict(good, expert_ids=good["expert_ids"].copy())
+    masked["expert_ids"][0, 3, 0] = 99
+    assert status(m1, masked) == 0
+    assert status(base.with_(ep_world_size=1, moe_expert_num=4), inp) == 1
+    assert status(base.with_(moe_expert_num=5), inp) == 1
+    assert status(base.with_(quant_mode=2), inp) == 2
+
+
+def run_all():
+    """Every pin, on the fixtures plus small and random workloads."""
+    pin_dispatch_combine_hand()
+    pin_combine_order_hand()
+    pin_quant_hand()
+    pin_plane_hand()
+    pin_errors()
+    for name in ("w2_bs8_h16_k2_e4_i32", "w8_bs8_h16_k2_e64_i32", "w2_bs8_h256_k2_e4_i32"):
+        wl = WL.WORKLOADS[name]
+        inp = WL.make_inputs(wl)
+        d = pin_layout_bruteforce(wl, inp)
+        pin_invariants(wl, inp, d)
+        pin_combine_closed_form_int(wl, inp, d)
+        pin_combine_gather(wl, inp, d)
+    rng = np.random.default_rng(2024)
+    for _ in range(25):
+        wl = WL.small_random_workload(rng)
+        inp = WL.make_inputs(wl)
+        d = pin_layout_bruteforce(wl, inp)
+        pin_invariants(wl, inp, d)
+        pin_combine_closed_form_int(wl, inp, d)
+        pin_combine_gather(wl, inp, d)
+    wl = WL.WORKLOADS["w8_bs8_h16_k2_e64_f16"]
+    inp = WL.make_inputs(wl)
+    d = pin_layout_bruteforce(wl, inp)
+    pin_invariants(wl, inp, d)
+    pin_combine_closed_form_float(wl, inp, d)
+    wlb = WL.Workload("bf16_small", 4, 6, 32, 3, 8, WL.X_BF16, zero_expert_num=2, copy_expert_num=2,
+                      mask_kind=2, special_p=0.2, mask_false_p=0.2, seed=17)
+    inp = WL.make_inputs(wlb)
+    d = pin_layout_bruteforce(wlb, inp)
+    pin_invariants(wlb, inp, d)
+    pin_combine_closed_form_float(wlb, inp, d)
+    wq = WL.Workload("q2_small", 4, 5, 64, 3, 8, WL.X_FP16, quant_mode=2, mask_kind=1, seed=19)
+    inp = WL.make_inputs(wq)
+    d = pin_quant_dispatch(wq, inp)
+    pin_invariants(wq, inp, d)
+    pin_quant_exact()
+    pin_conversions(n=4000)
+    pin_swiglu_torch()
+    pin_ffn_tokens_compose()

@@ -1,0 +1,103 @@
+"""Plant plausible mistakes in copies of the oracle (on the CPU) and check that
+the pins catch every one: a dropped term, a wrong index, a swapped loop, the
+wrong rounding, an off-by-one comparison."""
+import os
+import subprocess
+import tempfile
+
+import pytest
+
+import oracle_pins as P
+from oracle import oracle as O
+
+SRC = os.path.join(os.path.dirname(os.path.dirname(os.path.abspath(__file__))), "oracle", "moe_oracle.c")
+
+MUTANTS = {
+    "rank_from_modulo": [("int d = e / L;", "int d = e % W;")],
+    "exclusive_counts": [("run += cnt[g];\n        ep_recv_count[g] = (int32_t)run;",
+                          "ep_recv_count[g] = (int32_t)run;\n        run += cnt[g];")],
+    "source_major_segments": [(
+        "for (int le = 0; le < L; ++le)\n      for (int s = 0; s < W; ++s) {\n        size_t g = ((size_t)d * L + le) * W + s;\n        next[g] = run;",
+        "for (int s = 0; s < W; ++s)\n      for (int le = 0; le < L; ++le) {\n        size_t g = ((size_t)d * L + le) * W + s;\n        next[g] = run;")],
+    "tokens_reversed_in_segment": [("for (int t = 0; t < bs; ++t) {\n      size_t src",
+                                    "for (int t = bs - 1; t >= 0; --t) {\n      size_t src")],
+    "assist_fields_swapped": [("assist[row * 3 + 0] = s;\n        assist[row * 3 + 1] = t;",
+                               "assist[row * 3 + 0] = t;\n        assist[row * 3 + 1] = s;")],
+    "capacity_uses_k": [("return (int64_t)c->bs * c->W * (L < c->K ? L : c->K);",
+                         "return (int64_t)c->bs * c->W * c->K;")],
+    "mask_ignored": [("if (c->mask_kind == 0 || mask == NULL) return 1;", "return 1;")],
+    "mask_order_unchecked": [("else if (seen_false) return ORC_ERR_MASK_ORDER;", "else if (seen_false) {}")],
+    "duplicates_allowed": [("if (classify(c, ids, mask, s, t, k2, &e2) == PICK_ROUTED && e2 == e) {",
+                            "if (0) {")],
+    "zero_as_copy": [("if ((int64_t)e < (int64_t)c->E + c->Z) return PICK_ZERO;",
+                      "if ((int64_t)e < (int64_t)c->E + c->Z) return PICK_COPY;")],
+    "copy_weight_dropped_int": [("acc += w * ((const int32_t*)x)[tok * h + j];",
+                                 "acc += ((const int32_t*)x)[tok * h + j];")],
+    "copy_weight_dropped_float": [("acc = fmaf(w, load_f(c, x, tok * h + j), acc);",
+                                   "acc += load_f(c, x, tok * h + j);")],
+    "combine_unfused": [("acc = fmaf(w, load_f(c, x, tok * h + j), acc);",
+                         "acc = acc + w * load_f(c, x, tok * h + j);")],
+    "combine_k_descending": [("for (int k = 0; k < K; ++k) {\n            float w",
+                              "for (int k = K - 1; k >= 0; --k) {\n            float w")],
+    "combine_routed_weight_dropped": [(
+        "acc += w * ((const int32_t*)expert_out)[(size_t)where[tok * K + k] * h + j];",
+        "acc += ((const int32_t*)expert_out)[(size_t)where[tok * K + k] * h + j];")],
+    "quant_reciprocal": [("float r = nearbyintf(load_f(c, x, row * c->h + j) / scale);",
+                          "float r = nearbyintf(load_f(c, x, row * c->h + j) * (127.0f / amax));")],
+    "quant_round_away": [("float r = nearbyintf(", "float r = roundf(")],
+    "quant_scale_255": [("float scale = amax / 127.0f;", "float scale = amax / 255.0f;")],
+    "bf16_truncates": [("u += 0x7FFFu + lsb;", "u += 0u * lsb;")],
+    "plane_size_strict": [("bytes >= c->bulk_min_bytes && bytes * den > num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch",
+                           "bytes > c->bulk_min_bytes && bytes * den > num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch")],
+    "plane_mean_non_strict": [("bytes >= c->bulk_min_bytes && bytes * den > num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch",
+                               "bytes >= c->bulk_min_bytes && bytes * den >= num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch")],
+    "plane_remote_counts_local": [("if (s != d) remote += seg_rows", "remote += seg_rows")],
+    "dispatch_plane_wrong_den": [("const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));\n  const int64_t den = (int64_t)(W - 1 > 1 ? W - 1 : 1) * L;",
+                                  "const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));\n  const int64_t den = (int64_t)W * L;")],
+    "silu_sign": [("a[i] = a[i] / (1.0 + exp(-a[i])) * b[i];", "a[i] = a[i] / (1.0 + exp(a[i])) * b[i];")],
+    "gate_up_swapped": [("a[i] += xv * bf16_to_f32(wg[", "a[i] += xv * bf16_to_f32(wu[")],
+    "down_transposed": [("yr[j] += a[i] * bf16_to_f32(wd[(size_t)i * h + j]);",
+                         "yr[j] += a[i] * bf16_to_f32(wd[(size_t)j * I + i]);")],
+}
+
+
+def _build_mutant(text: str, workdir: str, name: str) -> str:
+    src = os.path.join(workdir, f"{name}.c")
+    lib = os.path.join(workdir, f"lib_{name}.so")
+    with open(src, "w") as f:
+        f.write(text)
+    subprocess.run(["gcc", "-O1", "-std=gnu11", "-ffp-contract=off", "-fPIC", "-shared", "-w",
+                    "-o", lib, src, "-lm"], check=True)
+    return lib
+
+
+@pytest.fixture(scope="module")
+def workdir():
+    with tempfile.TemporaryDirectory(prefix="oracle_mutants_") as d:
+        yield d
+
+
+@pytest.mark.parametrize("name", sorted(MUTANTS))
+def test_pins_catch_mutant(name, workdir):
+    with open(SRC) as f:
+        text = f.read()
+    for old, new in MUTANTS[name]:
+        assert text.count(old) == 1, f"mutation site for {name} not found exactly once"
+        text = text.replace(old, new)
+    lib = _build_mutant(text, workdir, name)
+    O.use_library(lib)
+    try:
+        with pytest.raises((AssertionError, O.OracleError, KeyError)):
+            P.run_all()
+    finally:
+        O.use_library(None)
+
+
+def test_unmutated_copy_passes(workdir):
+    with open(SRC) as f:
+        lib = _build_mutant(f.read(), workdir, "clean")
+    O.use_library(lib)
+    try:
+        P.run_all()
+    finally:
+        O.use_library(None)
