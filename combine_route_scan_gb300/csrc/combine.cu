@@ -1,0 +1,268 @@
+// MoE combine (combine_doubleplane README, 功能说明, check formula):
+//   x_out[token] = sum_k topk_output[token, k] * expert_scales[token, k]
+// where topk_output of a routed pick is the expert-output row that
+// assist_info_for_combine names for it (rows [0, ep_recv_count[d][L*W-1]) of
+// every rank d), a copy expert gives x[token] and a zero expert or an inactive
+// pick gives nothing (aclnnMoeDistributeDispatchV4, 参数说明).
+//
+// GB300 form (one HBM, so no write-back pass is needed): an inverse-map kernel
+// turns assist_info (row -> pick) into pick -> row, then a gather kernel reads
+// each token's K rows with 16-byte loads and reduces them in fp32, k
+// ascending, one fused multiply-add per pick, and rounds once to the output
+// type. The reduce checks every pick it reads against assist_info, so a row
+// map that does not match the routing is reported, not silently used.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "common.cuh"
+
+namespace crs {
+
+constexpr int kInvThreads = 256;
+constexpr int kReduceThreads = 256;
+constexpr int kReduceGroup = 4;  // picks whose loads are in flight together
+
+__global__ void __launch_bounds__(kInvThreads) combine_inverse_kernel(CombineParams p) {
+  const Shape sh = p.sh;
+  const int d = blockIdx.y;
+  const int LW = sh.L * sh.W;
+  pdl_wait();
+  pdl_launch_dependents();
+  long long count = p.ep_recv_count[(size_t)d * LW + LW - 1];
+  if (count < 0 || count > sh.A) {
+    if (threadIdx.x == 0 && blockIdx.x == 0) set_error(p.status, MOE_ERR_BAD_ASSIST);
+    count = count < 0 ? 0 : sh.A;
+  }
+  for (long long row = (long long)blockIdx.x * kInvThreads + threadIdx.x; row < count;
+       row += (long long)gridDim.x * kInvThreads) {
+    const long long fr = (long long)d * sh.A + row;
+    const int s = p.assist[fr * 3 + 0], t = p.assist[fr * 3 + 1], k = p.assist[fr * 3 + 2];
+    if (s < 0 || s >= sh.W || t < 0 || t >= sh.bs || k < 0 || k >= sh.K) {
+      set_error(p.status, MOE_ERR_BAD_ASSIST);
+      continue;
+    }
+    p.inv[((size_t)s * sh.bs + t) * sh.K + k] = (int32_t)fr;
+  }
+}
+
+// Element traits: 16-byte vectors of T, fp32 (or wrapping int32) accumulators.
+template <int DT>
+struct Vec;
+template <>
+struct Vec<MOE_F16> {
+  static constexpr int N = 8;
+  __device__ static void fma(float* acc, float w, int4 v) {
+    const __half2* h = reinterpret_cast<const __half2*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __half22float2(h[i]);
+      acc[2 * i] = __fmaf_rn(w, f.x, acc[2 * i]);
+      acc[2 * i + 1] = __fmaf_rn(w, f.y, acc[2 * i + 1]);
+    }
+  }
+  __device__ static int4 pack(const float* acc) {
+    int4 o;
+    __half2* h = reinterpret_cast<__half2*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2half2_rn(acc[2 * i], acc[2 * i + 1]);
+    return o;
+  }
+};
+template <>
+struct Vec<MOE_BF16> {
+  static constexpr int N = 8;
+  __device__ static void fma(float* acc, float w, int4 v) {
+    const __nv_bfloat162* h = reinterpret_cast<const __nv_bfloat162*>(&v);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const float2 f = __bfloat1622float2(h[i]);
+      acc[2 * i] = __fmaf_rn(w, f.x, acc[2 * i]);
+      acc[2 * i + 1] = __fmaf_rn(w, f.y, acc[2 * i + 1]);
+    }
+  }
+  __device__ static int4 pack(const float* acc) {
+    int4 o;
+    __nv_bfloat162* h = reinterpret_cast<__nv_bfloat162*>(&o);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) h[i] = __floats2bfloat162_rn(acc[2 * i], acc[2 * i + 1]);
+    return o;
+  }
+};
+
+// Builds the contributing-pick list of token `tau` (warp 0): source row
+// pointers and weights in ascending k. Records errors for ids out of range and
+// for a row map that does not name this pick.
+struct ReduceTable {
+  const uint8_t* src[32];
+  uint32_t w[32];  // fp32 or int32 bits
+  int n;
+};
+
+__device__ __forceinline__ void build_reduce_table(const CombineParams& p, size_t tau, ReduceTable& tab) {
+  const Shape& sh = p.sh;
+  const int lane = threadIdx.x & 31;
+  const uint8_t* src = nullptr;
+  uint32_t w = 0;
+  if (lane < sh.K) {
+    const int c = classify_pick(p.ids, p.mask, sh, tau, lane);
+    if (c == kPickBad) {
+      set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+    } else if (c >= 0) {
+      const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
+      const long long r = p.inv[tau * sh.K + lane];
+      const int LW = sh.L * sh.W;
+      const int d = c / sh.L;
+      const long long row = r - (long long)d * sh.A;
+      bool good = row >= 0 && row < sh.A && row < p.ep_recv_count[(size_t)d * LW + LW - 1];
+      if (good) {
+        const int32_t* a = p.assist + r * 3;
+        good = a[0] == s && a[1] == t && a[2] == lane;
+      }
+      if (good) {
+        src = static_cast<const uint8_t*>(p.expert_out) + r * (long long)sh.row_in;
+      } else {
+        set_error(p.status, MOE_ERR_BAD_ASSIST);
+      }
+    } else if (c == kPickCopy) {
+      src = static_cast<const uint8_t*>(p.x) + tau * (size_t)sh.row_in;
+    }
+    if (src) w = reinterpret_cast<const uint32_t*>(p.scales)[tau * sh.K + lane];
+  }
+  const uint32_t m = __ballot_sync(0xffffffffu, src != nullptr);
+  if (src) {
+    const int j = __popc(m & lanemask_lt());
+    tab.src[j] = src;
+    tab.w[j] = w;
+  }
+  if (lane == 0) tab.n = __popc(m);
+}
+
+// One CTA per (token, chunk of vectors); each thread owns one 16-byte output
+// vector per pass and keeps kReduceGroup picks' loads in flight.
+template <int DT>
+__global__ void __launch_bounds__(kReduceThreads) combine_reduce_kernel(CombineParams p, int chunks, int vpc) {
+  __shared__ ReduceTable tab;
+  const Shape sh = p.sh;
+  const size_t tau = blockIdx.x / chunks;
+  const int c = blockIdx.x % chunks;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (threadIdx.x < 32) build_reduce_table(p, tau, tab);
+  __syncthreads();
+  const int n = tab.n;
+  const int nvec = sh.row_in / 16;
+  const int v0 = c * vpc, v1 = min(nvec, v0 + vpc);
+  uint8_t* out = static_cast<uint8_t*>(p.x_out) + tau * (size_t)sh.row_in;
+  for (int v = v0 + threadIdx.x; v < v1; v += kReduceThreads) {
+    const size_t off = (size_t)v * 16;
+    if constexpr (DT == MOE_I32) {
+      uint32_t acc[4] = {0u, 0u, 0u, 0u};
+      int j = 0;
+      for (; j + kReduceGroup <= n; j += kReduceGroup) {
+        int4 y[kReduceGroup];
+#pragma unroll
+        for (int g = 0; g < kReduceGroup; ++g) y[g] = ld_nc_v4(tab.src[j + g] + off);
+#pragma unroll
+        for (int g = 0; g < kReduceGroup; ++g) {
+          const uint32_t w = tab.w[j + g];
+          acc[0] += w * (uint32_t)y[g].x;
+          acc[1] += w * (uint32_t)y[g].y;
+          acc[2] += w * (uint32_t)y[g].z;
+          acc[3] += w * (uint32_t)y[g].w;
+        }
+      }
+      for (; j < n; ++j) {
+        const int4 y = ld_nc_v4(tab.src[j] + off);
+        const uint32_t w = tab.w[j];
+        acc[0] += w * (uint32_t)y.x;
+        acc[1] += w * (uint32_t)y.y;
+        acc[2] += w * (uint32_t)y.z;
+        acc[3] += w * (uint32_t)y.w;
+      }
+      st_v4(out + off, make_int4((int)acc[0], (int)acc[1], (int)acc[2], (int)acc[3]));
+    } else {
+      float acc[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+      int j = 0;
+      for (; j + kReduceGroup <= n; j += kReduceGroup) {
+        int4 y[kReduceGroup];
+#pragma unroll
+        for (int g = 0; g < kReduceGroup; ++g) y[g] = ld_nc_v4(tab.src[j + g] + off);
+#pragma unroll
+        for (int g = 0; g < kReduceGroup; ++g) Vec<DT>::fma(acc, __uint_as_float(tab.w[j + g]), y[g]);
+      }
+      for (; j < n; ++j) Vec<DT>::fma(acc, __uint_as_float(tab.w[j]), ld_nc_v4(tab.src[j] + off));
+      st_v4(out + off, Vec<DT>::pack(acc));
+    }
+  }
+}
+
+// Element-wise fallback for rows that are not 16-byte multiples.
+template <int DT>
+__global__ void __launch_bounds__(kReduceThreads) combine_reduce_plain_kernel(CombineParams p) {
+  __shared__ ReduceTable tab;
+  const Shape sh = p.sh;
+  pdl_wait();
+  pdl_launch_dependents();
+  for (size_t tau = blockIdx.x; tau < (size_t)sh.W * sh.bs; tau += gridDim.x) {
+    if (threadIdx.x < 32) build_reduce_table(p, tau, tab);
+    __syncthreads();
+    const int n = tab.n;
+    for (int j = threadIdx.x; j < sh.h; j += kReduceThreads) {
+      if constexpr (DT == MOE_I32) {
+        uint32_t acc = 0;
+        for (int q = 0; q < n; ++q) acc += tab.w[q] * reinterpret_cast<const uint32_t*>(tab.src[q])[j];
+        reinterpret_cast<uint32_t*>(p.x_out)[tau * sh.h + j] = acc;
+      } else {
+        float acc = 0.f;
+        for (int q = 0; q < n; ++q) {
+          const uint16_t b = reinterpret_cast<const uint16_t*>(tab.src[q])[j];
+          const float y = DT == MOE_F16 ? __half2float(__ushort_as_half(b))
+                                        : __bfloat162float(__ushort_as_bfloat16(b));
+          acc = __fmaf_rn(__uint_as_float(tab.w[q]), y, acc);
+        }
+        uint16_t o = DT == MOE_F16 ? __half_as_ushort(__float2half_rn(acc))
+                                   : __bfloat16_as_ushort(__float2bfloat16_rn(acc));
+        reinterpret_cast<uint16_t*>(p.x_out)[tau * sh.h + j] = o;
+      }
+    }
+    __syncthreads();
+  }
+}
+
+cudaError_t launch_combine_inverse(const CombineParams& p, cudaStream_t st) {
+  const Shape& sh = p.sh;
+  const long long per_rank_blocks = (sh.A + kInvThreads - 1) / kInvThreads;
+  const int gx = (int)(per_rank_blocks < 32 ? (per_rank_blocks > 0 ? per_rank_blocks : 1) : 32);
+  PdlLaunch L(dim3(gx, sh.W), dim3(kInvThreads), 0, st);
+  return cudaLaunchKernelEx(&L.cfg, combine_inverse_kernel, p);
+}
+
+cudaError_t launch_combine_reduce(const CombineParams& p, cudaStream_t st, int num_sms) {
+  const Shape& sh = p.sh;
+  const long long n_tok = (long long)sh.W * sh.bs;
+  if (n_tok == 0) return cudaSuccess;
+  if (sh.row_in % 16 != 0) {
+    const int grid = (int)(n_tok < num_sms * 8LL ? n_tok : num_sms * 8LL);
+    PdlLaunch L(dim3(grid), dim3(kReduceThreads), 0, st);
+    if (sh.x_dtype == MOE_I32) return cudaLaunchKernelEx(&L.cfg, combine_reduce_plain_kernel<MOE_I32>, p);
+    if (sh.x_dtype == MOE_F16) return cudaLaunchKernelEx(&L.cfg, combine_reduce_plain_kernel<MOE_F16>, p);
+    return cudaLaunchKernelEx(&L.cfg, combine_reduce_plain_kernel<MOE_BF16>, p);
+  }
+  const int nvec = sh.row_in / 16;
+  const int vpc = kReduceThreads;  // one vector per thread per chunk
+  const int chunks = (nvec + vpc - 1) / vpc;
+  const long long grid = n_tok * chunks;
+  if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
+  PdlLaunch L(dim3((unsigned)grid), dim3(kReduceThreads), 0, st);
+  if (sh.x_dtype == MOE_I32) return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_I32>, p, chunks, vpc);
+  if (sh.x_dtype == MOE_F16) return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_F16>, p, chunks, vpc);
+  return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_BF16>, p, chunks, vpc);
+}
+
+}  // namespace crs
+
+namespace crs {
+cudaError_t launch_combine_two_phase(const CombineParams&, cudaStream_t, int) { return cudaErrorNotSupported; }
+}  // namespace crs

@@ -1,0 +1,138 @@
+// Internal declarations of the MoE dispatch / combine library: workspace
+// layout, kernel parameter blocks and launchers. Not part of the public ABI.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stddef.h>
+#include <stdint.h>
+
+#include "../../include/moe.h"
+
+namespace crs {
+
+// Workspace header (first 256 bytes of the workspace).
+struct WsHeader {
+  int status;           // first device-side error (moe_status_t), sticky until read
+  uint32_t epoch;       // two-phase combine flag epoch (last completed call)
+  uint32_t route_done;  // route CTAs finished in the current dispatch
+  uint32_t tp_done;     // two-phase combine CTAs finished in the current call
+  uint32_t pad[60];
+};
+static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
+
+// Byte offsets of the workspace regions.
+struct WsLayout {
+  size_t cnt;      // int32 [E*W]     rows of segment g = e*W + s
+  size_t base;     // int32 [E*W]     first row of segment g inside its rank
+  size_t plane_d;  // uint8 [E*W]     dispatch plane per segment
+  size_t rank;     // int32 [W*bs*K]  position of a routed pick inside its segment
+  size_t inv;      // int32 [W*bs*K]  combine: flat expert-output row of each pick
+  size_t plane_c;  // uint8 [E*W]     two-phase combine plane per segment
+  size_t flags;    // uint32 [W*bs*K] two-phase combine ready flags
+  size_t window;   // [W*bs*K][h]     two-phase combine window
+  // moe_dispatch_ffn_combine only
+  size_t ffn_expand_x;   // bf16 [W*A][h]
+  size_t ffn_assist;     // int32 [W*A][3]
+  size_t ffn_ep;         // int32 [W][L*W]
+  size_t ffn_h1;         // bf16 [W*A][I]
+  size_t ffn_y;          // bf16 [W*A][h]
+  size_t ffn_tiles;      // int32 tile table
+  size_t total;
+};
+
+struct Shape {
+  int W, bs, h, K, E, L, Z, C;
+  int mask_kind, quant, x_dtype;
+  int64_t A;         // rows per rank
+  int es;            // element bytes of x
+  int row_in;        // h * es
+  int row_out;       // bytes of an expand_x row (h for int8)
+};
+
+struct RouteParams {
+  const int32_t* ids;
+  const uint8_t* mask;
+  Shape sh;
+  int32_t* cnt;
+  int32_t* rank;
+  int32_t* base;
+  int32_t* ep_recv_count;
+  uint8_t* plane;
+  uint8_t* seg_plane_out;  // optional user copy of plane
+  int plane_policy;
+  int bulk_ok;             // rows and pointers allow TMA bulk copies
+  int64_t bulk_min_bytes;
+  uint32_t* done;
+  int* status;
+};
+
+struct ScatterParams {
+  const void* x;
+  const int32_t* ids;
+  const uint8_t* mask;
+  const void* scales;      // may be null
+  void* expand_x;
+  float* dyn_scales;       // quant 2
+  int32_t* assist;
+  void* expand_scales;     // may be null
+  const int32_t* rank;
+  const int32_t* base;
+  const uint8_t* plane;
+  Shape sh;
+  int* status;
+  uint64_t timeout_ns;
+};
+
+struct CombineParams {
+  const void* expert_out;
+  const int32_t* assist;
+  const int32_t* ep_recv_count;
+  const int32_t* ids;
+  const void* scales;
+  const uint8_t* mask;
+  const void* x;
+  void* x_out;
+  int32_t* inv;
+  Shape sh;
+  int* status;
+  // two-phase
+  void* window;
+  uint32_t* flags;
+  uint8_t* plane;
+  uint8_t* seg_plane_out;
+  WsHeader* hdr;
+  int plane_policy;
+  int bulk_ok;
+  int64_t bulk_min_bytes;
+  int put_only;
+  uint64_t timeout_ns;
+};
+
+// True when the TMA scatter's shared-memory ring fits for this shape.
+bool scatter_tma_fits(const Shape& sh);
+
+// Launchers (each returns the launch error, if any).
+cudaError_t launch_route(const RouteParams& p, cudaStream_t st);
+cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t st, int num_sms, bool tma);
+cudaError_t launch_combine_inverse(const CombineParams& p, cudaStream_t st);
+cudaError_t launch_combine_reduce(const CombineParams& p, cudaStream_t st, int num_sms);
+cudaError_t launch_combine_two_phase(const CombineParams& p, cudaStream_t st, int num_sms);
+
+// Launch config helper: programmatic dependent launch on `st`.
+struct PdlLaunch {
+  cudaLaunchConfig_t cfg;
+  cudaLaunchAttribute attr[1];
+  PdlLaunch(dim3 grid, dim3 block, size_t smem, cudaStream_t st) {
+    cfg = cudaLaunchConfig_t{};
+    cfg.gridDim = grid;
+    cfg.blockDim = block;
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = st;
+    attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    attr[0].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+  }
+};
+
+}  // namespace crs

@@ -1,0 +1,297 @@
+// Host side of the C ABI declared in include/moe.h: argument validation
+// (value ranges of aclnnMoeDistributeDispatchV4, 参数说明), the workspace
+// layout (first phase of its GetWorkspaceSize + execute contract) and the
+// kernel launches, chained on the caller's stream with programmatic
+// dependent launch.
+#include <string.h>
+
+#include "internal.h"
+
+using namespace crs;
+
+namespace {
+
+constexpr size_t kAlign = 256;
+
+size_t align_up(size_t v, size_t a) { return (v + a - 1) / a * a; }
+
+int elem_bytes(int dt) { return dt == MOE_I32 ? 4 : 2; }
+
+moe_status_t make_shape(const moe_config_t* c, Shape* sh) {
+  if (!c) return MOE_ERR_INVALID_ARG;
+  if (c->ep_world_size < 2 || c->ep_world_size > 768) return MOE_ERR_INVALID_ARG;
+  if (c->moe_expert_num <= 0 || c->moe_expert_num > 1024 || c->moe_expert_num % c->ep_world_size)
+    return MOE_ERR_INVALID_ARG;
+  if (c->bs < 0 || c->h <= 0 || c->topk < 1 || c->topk > 32) return MOE_ERR_INVALID_ARG;
+  if (c->zero_expert_num < 0 || c->copy_expert_num < 0 || c->const_expert_num < 0) return MOE_ERR_INVALID_ARG;
+  if ((long long)c->moe_expert_num + c->zero_expert_num + c->copy_expert_num + c->const_expert_num >=
+      2147483647LL)
+    return MOE_ERR_INVALID_ARG;
+  if (c->const_expert_num != 0) return MOE_ERR_UNSUPPORTED;
+  if (c->mask_kind < 0 || c->mask_kind > 2) return MOE_ERR_INVALID_ARG;
+  if (c->x_dtype < MOE_I32 || c->x_dtype > MOE_BF16) return MOE_ERR_INVALID_ARG;
+  if (c->quant_mode != 0 && c->quant_mode != 2) return MOE_ERR_UNSUPPORTED;
+  if (c->quant_mode == 2 && c->x_dtype == MOE_I32) return MOE_ERR_UNSUPPORTED;
+  if (c->plane_policy < MOE_PLANE_RULE || c->plane_policy > MOE_PLANE_BULK_ALL) return MOE_ERR_INVALID_ARG;
+  if (c->bulk_min_bytes < 0) return MOE_ERR_INVALID_ARG;
+  if (c->combine_mode < MOE_COMBINE_GATHER || c->combine_mode > MOE_COMBINE_PUT_ONLY) return MOE_ERR_INVALID_ARG;
+  if (c->wait_timeout_us <= 0) return MOE_ERR_INVALID_ARG;
+  if (c->ffn_intermediate < 0 || c->reserved0 != 0) return MOE_ERR_INVALID_ARG;
+  const long long picks = (long long)c->ep_world_size * c->bs * c->topk;
+  if (picks >= 2147483647LL) return MOE_ERR_INVALID_ARG;
+  sh->W = c->ep_world_size;
+  sh->bs = c->bs;
+  sh->h = c->h;
+  sh->K = c->topk;
+  sh->E = c->moe_expert_num;
+  sh->L = c->moe_expert_num / c->ep_world_size;
+  sh->Z = c->zero_expert_num;
+  sh->C = c->copy_expert_num;
+  sh->mask_kind = c->mask_kind;
+  sh->quant = c->quant_mode;
+  sh->x_dtype = c->x_dtype;
+  sh->A = (int64_t)c->bs * c->ep_world_size * (sh->L < sh->K ? sh->L : sh->K);
+  sh->es = elem_bytes(c->x_dtype);
+  const long long row_in = (long long)c->h * sh->es;
+  if (row_in > (1LL << 30)) return MOE_ERR_INVALID_ARG;
+  sh->row_in = (int)row_in;
+  sh->row_out = c->quant_mode == 2 ? c->h : sh->row_in;
+  if ((long long)sh->W * sh->A >= 2147483647LL) return MOE_ERR_INVALID_ARG;  // flat rows fit int32
+  return MOE_OK;
+}
+
+WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
+  WsLayout L{};
+  size_t off = sizeof(WsHeader);
+  auto take = [&](size_t bytes) {
+    size_t o = off;
+    off = align_up(off + bytes, kAlign);
+    return o;
+  };
+  const size_t segs = (size_t)sh.E * sh.W;
+  const size_t picks = (size_t)sh.W * sh.bs * sh.K;
+  L.cnt = take(segs * 4);
+  L.base = take(segs * 4);
+  L.plane_d = take(segs);
+  L.rank = take(picks * 4);
+  L.inv = take(picks * 4);
+  if (c->combine_mode != MOE_COMBINE_GATHER) {
+    L.plane_c = take(segs);
+    L.flags = take(picks * 4);
+    L.window = take(picks * (size_t)sh.row_in);
+  }
+  L.total = off;
+  return L;
+}
+
+int num_sms_of_current_device() {
+  static int cache[64] = {};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (dev >= 0 && dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev);
+  if (dev >= 0 && dev < 64) cache[dev] = n;
+  return n;
+}
+
+bool aligned(const void* p, size_t a) { return ((uintptr_t)p % a) == 0; }
+
+uint64_t timeout_ns(const moe_config_t* c) { return (uint64_t)c->wait_timeout_us * 1000ull; }
+
+moe_status_t check_ws(const moe_config_t* c, const Shape& sh, void* ws, size_t ws_bytes, WsLayout* L) {
+  *L = make_layout(c, sh);
+  if (!ws || ws_bytes < L->total || !aligned(ws, kAlign)) return MOE_ERR_WORKSPACE;
+  return MOE_OK;
+}
+
+moe_status_t record(void* const* ev, int which, cudaStream_t st) {
+  if (!ev || !ev[which]) return MOE_OK;
+  return cudaEventRecord(static_cast<cudaEvent_t>(ev[which]), st) == cudaSuccess ? MOE_OK : MOE_ERR_CUDA;
+}
+
+}  // namespace
+
+extern "C" {
+
+moe_status_t moe_get_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, int64_t* rows_per_rank) {
+  Shape sh;
+  moe_status_t st = make_shape(cfg, &sh);
+  if (st != MOE_OK) return st;
+  const WsLayout L = make_layout(cfg, sh);
+  if (ws_bytes) *ws_bytes = L.total;
+  if (rows_per_rank) *rows_per_rank = sh.A;
+  return MOE_OK;
+}
+
+moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, void* stream) {
+  Shape sh;
+  moe_status_t st = make_shape(cfg, &sh);
+  if (st != MOE_OK) return st;
+  WsLayout L;
+  st = check_ws(cfg, sh, ws, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (L.flags && cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.flags, 0,
+                                 (size_t)sh.W * sh.bs * sh.K * 4, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
+                          const uint8_t* active_mask, const void* expert_scales, void* expand_x,
+                          float* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                          void* expand_scales, uint8_t* seg_plane, void* ws, size_t ws_bytes, void* stream) {
+  Shape sh;
+  moe_status_t st = make_shape(cfg, &sh);
+  if (st != MOE_OK) return st;
+  const bool empty = sh.W * (long long)sh.bs == 0;
+  if (!empty && (!x || !expert_ids || !expand_x || !assist_info)) return MOE_ERR_INVALID_ARG;
+  if (!ep_recv_count) return MOE_ERR_INVALID_ARG;
+  if (sh.mask_kind != 0 && !active_mask && !empty) return MOE_ERR_INVALID_ARG;
+  if (expand_scales && !expert_scales) return MOE_ERR_INVALID_ARG;
+  if (sh.quant == 2 && !dynamic_scales) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4) ||
+      !aligned(assist_info, 4) || !aligned(ep_recv_count, 4) || !aligned(expand_scales, 4) ||
+      !aligned(dynamic_scales, 4))
+    return MOE_ERR_INVALID_ARG;
+  WsLayout L;
+  st = check_ws(cfg, sh, ws, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nsm = num_sms_of_current_device();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+
+  const bool tma = sh.row_in % 16 == 0 && sh.row_out % 16 == 0 && scatter_tma_fits(sh);
+
+  RouteParams rp{};
+  rp.ids = expert_ids;
+  rp.mask = sh.mask_kind ? active_mask : nullptr;
+  rp.sh = sh;
+  rp.cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+  rp.rank = reinterpret_cast<int32_t*>(w + L.rank);
+  rp.base = reinterpret_cast<int32_t*>(w + L.base);
+  rp.ep_recv_count = ep_recv_count;
+  rp.plane = w + L.plane_d;
+  rp.seg_plane_out = seg_plane;
+  rp.plane_policy = cfg->plane_policy;
+  rp.bulk_ok = tma ? 1 : 0;
+  rp.bulk_min_bytes = cfg->bulk_min_bytes;
+  rp.done = &hdr->route_done;
+  rp.status = &hdr->status;
+  if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
+
+  ScatterParams sp{};
+  sp.x = x;
+  sp.ids = expert_ids;
+  sp.mask = rp.mask;
+  sp.scales = expert_scales;
+  sp.expand_x = expand_x;
+  sp.dyn_scales = dynamic_scales;
+  sp.assist = assist_info;
+  sp.expand_scales = expand_scales;
+  sp.rank = rp.rank;
+  sp.base = rp.base;
+  sp.plane = rp.plane;
+  sp.sh = sh;
+  sp.status = &hdr->status;
+  sp.timeout_ns = timeout_ns(cfg);
+  if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
+  if (launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const int32_t* assist_info,
+                         const int32_t* ep_recv_count, const int32_t* expert_ids, const void* expert_scales,
+                         const uint8_t* active_mask, const void* x, void* x_out, uint8_t* seg_plane, void* ws,
+                         size_t ws_bytes, void* stream) {
+  Shape sh;
+  moe_status_t st = make_shape(cfg, &sh);
+  if (st != MOE_OK) return st;
+  if (cfg->quant_mode != 0) return MOE_ERR_UNSUPPORTED;  // expert outputs are in x's type
+  const bool empty = sh.W * (long long)sh.bs == 0;
+  if (!ep_recv_count) return MOE_ERR_INVALID_ARG;
+  if (!empty && (!expert_out || !assist_info || !expert_ids || !expert_scales)) return MOE_ERR_INVALID_ARG;
+  if (!empty && cfg->combine_mode != MOE_COMBINE_PUT_ONLY && !x_out) return MOE_ERR_INVALID_ARG;
+  if (sh.mask_kind != 0 && !active_mask && !empty) return MOE_ERR_INVALID_ARG;
+  if (sh.C > 0 && !x && !empty) return MOE_ERR_INVALID_ARG;
+  if (!aligned(expert_out, 16) || !aligned(x, 16) || !aligned(x_out, 16) || !aligned(assist_info, 4) ||
+      !aligned(ep_recv_count, 4) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4))
+    return MOE_ERR_INVALID_ARG;
+  WsLayout L;
+  st = check_ws(cfg, sh, ws, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nsm = num_sms_of_current_device();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+
+  CombineParams cp{};
+  cp.expert_out = expert_out;
+  cp.assist = assist_info;
+  cp.ep_recv_count = ep_recv_count;
+  cp.ids = expert_ids;
+  cp.scales = expert_scales;
+  cp.mask = sh.mask_kind ? active_mask : nullptr;
+  cp.x = x;
+  cp.x_out = x_out;
+  cp.inv = reinterpret_cast<int32_t*>(w + L.inv);
+  cp.sh = sh;
+  cp.status = &hdr->status;
+  cp.hdr = hdr;
+  cp.plane_policy = cfg->plane_policy;
+  cp.bulk_min_bytes = cfg->bulk_min_bytes;
+  cp.timeout_ns = timeout_ns(cfg);
+  cp.seg_plane_out = seg_plane;
+  if (empty) return MOE_OK;
+  if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
+  if (cfg->combine_mode == MOE_COMBINE_GATHER) {
+    if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    cp.window = w + L.window;
+    cp.flags = reinterpret_cast<uint32_t*>(w + L.flags);
+    cp.plane = w + L.plane_c;
+    cp.bulk_ok = sh.row_in % 16 == 0 && aligned(expert_out, 16);
+    cp.put_only = cfg->combine_mode == MOE_COMBINE_PUT_ONLY;
+    cudaError_t e = launch_combine_two_phase(cp, s, nsm);
+    if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  }
+  if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_get_device_status(void* ws, void* stream, int32_t* status) {
+  if (!ws || !status) return MOE_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, ws, sizeof(int32_t), cudaMemcpyDeviceToHost, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(ws, 0, sizeof(int32_t), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return MOE_ERR_CUDA;
+  *status = v;
+  return MOE_OK;
+}
+
+const char* moe_status_string(int32_t status) {
+  switch (status) {
+    case MOE_OK: return "ok";
+    case MOE_ERR_INVALID_ARG: return "invalid argument";
+    case MOE_ERR_UNSUPPORTED: return "unsupported";
+    case MOE_ERR_WORKSPACE: return "workspace too small or misaligned";
+    case MOE_ERR_BAD_EXPERT_ID: return "expert id out of range or repeated in a token";
+    case MOE_ERR_MASK_ORDER: return "1D active mask has a true after a false";
+    case MOE_ERR_TIMEOUT: return "bounded wait timed out";
+    case MOE_ERR_CUDA: return "CUDA runtime error";
+    case MOE_ERR_CAPACITY: return "receive capacity exceeded";
+    case MOE_ERR_BAD_ASSIST: return "assist_info / ep_recv_count do not match the routing";
+    default: return "unknown status";
+  }
+}
+
+}  // extern "C"

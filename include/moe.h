@@ -1,0 +1,186 @@
+/*
+ * moe.h - C ABI of the GB300 MoE token dispatch / combine library
+ * (libcrs_moe.so, built from combine_route_scan_gb300/csrc).
+ *
+ * The W ranks of an expert-parallel (EP) group are emulated as W partitions of
+ * one GPU's memory: every array carries a leading W axis, and a "remote put"
+ * from rank s to rank d is a store into partition d. One call handles all W
+ * ranks at once.
+ *
+ * Sources (web pages):
+ *   [DISP]  "aclnnMoeDistributeDispatchV4" (CANN API doc): 接口功能
+ *           (expandXOut = AllToAllV(X), optional quantisation first), 参数说明
+ *           (active masks, zero / copy / const expert id ranges, quantMode,
+ *           epRecvCountsOut and expandScalesOut shapes, value ranges), 约束说明
+ *           (deterministic; dispatch outputs go unchanged into combine; "/" is
+ *           integer division), the two-phase GetWorkspaceSize + execute
+ *           contract, 环境变量约束 (receive buffer of BS*W*min(L,K) rows).
+ *   [SHMEM] "双平面 MoE Combine 示例" (cann/shmem combine_doubleplane README):
+ *           功能说明 (combine inputs, check formula), 方案设计 (plane choice),
+ *           实现逻辑 (bounded bulk backlog, status-after-payload protocol).
+ *   [MEGA]  xLLM "MegaMoe" pull request: dispatch + expert FFN/activation +
+ *           combine in one operator.
+ *
+ * Conventions, for every entry point:
+ *   - Pointers named like arrays are DEVICE pointers (cudaMalloc or torch
+ *     memory) unless the comment says host. The caller owns every buffer; the
+ *     library never allocates, frees or keeps a pointer past the call.
+ *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy stream.
+ *     Every call only enqueues work and returns.
+ *   - Argument errors return at once, before anything is launched.
+ *   - Errors found on the device (bad expert id, 1D mask out of order, a
+ *     capacity overflow, inconsistent assist_info, a flag wait that timed out)
+ *     are recorded in the workspace's status word; read them with
+ *     moe_get_device_status. Outputs are unspecified after such an error.
+ *   - Rows of expand_x / assist_info / dynamic_scales / expand_scales at or
+ *     beyond ep_recv_count[d][L*W-1] are left untouched (their content is
+ *     unspecified and no one may depend on it, as [DISP] says).
+ *   - Results do not depend on thread timing: same inputs, same bytes.
+ */
+#ifndef CRS_MOE_H
+#define CRS_MOE_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  MOE_OK = 0,
+  MOE_ERR_INVALID_ARG = 1,   /* a value out of the ranges below, a NULL array, misalignment */
+  MOE_ERR_UNSUPPORTED = 2,   /* const experts, quant_mode other than 0/2, int32 x with quant */
+  MOE_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than moe_get_workspace_size */
+  MOE_ERR_BAD_EXPERT_ID = 4, /* an active id outside [0, E+Z+C), or a routed id twice in a token */
+  MOE_ERR_MASK_ORDER = 5,    /* a 1D active mask with a true after a false */
+  MOE_ERR_TIMEOUT = 6,       /* a bounded flag / barrier wait ran out */
+  MOE_ERR_CUDA = 7,          /* a CUDA runtime call failed */
+  MOE_ERR_CAPACITY = 8,      /* a rank would receive more than A rows */
+  MOE_ERR_BAD_ASSIST = 9,    /* assist_info / ep_recv_count do not match the routing */
+} moe_status_t;
+
+typedef enum { MOE_I32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype_t;
+
+/* Which plane carries each (local expert, source) segment ([SHMEM] 方案设计). */
+enum {
+  MOE_PLANE_RULE = 0,        /* the page's rule: bulk iff remote, non-empty, >= bulk_min_bytes
+                                and larger than the writer's mean remote segment */
+  MOE_PLANE_STORES_ONLY = 1, /* every segment by SM stores (the classic single plane) */
+  MOE_PLANE_BULK_ALL = 2,    /* every non-empty remote segment by TMA bulk copies */
+};
+
+/* How moe_combine runs. */
+enum {
+  MOE_COMBINE_GATHER = 0,    /* one pass: gather each token's K expert rows and reduce */
+  MOE_COMBINE_TWO_PHASE = 1, /* [SHMEM]: put expert rows into the source's window with
+                                per-pick ready flags, then wait on the flags and reduce */
+  MOE_COMBINE_PUT_ONLY = 2,  /* phase 1 of TWO_PHASE alone (the page's comm_only);
+                                x_out is not written */
+};
+
+typedef struct {
+  int32_t ep_world_size;    /* W: EP ranks, [2, 768] */
+  int32_t bs;               /* BS: tokens per rank, >= 0, W*bs*topk < 2^31 */
+  int32_t h;                /* H: hidden size, > 0 */
+  int32_t topk;             /* K: picks per token, [1, 32] */
+  int32_t moe_expert_num;   /* E: routed experts, (0, 1024], E % W == 0; L = E / W
+                               experts live on each rank, expert e on rank e / L */
+  int32_t zero_expert_num;  /* Z >= 0: ids [E, E+Z) contribute nothing */
+  int32_t copy_expert_num;  /* C >= 0: ids [E+Z, E+Z+C) contribute w * x */
+  int32_t const_expert_num; /* must be 0 (the page gives no formula) */
+  int32_t quant_mode;       /* 0: none; 2: per-token dynamic int8 */
+  int32_t mask_kind;        /* 0: no mask; 1: (BS,) per token; 2: (BS, K) per pick */
+  int32_t x_dtype;          /* moe_dtype_t of x, expand_x (quant 0), expert_out, x_out;
+                               expert_scales are int32 for MOE_I32, fp32 otherwise */
+  int32_t plane_policy;     /* MOE_PLANE_* */
+  int64_t bulk_min_bytes;   /* bulk-plane size threshold; the page's "2MB" = 2097152 */
+  int32_t combine_mode;     /* MOE_COMBINE_* */
+  int32_t wait_timeout_us;  /* bound on every flag wait (two-phase combine), > 0 */
+  int32_t ffn_intermediate; /* I for moe_dispatch_ffn_combine, else 0 */
+  int32_t reserved0;        /* must be 0 */
+  void* const* prof_events; /* optional host array {start, stop} of cudaEvent_t: recorded
+                               on `stream` around the call's main kernel (scatter for
+                               dispatch, reduce for combine); NULL for none */
+} moe_config_t;
+
+/* Workspace bytes for `cfg` (first phase of [DISP]'s two-phase contract), and
+ * the per-rank receive capacity A = bs * W * min(L, K) ([DISP] 环境变量约束).
+ * Either output pointer (host) may be NULL. Validates cfg. */
+moe_status_t moe_get_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, int64_t* rows_per_rank);
+
+/* Clears the workspace header (status word, call counters, flag epoch).
+ * Required once before the first call that uses a workspace, and after
+ * reallocating it. Enqueued on `stream`. */
+moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch ([DISP] 接口功能: expandXOut = AllToAllV(X), quantised first for quantMode 2).
+ *
+ * Inputs (device, row-major, leading W axis):
+ *   x             [W][bs][h] of x_dtype
+ *   expert_ids    [W][bs][K] int32
+ *   active_mask   NULL, [W][bs] (mask_kind 1) or [W][bs][K] (mask_kind 2) bytes, 0 = false
+ *   expert_scales NULL or [W][bs][K] (int32 / fp32); needed iff expand_scales != NULL
+ * Outputs (device):
+ *   expand_x       [W][A][h]: rank d's received rows, grouped by local expert, then
+ *                  by source rank, then in (token, k) order; int8 for quant_mode 2
+ *   dynamic_scales [W][A] fp32, one per row (quant_mode 2; else may be NULL)
+ *   assist_info    [W][A][3] int32: (src_rank, src_token, src_topk) of each row
+ *   ep_recv_count  [W][L*W] int32: running row count over segments le*W + s of rank d
+ *   expand_scales  NULL or [W][A]: the row's weight expert_scales[s][t][k]
+ *   seg_plane      NULL or [W][L*W] uint8: 1 where the segment went by bulk copies
+ * Alignment: every array 16-byte aligned; rows use TMA only when h*elem bytes
+ * (and h for int8 output) are multiples of 16, else plain stores carry all rows. */
+moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
+                          const uint8_t* active_mask, const void* expert_scales, void* expand_x,
+                          float* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                          void* expand_scales, uint8_t* seg_plane, void* ws, size_t ws_bytes,
+                          void* stream);
+
+/* Combine ([SHMEM] 功能说明, check formula):
+ *   x_out[s][t] = sum over k ascending of expert_scales[s][t][k] * y_k
+ * with y_k the expert-output row that assist_info names for pick (s,t,k), x[s][t]
+ * for a copy expert, nothing for a zero expert or an inactive pick; fp32
+ * accumulation by fused multiply-add, rounded to nearest-even into x_dtype
+ * (int32: the exact sum modulo 2^32). A token with no contribution gets zeros.
+ *
+ *   expert_out    [W][A][h] of x_dtype (the expert outputs at dispatch's rows)
+ *   assist_info, ep_recv_count: dispatch's outputs, unchanged ([DISP] 接口配套约束)
+ *   expert_ids, expert_scales, active_mask: as given to dispatch
+ *   x             [W][bs][h]; needed iff copy_expert_num > 0 (else may be NULL)
+ *   x_out         [W][bs][h] of x_dtype (not written for MOE_COMBINE_PUT_ONLY)
+ *   seg_plane     NULL or [W][L*W] uint8: two-phase plane per segment (writer = rank d)
+ * combine_mode selects the gather or the two-phase window protocol; both give
+ * the same bytes. */
+moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const int32_t* assist_info,
+                         const int32_t* ep_recv_count, const int32_t* expert_ids,
+                         const void* expert_scales, const uint8_t* active_mask, const void* x,
+                         void* x_out, uint8_t* seg_plane, void* ws, size_t ws_bytes, void* stream);
+
+/* Dispatch -> per-expert SwiGLU FFN -> combine in one call ([MEGA] 背景与目标 and
+ * 依赖关系: one operator for dispatch, expert FFN with activation, and combine;
+ * intermediate_hidden = 512 on A3):
+ *   x_out[s][t] = sum_k w_k * ( silu(x Wg[e]) * (x Wu[e]) ) Wd[e]   (routed picks)
+ *               + sum_k w_k * x                                       (copy experts)
+ * bf16 only, quant_mode 0. The FFN runs on tcgen05 tensor cores with fp32
+ * accumulation; the intermediate and expert outputs are rounded to bf16.
+ *   w_gate, w_up [E][h][I] bf16, w_down [E][I][h] bf16; expert_scales fp32.
+ * The workspace holds the dispatch outputs and intermediates (size from
+ * moe_get_workspace_size with ffn_intermediate = I). */
+moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
+                                      const uint8_t* active_mask, const float* expert_scales,
+                                      const void* w_gate, const void* w_up, const void* w_down,
+                                      void* x_out, void* ws, size_t ws_bytes, void* stream);
+
+/* Synchronises `stream`, returns in *status (host) the first device-side error
+ * recorded in the workspace since the last read (MOE_OK if none), and clears it. */
+moe_status_t moe_get_device_status(void* ws, void* stream, int32_t* status);
+
+/* Static text for a status code. */
+const char* moe_status_string(int32_t status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* CRS_MOE_H */

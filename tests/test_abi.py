@@ -1,0 +1,109 @@
+"""The C ABI without a GPU: the library builds, loads, exports every symbol
+include/moe.h declares, and its host-side validation and workspace query
+(which touch no CUDA call) behave as documented."""
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    from combine_route_scan_gb300 import build
+    build.build()
+    from combine_route_scan_gb300 import moe
+    return moe
+
+
+def declared_functions():
+    with open(os.path.join(ROOT, "include", "moe.h")) as f:
+        text = f.read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"^\s*(?:moe_status_t|const char\*)\s+(moe_\w+)\s*\(", text, flags=re.M)))
+
+
+def test_header_declares_the_abi():
+    assert declared_functions() == sorted(
+        ["moe_get_workspace_size", "moe_workspace_init", "moe_dispatch", "moe_combine",
+         "moe_dispatch_ffn_combine", "moe_get_device_status", "moe_status_string"])
+
+
+def test_library_exports_every_declared_symbol(lib):
+    L = lib.lib()
+    for name in declared_functions():
+        assert hasattr(L, name), name
+    assert set(lib.EXPORTS) == set(declared_functions())
+
+
+def test_config_struct_layout_matches_header(lib):
+    # 17 int32/int64 fields plus a pointer: offsets follow C layout rules
+    assert ctypes.sizeof(lib.MoeConfig) == 80
+    assert lib.MoeConfig.bulk_min_bytes.offset == 48
+    assert lib.MoeConfig.prof_events.offset == 72
+
+
+def test_workspace_query_and_capacity(lib):
+    import torch
+    cfg = lib.config(16, 256, 7168, 8, 256, torch.bfloat16, zero_expert_num=4, copy_expert_num=4, mask_kind=2)
+    n, A = lib.workspace_size(cfg)
+    assert A == 256 * 16 * min(16, 8)
+    assert n > 0 and n % 256 == 0
+    cfg2 = lib.config(16, 256, 7168, 8, 256, torch.bfloat16, combine_mode=lib.COMBINE_TWO_PHASE)
+    n2, _ = lib.workspace_size(cfg2)
+    # the two-phase window holds one row per pick
+    assert n2 - n >= 16 * 256 * 8 * 7168 * 2
+    cfg3 = lib.config(2, 8, 16, 2, 4, torch.int32)
+    assert lib.workspace_size(cfg3)[1] == 8 * 2 * 2
+
+
+@pytest.mark.parametrize("field,value,code", [
+    ("ep_world_size", 1, "INVALID_ARG"),
+    ("ep_world_size", 769, "INVALID_ARG"),
+    ("moe_expert_num", 0, "INVALID_ARG"),
+    ("moe_expert_num", 1025, "INVALID_ARG"),
+    ("moe_expert_num", 63, "INVALID_ARG"),
+    ("topk", 0, "INVALID_ARG"),
+    ("topk", 33, "INVALID_ARG"),
+    ("h", 0, "INVALID_ARG"),
+    ("bs", -1, "INVALID_ARG"),
+    ("const_expert_num", 1, "UNSUPPORTED"),
+    ("quant_mode", 1, "UNSUPPORTED"),
+    ("quant_mode", 3, "UNSUPPORTED"),
+    ("mask_kind", 3, "INVALID_ARG"),
+    ("x_dtype", 7, "INVALID_ARG"),
+    ("plane_policy", 3, "INVALID_ARG"),
+    ("combine_mode", 3, "INVALID_ARG"),
+    ("wait_timeout_us", 0, "INVALID_ARG"),
+    ("bulk_min_bytes", -1, "INVALID_ARG"),
+])
+def test_host_validation(lib, field, value, code):
+    import torch
+    cfg = lib.config(8, 32, 7168, 8, 64, torch.float16)
+    setattr(cfg, field, value)
+    with pytest.raises(lib.MoeError) as ei:
+        lib.workspace_size(cfg)
+    assert ei.value.name == code
+
+
+def test_quant_with_int32_is_rejected(lib):
+    import torch
+    cfg = lib.config(8, 32, 7168, 8, 64, torch.int32, quant_mode=2)
+    with pytest.raises(lib.MoeError) as ei:
+        lib.workspace_size(cfg)
+    assert ei.value.name == "UNSUPPORTED"
+
+
+def test_status_strings(lib):
+    for code in range(10):
+        assert lib.status_string(code)
+
+
+def test_binding_refuses_cpu_tensors(lib):
+    import torch
+    cfg = lib.config(2, 8, 16, 2, 4, torch.int32)
+    x = torch.zeros(2, 8, 16, dtype=torch.int32)
+    with pytest.raises(ValueError):
+        lib.dispatch(cfg, x, x, None, None, x, None, x, x, ws=x)

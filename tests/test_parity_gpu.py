@@ -1,0 +1,229 @@
+"""CUDA dispatch / combine against the CPU oracle, element by element.
+
+Integer, index, count and int8 outputs must match bit for bit; float combine
+outputs within max |gpu - oracle| <= 1e-3 * max |oracle|. The kernels fix the
+fp32 accumulation order (k ascending, fused multiply-add), so the float
+outputs are also checked for bit equality.
+"""
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import gpu_harness as H
+    from combine_route_scan_gb300 import moe as M
+    from combine_route_scan_gb300 import build as B
+    B.build()
+
+SMALL = ["w2_bs8_h16_k2_e4_i32", "w8_bs8_h16_k2_e64_i32", "w8_bs8_h16_k2_e64_f16", "w2_bs8_h256_k2_e4_i32"]
+FULL = ["w8_bs32_h7168_k8_e64_f16", "w8_bs32_h7168_k8_e64_f16_q2", "w8_bs32_h7168_k8_e64_i32",
+        "w16_bs256_h7168_k8_e256_bf16_zipf", "w8_bs64_h2048_k8_e128_bf16_ffn"]
+
+
+def run_and_compare(wl, inp=None, plane_policy=0, bulk_min_bytes=O.DEFAULT_BULK_MIN_BYTES, exact_float=True):
+    inp = WL.make_inputs(wl) if inp is None else inp
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    got, ws, _ = H.gpu_dispatch(wl, dev, plane_policy=plane_policy, bulk_min_bytes=bulk_min_bytes)
+    plane_ref = O.dispatch_plane(wl, ref["ep_recv_count"], bulk_min_bytes) if plane_policy == 0 else None
+    if plane_policy == 0 and not _tma_rows(wl):
+        plane_ref = np.zeros_like(ref["ep_recv_count"], dtype=np.uint8)
+    H.compare_dispatch(wl, got, ref, plane_ref)
+    err = None
+    if wl.quant_mode == 0:
+        x_out, _, _ = H.gpu_combine(wl, dev, got["expand_x"], got["assist_info"], got["ep_recv_count"])
+        x_ref = O.combine(wl, ref["expand_x"], ref["assist_info"], ref["ep_recv_count"], inp)
+        got_out = H.to_host(x_out)
+        err = H.compare_combine(wl, got_out, x_ref)
+        if exact_float:
+            assert np.array_equal(got_out.view(np.uint8), x_ref.view(np.uint8)), "combine bytes"
+    return got, ref, err
+
+
+def _tma_rows(wl):
+    row_in = wl.h * wl.es
+    row_out = wl.h if wl.quant_mode == 2 else row_in
+    return row_in % 16 == 0 and row_out % 16 == 0
+
+
+@pytest.mark.parametrize("name", SMALL)
+@pytest.mark.parametrize("plane_policy", [0, 1, 2])
+def test_small_workloads(name, plane_policy):
+    run_and_compare(WL.WORKLOADS[name], plane_policy=plane_policy)
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_random_small(seed):
+    rng = np.random.default_rng(500 + seed)
+    dt = [WL.X_INT32, WL.X_FP16, WL.X_BF16][seed % 3]
+    wl = WL.small_random_workload(rng, x_dtype=dt, max_w=6, max_bs=12)
+    run_and_compare(wl, plane_policy=seed % 3, bulk_min_bytes=0 if seed % 2 else O.DEFAULT_BULK_MIN_BYTES)
+
+
+@pytest.mark.parametrize("h,dt,q", [(12, WL.X_FP16, 0), (20, WL.X_BF16, 0), (3, WL.X_INT32, 0),
+                                    (24, WL.X_FP16, 2), (40, WL.X_BF16, 2), (5, WL.X_BF16, 2)])
+def test_rows_not_multiple_of_16_bytes(h, dt, q):
+    wl = WL.Workload(f"ragged_h{h}", 4, 9, h, 3, 8, dt, zero_expert_num=1, copy_expert_num=1, mask_kind=2,
+                     special_p=0.2, mask_false_p=0.2, quant_mode=q, seed=h)
+    run_and_compare(wl)
+
+
+@pytest.mark.parametrize("name", FULL)
+def test_full_size_workloads(name):
+    got, ref, err = run_and_compare(WL.WORKLOADS[name])
+    if name.endswith("_zipf"):
+        # the skewed routing really sends some segments by the bulk plane
+        assert H.to_host(got["seg_plane"]).sum() > 0
+
+
+def test_planes_give_identical_bytes():
+    """The page requires the two-plane version to give the same outputs as the
+    single-plane one: rule, stores only and bulk for all remote segments."""
+    wl = WL.WORKLOADS["w16_bs256_h7168_k8_e256_bf16_zipf"]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    outs = []
+    for pol in (0, 1, 2):
+        got, _, _ = H.gpu_dispatch(wl, dev, plane_policy=pol)
+        outs.append(got)
+    ep = H.to_host(outs[0]["ep_recv_count"])
+    for other in outs[1:]:
+        assert np.array_equal(H.to_host(other["ep_recv_count"]), ep)
+        for d in range(wl.ep_world_size):
+            n = int(ep[d, -1])
+            assert torch.equal(other["expand_x"][d, :n], outs[0]["expand_x"][d, :n])
+            assert torch.equal(other["assist_info"][d, :n], outs[0]["assist_info"][d, :n])
+    assert H.to_host(outs[1]["seg_plane"]).sum() == 0
+    assert H.to_host(outs[2]["seg_plane"]).sum() > H.to_host(outs[0]["seg_plane"]).sum() > 0
+
+
+def test_quant_q2_small_with_ties():
+    """quantMode 2 on rows built to hit exact .5 ties (amax 127, scale 1)."""
+    wl = WL.Workload("q2_ties", 2, 16, 64, 2, 4, WL.X_FP16, quant_mode=2, seed=3)
+    inp = WL.make_inputs(wl)
+    rng = np.random.default_rng(4)
+    x = (rng.integers(-254, 255, size=inp["x"].shape) / 2.0).astype(np.float16)
+    x[..., 0] = 127.0
+    x[0, 3] = 0.0  # an all-zero token: scale 0, q 0
+    inp["x"] = x
+    run_and_compare(wl, inp)
+
+
+def test_determinism_same_bytes():
+    wl = WL.WORKLOADS["w16_bs256_h7168_k8_e256_bf16_zipf"]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    a, ws, _ = H.gpu_dispatch(wl, dev)
+    b, _, _ = H.gpu_dispatch(wl, dev, ws=ws)
+    ep = H.to_host(a["ep_recv_count"])
+    assert np.array_equal(ep, H.to_host(b["ep_recv_count"]))
+    for d in range(wl.ep_world_size):
+        n = int(ep[d, -1])
+        assert torch.equal(a["expand_x"][d, :n], b["expand_x"][d, :n])
+    xa, _, _ = H.gpu_combine(wl, dev, a["expand_x"], a["assist_info"], a["ep_recv_count"])
+    xb, _, _ = H.gpu_combine(wl, dev, a["expand_x"], a["assist_info"], a["ep_recv_count"])
+    assert torch.equal(xa, xb)
+
+
+def test_empty_batch():
+    wl = WL.Workload("empty", 4, 0, 64, 2, 8, WL.X_FP16)
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    assert H.to_host(got["ep_recv_count"]).sum() == 0
+    x_out, _, _ = H.gpu_combine(wl, dev, got["expand_x"], got["assist_info"], got["ep_recv_count"])
+    assert x_out.numel() == 0
+
+
+def test_all_masked_and_all_special():
+    wl = WL.Workload("masked", 4, 8, 32, 2, 8, WL.X_INT32, mask_kind=2, mask_false_p=1.0, seed=1)
+    got, ref, _ = run_and_compare(wl)
+    assert H.to_host(got["ep_recv_count"]).sum() == 0
+    wl = WL.Workload("special", 4, 8, 32, 2, 8, WL.X_BF16, zero_expert_num=1, copy_expert_num=2,
+                     special_p=1.0, seed=2)
+    got, ref, _ = run_and_compare(wl)
+    assert H.to_host(got["ep_recv_count"]).sum() == 0
+
+
+def test_one_expert_takes_everything():
+    """Every token routes to expert 0 (plus distinct others): one segment per
+    source holds the whole batch."""
+    wl = WL.Workload("hot", 8, 64, 1024, 2, 16, WL.X_FP16, seed=6)
+    inp = WL.make_inputs(wl)
+    ids = inp["expert_ids"]
+    ids[..., 0] = 0
+    ids[..., 1] = np.where(ids[..., 1] == 0, 1, ids[..., 1])
+    run_and_compare(wl, inp, bulk_min_bytes=64 * 1024)
+
+
+@pytest.mark.parametrize("W,E,bs,K,h", [(64, 1024, 16, 8, 64), (768, 768, 2, 1, 16), (32, 256, 40, 16, 128)])
+def test_wide_configurations(W, E, bs, K, h):
+    wl = WL.Workload(f"wide_w{W}", W, bs, h, K, E, WL.X_BF16, zero_expert_num=2, copy_expert_num=2,
+                     mask_kind=1, special_p=0.1, seed=W)
+    run_and_compare(wl)
+
+
+def test_one_dimensional_mask():
+    wl = WL.Workload("mask1d", 8, 32, 256, 4, 32, WL.X_FP16, mask_kind=1, copy_expert_num=2, special_p=0.1, seed=8)
+    run_and_compare(wl)
+
+
+# ----------------------------------------------------------------- errors
+
+def _status_of_dispatch(wl, inp):
+    dev = H.device_inputs(wl, inp)
+    _, _, st = H.gpu_dispatch(wl, dev, check_status=False)
+    return M.STATUS[st]
+
+
+def test_device_errors_match_oracle():
+    base = WL.Workload("err", 2, 4, 16, 2, 4, WL.X_INT32, zero_expert_num=1, copy_expert_num=1)
+    inp = WL.make_inputs(base)
+    bad = dict(inp, expert_ids=inp["expert_ids"].copy())
+    bad["expert_ids"][1, 2, 1] = 6
+    assert _status_of_dispatch(base, bad) == "BAD_EXPERT_ID" == O.STATUS_NAMES[O.dispatch(base, bad, raise_on_error=False)["status"]]
+    bad["expert_ids"][1, 2, 1] = -3
+    assert _status_of_dispatch(base, bad) == "BAD_EXPERT_ID"
+    dup = dict(inp, expert_ids=inp["expert_ids"].copy())
+    dup["expert_ids"][0, 0, :] = 3
+    assert _status_of_dispatch(base, dup) == "BAD_EXPERT_ID"
+    m1 = base.with_(mask_kind=1)
+    badm = dict(inp, active_mask=np.array([[1, 0, 1, 0], [1, 1, 1, 1]], dtype=np.uint8))
+    assert _status_of_dispatch(m1, badm) == "MASK_ORDER" == O.STATUS_NAMES[O.dispatch(m1, badm, raise_on_error=False)["status"]]
+    # the status word is cleared by reading it: a good call afterwards is OK
+    assert _status_of_dispatch(base, inp) == "OK"
+
+
+def test_combine_detects_inconsistent_assist_info():
+    wl = WL.WORKLOADS["w8_bs8_h16_k2_e64_i32"]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    ai = got["assist_info"].clone()
+    ep = H.to_host(got["ep_recv_count"])
+    d = int(np.argmax(ep[:, -1]))
+    ai[d, 0, 1] = (ai[d, 0, 1] + 1) % wl.bs  # row 0 of rank d now names another token
+    _, st, _ = H.gpu_combine(wl, dev, got["expand_x"], ai, got["ep_recv_count"], check_status=False)
+    assert M.STATUS[st] == "BAD_ASSIST"
+
+
+def test_host_argument_errors():
+    wl = WL.WORKLOADS["w2_bs8_h16_k2_e4_i32"]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    cfg = H.make_cfg(wl)
+    out = M.alloc_dispatch_outputs(cfg, torch.int32)
+    ws = M.alloc_workspace(cfg)
+    with pytest.raises(M.MoeError) as ei:
+        M.dispatch(cfg, dev["x"], dev["expert_ids"], None, dev["expert_scales"], out["expand_x"], None,
+                   out["assist_info"], out["ep_recv_count"], ws=ws[:64])
+    assert ei.value.name == "WORKSPACE"
+    with pytest.raises(M.MoeError) as ei:
+        M.dispatch(cfg, dev["x"], dev["expert_ids"], None, None, out["expand_x"], None,
+                   out["assist_info"], out["ep_recv_count"], expand_scales=out["expand_scales"], ws=ws)
+    assert ei.value.name == "INVALID_ARG"
