@@ -1,0 +1,462 @@
+#!/usr/bin/env python
+"""Dispatch + combine throughput of the GB300 MoE library.
+
+One step = one pass of the whole hot path over one batch: moe_dispatch (route +
+scatter, with expand_scales) then moe_combine (inverse map + gather reduce)
+with the identity expert (the expert output is expand_x), as in the
+combine_doubleplane example. Default workload: skewed (Zipf) routing, W=16
+emulated EP ranks, bs=256 tokens per rank, h=7168, topk 8, 256 experts plus 4
+zero and 4 copy experts, 2D active mask, bf16 data.
+
+Prints one JSON line. ``value`` is the algorithmic bytes of dispatch + combine
+moved per second (GB/s, whole job over all ranks); ``tokens_per_s`` and the
+fraction of the 8 TB/s HBM roofline ride along. ``--impl reference`` times the
+CPU oracle on the same workload instead (the reference arm).
+
+Multi-GPU (torchrun): every rank runs its own independent batch (the W
+emulated ranks live inside each GPU), no collective on the data path; weak
+scaling.
+"""
+from __future__ import annotations
+
+import argparse
+import hashlib
+import json
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+import numpy as np
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+import workloads as WL  # noqa: E402
+
+METRIC = "dispatch+combine GB/s and tokens/s on 1 GB300; fraction of 8 TB/s HBM roofline"
+DEFAULT_WORKLOAD = "w16_bs256_h7168_k8_e256_bf16_zipf"
+HBM_NOMINAL_GBPS = 8000.0
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBPS = 6800.0
+
+
+def parse_args():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=1000)
+    ap.add_argument("--warmup", type=int, default=20)
+    ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--plane-policy", type=int, default=0)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--e2e-steps", type=int, default=200)
+    return ap.parse_args()
+
+
+# ------------------------------------------------------------ accounting
+
+def pick_counts(wl: WL.Workload, inp: dict) -> dict:
+    """Routed picks P, copy picks, tokens with at least one routed pick."""
+    ids = inp["expert_ids"].astype(np.int64)
+    E, Z, C = wl.moe_expert_num, wl.zero_expert_num, wl.copy_expert_num
+    act = np.ones(ids.shape, dtype=bool)
+    m = inp.get("active_mask")
+    if m is not None:
+        act = np.broadcast_to(m.astype(bool)[..., None], ids.shape) if m.ndim == 2 else m.astype(bool)
+    routed = act & (ids >= 0) & (ids < E)
+    copy = act & (ids >= E + Z) & (ids < E + Z + C)
+    return {"P": int(routed.sum()), "copy": int(copy.sum()), "tok_routed": int(routed.any(-1).sum())}
+
+
+def algorithmic_bytes(wl: WL.Workload, inp: dict) -> dict:
+    """Bytes the method must move (inputs read once, outputs written once)."""
+    c = pick_counts(wl, inp)
+    W, bs, K, h = wl.ep_world_size, wl.bs, wl.topk, wl.h
+    L = wl.moe_expert_num // W
+    r_in = h * wl.es
+    r_out = h if wl.quant_mode == 2 else r_in
+    picks = W * bs * K
+    mask = 0 if inp.get("active_mask") is None else inp["active_mask"].size
+    ep = W * L * W * 4
+    P, Cp, Nt = c["P"], c["copy"], c["tok_routed"]
+    meta = P * (4 + 12 + 4) + (P * 4 if wl.quant_mode == 2 else 0)  # weights read; assist, expand_scales written
+    scatter = Nt * r_in + P * r_out + meta
+    dispatch = scatter + picks * 4 + mask + ep
+    reduce_ = P * r_in + Cp * r_in + picks * 8 + mask + W * bs * r_in
+    combine = reduce_ + P * 12 + ep
+    return {"dispatch": dispatch, "combine": combine, "scatter": scatter, "reduce": reduce_, **c}
+
+
+# ------------------------------------------------------------ clocks
+
+class ClockSampler:
+    """nvidia-smi clock / throttle-reason samples with host timestamps."""
+
+    FIELDS = ("clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.hw_slowdown,"
+              "clocks_event_reasons.hw_thermal_slowdown,clocks_event_reasons.sw_thermal_slowdown,"
+              "clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_id: str, period_ms: int = 50):
+        self.samples = []
+        self.proc = None
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", gpu_id, f"--query-gpu={self.FIELDS}", "--format=csv,noheader,nounits",
+                 f"-lms", str(period_ms)], stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            return
+        self.thread = threading.Thread(target=self._read, daemon=True)
+        self.thread.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 7:
+                continue
+            try:
+                self.samples.append((time.time(), float(parts[0]), float(parts[1]), parts[3:7]))
+            except ValueError:
+                continue
+
+    def stop(self):
+        if self.proc is not None:
+            self.proc.terminate()
+            try:
+                self.proc.wait(timeout=5)
+            except subprocess.TimeoutExpired:
+                self.proc.kill()
+
+    def summary(self, t0: float, t1: float) -> dict:
+        inside = [s for s in self.samples if t0 <= s[0] <= t1]
+        if not inside:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": [], "samples": 0}
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        reasons = sorted({names[i] for s in inside for i, v in enumerate(s[3]) if v.lower() == "active"})
+        return {"sm_mhz": statistics.median(s[1] for s in inside), "sm_max_mhz": max(s[2] for s in inside),
+                "reasons": reasons, "samples": len(inside)}
+
+
+def gpu_id_for_smi(local_rank: int) -> str:
+    import torch
+    try:
+        u = str(torch.cuda.get_device_properties(local_rank).uuid)
+        return u if u.startswith("GPU-") else "GPU-" + u
+    except Exception:
+        vis = os.environ.get("CUDA_VISIBLE_DEVICES")
+        return vis.split(",")[local_rank] if vis else str(local_rank)
+
+
+def measured_peaks() -> dict:
+    p = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(p):
+        with open(p) as f:
+            d = json.load(f)
+        return {"hbm_gbs": float(d["hbm_gbs"]), "source": "measured"}
+    return {"hbm_gbs": FALLBACK_HBM_GBPS, "source": "fallback"}
+
+
+def committed_traffic(kernel: str, workload: str):
+    """DRAM bytes per launch from the committed ncu summary, if it was taken on
+    the current kernel source (its hash is recorded beside the figure)."""
+    p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
+    if not os.path.exists(p):
+        return None
+    src = os.path.join(ROOT, "combine_route_scan_gb300", "csrc",
+                       {"scatter": "scatter.cu", "combine_reduce": "combine.cu"}[kernel])
+    with open(src, "rb") as f:
+        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    vals = {}
+    with open(p) as f:
+        for line in f:
+            if line.startswith("- ") and ":" in line:
+                k, v = line[2:].split(":", 1)
+                vals[k.strip()] = v.strip().strip("`")
+    if vals.get("source_sha256_16") != h or "dram_bytes_per_launch_full_size" not in vals:
+        return None
+    return float(vals["dram_bytes_per_launch_full_size"])
+
+
+# ------------------------------------------------------------ oracle timing
+
+def time_oracle(wl: WL.Workload, inp: dict, target_s: float, max_steps: int = 20):
+    from oracle import oracle as O
+    t = []
+    while True:
+        t0 = time.perf_counter()
+        d = O.dispatch(wl, inp)
+        O.combine(wl, d["expand_x"], d["assist_info"], d["ep_recv_count"], inp)
+        t.append(time.perf_counter() - t0)
+        if sum(t) >= target_s or len(t) >= max_steps:
+            return t
+
+
+def subsample(wl: WL.Workload, inp: dict, bs: int):
+    """The first `bs` tokens of every rank (same routing law, smaller batch)."""
+    sub = wl.with_(bs=bs, name=wl.name + f"_first{bs}")
+    out = {k: (None if v is None else np.ascontiguousarray(v[:, :bs])) for k, v in inp.items()
+           if k in ("x", "expert_ids", "active_mask", "expert_scales")}
+    return sub, out
+
+
+# ------------------------------------------------------------ distributed
+
+def dist_env():
+    rank = int(os.environ.get("RANK", "0"))
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return rank, world, local
+
+
+def run_reference(args):
+    rank, world, _ = dist_env()
+    if rank != 0:
+        return 0
+    wl = WL.WORKLOADS[args.workload]
+    inp = WL.make_inputs(wl)
+    from oracle import build as OB
+    OB.build()
+    # size each step so that warmup + steps end within about three minutes
+    one = time_oracle(wl, inp, 0.0, max_steps=1)[0]
+    budget = 180.0
+    n = max(1, args.steps + args.warmup)
+    bs = wl.bs
+    while bs > 1 and one * (bs / wl.bs) * n > budget:
+        bs //= 2
+    swl, sinp = (wl, inp) if bs == wl.bs else subsample(wl, inp, bs)
+    from oracle import oracle as O
+    times = []
+    for i in range(args.warmup + args.steps):
+        t0 = time.perf_counter()
+        d = O.dispatch(swl, sinp)
+        O.combine(swl, d["expand_x"], d["assist_info"], d["ep_recv_count"], sinp)
+        dt = time.perf_counter() - t0
+        if i >= args.warmup:
+            times.append(dt)
+    b = algorithmic_bytes(swl, sinp)
+    total = sum(times)
+    gbps = (b["dispatch"] + b["combine"]) * len(times) / total / 1e9
+    sample = (f"{len(times)} timed oracle steps of dispatch+combine over "
+              + ("the full batch" if bs == wl.bs else f"the first {bs} of {wl.bs} tokens of every rank"))
+    line = {
+        "impl": "reference", "metric": METRIC, "value": gbps, "unit": "GB/s", "n_gpus": args.gpus,
+        "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
+        "config": {"workload": wl.name, "sample_bs": bs},
+        "tokens_per_s": swl.ep_world_size * swl.bs * len(times) / total,
+        "cpu_baseline": {"value": gbps, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "e2e": {"value": gbps, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+    print(json.dumps(line))
+    return 0
+
+
+def run_ours(args):
+    import torch
+    import torch.distributed as dist
+
+    rank, world, local = dist_env()
+    if world > 1:
+        dist.init_process_group("nccl" if torch.cuda.is_available() else "gloo")
+    torch.cuda.set_device(local)
+    from combine_route_scan_gb300 import build as B
+    if rank == 0:
+        B.build()
+    if world > 1:
+        dist.barrier()
+    from combine_route_scan_gb300 import moe as M
+
+    wl = WL.WORKLOADS[args.workload]
+    inp = WL.make_inputs(wl, seed=wl.seed + rank)
+    acct = algorithmic_bytes(wl, inp)
+    step_bytes = acct["dispatch"] + acct["combine"]
+    tdt = {WL.X_INT32: torch.int32, WL.X_FP16: torch.float16, WL.X_BF16: torch.bfloat16}[wl.x_dtype]
+
+    def dev(a, bf=False):
+        if a is None:
+            return None
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if bf else t).cuda()
+
+    bf = wl.x_dtype == WL.X_BF16
+    x, ids = dev(inp["x"], bf), dev(inp["expert_ids"])
+    mask, scales = dev(inp.get("active_mask")), dev(inp["expert_scales"])
+    cfg = M.config(wl.ep_world_size, wl.bs, wl.h, wl.topk, wl.moe_expert_num, tdt,
+                   zero_expert_num=wl.zero_expert_num, copy_expert_num=wl.copy_expert_num,
+                   quant_mode=wl.quant_mode, mask_kind=wl.mask_kind, plane_policy=args.plane_policy)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, tdt)
+    x_out = torch.empty_like(x)
+    stream = torch.cuda.current_stream()
+
+    def step(cfg_d, cfg_c, xin=x, xo=x_out):
+        M.dispatch(cfg_d, xin, ids, mask, scales, out["expand_x"], out["dynamic_scales"], out["assist_info"],
+                   out["ep_recv_count"], out["expand_scales"], None, ws)
+        if wl.quant_mode == 0:
+            M.combine(cfg_c, out["expand_x"], out["assist_info"], out["ep_recv_count"], ids, scales, mask, xin,
+                      xo, None, ws)
+
+    for _ in range(max(3, args.warmup)):
+        step(cfg, cfg)
+    torch.cuda.synchronize()
+    st = M.get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {M.STATUS.get(st, st)} during warmup")
+
+    K = args.steps
+    ev_scatter = [M.ProfEvents() for _ in range(K)]
+    ev_reduce = [M.ProfEvents() for _ in range(K)]
+    cfg_s = [e.attach(cfg) for e in ev_scatter]
+    cfg_r = [e.attach(cfg) for e in ev_reduce]
+    t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+
+    sampler = ClockSampler(gpu_id_for_smi(local)) if rank == 0 else None
+    time.sleep(0.3 if sampler else 0)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    h0 = time.time()
+    t_start.record(stream)
+    for k in range(K):
+        step(cfg_s[k], cfg_r[k])
+    t_end.record(stream)
+    torch.cuda.synchronize()
+    if world > 1:
+        dist.barrier()
+    h1 = time.time()
+    total_ms = t_start.elapsed_time(t_end)
+    # keep the same load going until the clock record covers at least 1.5 s
+    h_ext = h1
+    if sampler and h1 - h0 < 1.5:
+        while time.time() - h0 < 1.5:
+            for _ in range(50):
+                step(cfg, cfg)
+            torch.cuda.synchronize()
+        h_ext = time.time()
+    if world > 1:
+        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    st = M.get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the timed region")
+
+    scatter_ms = statistics.mean(e.elapsed_ms() for e in ev_scatter)
+    reduce_ms = statistics.mean(e.elapsed_ms() for e in ev_reduce) if wl.quant_mode == 0 else 0.0
+    step_ms = total_ms / K
+    kernels = {"scatter": (scatter_ms, acct["scatter"]), "combine_reduce": (reduce_ms, acct["reduce"])}
+    dom = max(kernels, key=lambda k: kernels[k][0])
+    dom_ms, dom_bytes = kernels[dom]
+    peaks = measured_peaks()
+    achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
+    traffic = committed_traffic(dom, wl.name)
+
+    # end to end through the C ABI with host buffers: H2D of the step's inputs
+    # from pinned memory, dispatch, combine, D2H of x_out, every step
+    host = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).pin_memory())
+            for k, v in (("x", inp["x"].view(np.int16) if bf else inp["x"]), ("ids", inp["expert_ids"]),
+                         ("mask", inp.get("active_mask")), ("scales", inp["expert_scales"]))}
+    host_out = torch.empty(x_out.shape, dtype=x_out.dtype, pin_memory=True)
+    x_stage = torch.empty_like(x)
+    h2d = sum(v.numel() * v.element_size() for v in host.values() if v is not None)
+    d2h = host_out.numel() * host_out.element_size()
+
+    def e2e_step():
+        x_stage.view(torch.int16 if bf else x_stage.dtype).copy_(host["x"], non_blocking=True)
+        ids.copy_(host["ids"], non_blocking=True)
+        if mask is not None:
+            mask.copy_(host["mask"], non_blocking=True)
+        scales.copy_(host["scales"], non_blocking=True)
+        step(cfg, cfg, xin=x_stage)
+        host_out.copy_(x_out, non_blocking=True)
+
+    for _ in range(3):
+        e2e_step()
+    torch.cuda.synchronize()
+    Ke = max(1, min(args.e2e_steps, K))
+    e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    e0.record(stream)
+    for _ in range(Ke):
+        e2e_step()
+    e1.record(stream)
+    torch.cuda.synchronize()
+    e2e_ms = e0.elapsed_time(e1) / Ke
+    if world > 1:
+        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        e2e_ms = float(t.item())
+    st = M.get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the e2e region")
+
+    clocks = None
+    if sampler:
+        sampler.stop()
+        clocks = sampler.summary(h0, h_ext)
+        clocks["window_s"] = round(h_ext - h0, 3)
+        clocks["timed_region_s"] = round(h1 - h0, 3)
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline:
+        from oracle import build as OB
+        OB.build()
+        times = time_oracle(wl, inp, target_s=10.0, max_steps=10)
+        cpu = {"value": step_bytes / statistics.mean(times) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
+               "sample": f"{len(times)} full steps (dispatch+combine over all {wl.ep_world_size * wl.bs} tokens), "
+                         f"single-threaded C, mean {statistics.mean(times) * 1e3:.0f} ms/step"}
+
+    if rank != 0:
+        if world > 1:
+            dist.barrier()
+            dist.destroy_process_group()
+        return 0
+    ws_bytes = inp["x"].nbytes * 2 + acct["P"] * wl.h * wl.es * 2
+    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
+    tokens = world * wl.ep_world_size * wl.bs
+    line = {
+        "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
+        "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "bf16" if wl.x_dtype == WL.X_BF16 else ("fp16" if wl.x_dtype == WL.X_FP16 else "int32"),
+        "data": "synthetic",
+        "config": {"workload": wl.name, "ep_world_size": wl.ep_world_size, "bs": wl.bs, "h": wl.h,
+                   "topk": wl.topk, "moe_expert_num": wl.moe_expert_num, "zero_experts": wl.zero_expert_num,
+                   "copy_experts": wl.copy_expert_num, "mask": wl.mask_kind, "quant_mode": wl.quant_mode,
+                   "plane_policy": args.plane_policy, "combine": "gather",
+                   "l2": f"no flush: one step moves {step_bytes / 1e6:.0f} MB (> {L2_BYTES >> 20} MiB L2)",
+                   "accumulate": "fp32"},
+        "tokens_per_s": tokens * K / (total_ms * 1e-3),
+        "frac_of_8TBps": value / world / HBM_NOMINAL_GBPS,
+        "dispatch_bytes": acct["dispatch"], "combine_bytes": acct["combine"], "routed_picks": acct["P"],
+        "scatter_ms": scatter_ms, "combine_reduce_ms": reduce_ms,
+        "scatter_GBps": acct["scatter"] / (scatter_ms * 1e-3) / 1e9,
+        "combine_reduce_GBps": acct["reduce"] / (reduce_ms * 1e-3) / 1e9 if reduce_ms else None,
+        "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
+                     "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
+                     "algorithmic_bytes": dom_bytes, "peak_source": peaks["source"] + " copy bandwidth"},
+        "cpu_baseline": cpu,
+        "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
+                "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "gpu_launches": K * (4 if wl.quant_mode == 0 else 2),
+        "clocks": clocks,
+    }
+    print(json.dumps(line))
+    if world > 1:
+        dist.barrier()
+        dist.destroy_process_group()
+    return 0
+
+
+def main():
+    args = parse_args()
+    if args.impl == "reference":
+        return run_reference(args)
+    return run_ours(args)
+
+
+if __name__ == "__main__":
+    sys.exit(main())

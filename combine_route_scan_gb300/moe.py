@@ -119,6 +119,10 @@ class ProfEvents:
     def __init__(self):
         self.start = torch.cuda.Event(enable_timing=True)
         self.stop = torch.cuda.Event(enable_timing=True)
+        # torch creates its events on first record; record once so the handles
+        # exist (the library's later records replace these)
+        self.start.record()
+        self.stop.record()
         self._arr = (ctypes.c_void_p * 2)(self.start.cuda_event, self.stop.cuda_event)
 
     def attach(self, cfg: MoeConfig) -> MoeConfig:

@@ -98,6 +98,12 @@ WORKLOADS = {
         "w16_bs256_h7168_k8_e256_bf16_zipf", 16, 256, 7168, 8, 256, X_BF16,
         zero_expert_num=4, copy_expert_num=4, mask_kind=2, ids="zipf",
         special_p=0.05, mask_false_p=0.10, seed=3),
+    # the same routing law with half the batch (3.75 GB of receive buffers):
+    # used for full ncu captures, which must stay small on the device
+    "w16_bs128_h7168_k8_e256_bf16_zipf": Workload(
+        "w16_bs128_h7168_k8_e256_bf16_zipf", 16, 128, 7168, 8, 256, X_BF16,
+        zero_expert_num=4, copy_expert_num=4, mask_kind=2, ids="zipf",
+        special_p=0.05, mask_false_p=0.10, seed=3),
     # decode MoE layer with a SwiGLU expert FFN (intermediate 512)
     "w8_bs64_h2048_k8_e128_bf16_ffn": Workload(
         "w8_bs64_h2048_k8_e128_bf16_ffn", 8, 64, 2048, 8, 128, X_BF16,
