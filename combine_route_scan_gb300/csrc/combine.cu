@@ -20,7 +20,8 @@ namespace crs {
 
 constexpr int kInvThreads = 256;
 constexpr int kReduceThreads = 256;
-constexpr int kReduceGroup = 4;  // picks whose loads are in flight together
+constexpr int kReduceBatch = 8;  // picks whose loads are in flight together
+constexpr int kReduceVpl = 4;    // 16-byte vectors per lane per work item
 
 __global__ void __launch_bounds__(kInvThreads) combine_inverse_kernel(CombineParams p) {
   const Shape sh = p.sh;
@@ -137,64 +138,122 @@ __device__ __forceinline__ void build_reduce_table(const CombineParams& p, size_
   if (lane == 0) tab.n = __popc(m);
 }
 
-// One CTA per (token, chunk of vectors); each thread owns one 16-byte output
-// vector per pass and keeps kReduceGroup picks' loads in flight.
+// One warp per (token, chunk of 32*vpl vectors): lanes < K load the pick's id,
+// mask, weight and row in parallel, the warp compacts the contributing picks
+// (ascending k) into shared memory, then every lane reduces its 16-byte
+// vectors with up to kReduceBatch picks' loads in flight. No CTA-wide barrier.
+// The row map is checked against assist_info and ep_recv_count after the data
+// loads are issued (rows are bounds-checked against the capacity before any
+// read), so the check costs no round trip on the critical path.
 template <int DT>
-__global__ void __launch_bounds__(kReduceThreads) combine_reduce_kernel(CombineParams p, int chunks, int vpc) {
-  __shared__ ReduceTable tab;
-  const Shape sh = p.sh;
-  const size_t tau = blockIdx.x / chunks;
-  const int c = blockIdx.x % chunks;
-  pdl_wait();
-  pdl_launch_dependents();
-  if (threadIdx.x < 32) build_reduce_table(p, tau, tab);
-  __syncthreads();
-  const int n = tab.n;
-  const int nvec = sh.row_in / 16;
-  const int v0 = c * vpc, v1 = min(nvec, v0 + vpc);
-  uint8_t* out = static_cast<uint8_t*>(p.x_out) + tau * (size_t)sh.row_in;
-  for (int v = v0 + threadIdx.x; v < v1; v += kReduceThreads) {
-    const size_t off = (size_t)v * 16;
-    if constexpr (DT == MOE_I32) {
-      uint32_t acc[4] = {0u, 0u, 0u, 0u};
-      int j = 0;
-      for (; j + kReduceGroup <= n; j += kReduceGroup) {
-        int4 y[kReduceGroup];
+__device__ __forceinline__ void reduce_vector(const uint8_t* const* src, const uint32_t* w, int n, size_t off,
+                                              uint8_t* out) {
+  if constexpr (DT == MOE_I32) {
+    uint32_t acc[4] = {0u, 0u, 0u, 0u};
+    for (int j = 0; j < n; j += kReduceBatch) {
+      int4 y[kReduceBatch];
 #pragma unroll
-        for (int g = 0; g < kReduceGroup; ++g) y[g] = ld_nc_v4(tab.src[j + g] + off);
+      for (int g = 0; g < kReduceBatch; ++g)
+        if (j + g < n) y[g] = ld_nc_v4(src[j + g] + off);
 #pragma unroll
-        for (int g = 0; g < kReduceGroup; ++g) {
-          const uint32_t w = tab.w[j + g];
-          acc[0] += w * (uint32_t)y[g].x;
-          acc[1] += w * (uint32_t)y[g].y;
-          acc[2] += w * (uint32_t)y[g].z;
-          acc[3] += w * (uint32_t)y[g].w;
+      for (int g = 0; g < kReduceBatch; ++g) {
+        if (j + g < n) {
+          const uint32_t ww = w[j + g];
+          acc[0] += ww * (uint32_t)y[g].x;
+          acc[1] += ww * (uint32_t)y[g].y;
+          acc[2] += ww * (uint32_t)y[g].z;
+          acc[3] += ww * (uint32_t)y[g].w;
         }
       }
-      for (; j < n; ++j) {
-        const int4 y = ld_nc_v4(tab.src[j] + off);
-        const uint32_t w = tab.w[j];
-        acc[0] += w * (uint32_t)y.x;
-        acc[1] += w * (uint32_t)y.y;
-        acc[2] += w * (uint32_t)y.z;
-        acc[3] += w * (uint32_t)y.w;
-      }
-      st_v4(out + off, make_int4((int)acc[0], (int)acc[1], (int)acc[2], (int)acc[3]));
-    } else {
-      float acc[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) acc[i] = 0.f;
-      int j = 0;
-      for (; j + kReduceGroup <= n; j += kReduceGroup) {
-        int4 y[kReduceGroup];
-#pragma unroll
-        for (int g = 0; g < kReduceGroup; ++g) y[g] = ld_nc_v4(tab.src[j + g] + off);
-#pragma unroll
-        for (int g = 0; g < kReduceGroup; ++g) Vec<DT>::fma(acc, __uint_as_float(tab.w[j + g]), y[g]);
-      }
-      for (; j < n; ++j) Vec<DT>::fma(acc, __uint_as_float(tab.w[j]), ld_nc_v4(tab.src[j] + off));
-      st_v4(out + off, Vec<DT>::pack(acc));
     }
+    st_v4(out + off, make_int4((int)acc[0], (int)acc[1], (int)acc[2], (int)acc[3]));
+  } else {
+    float acc[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) acc[i] = 0.f;
+    for (int j = 0; j < n; j += kReduceBatch) {
+      int4 y[kReduceBatch];
+#pragma unroll
+      for (int g = 0; g < kReduceBatch; ++g)
+        if (j + g < n) y[g] = ld_nc_v4(src[j + g] + off);
+#pragma unroll
+      for (int g = 0; g < kReduceBatch; ++g)
+        if (j + g < n) Vec<DT>::fma(acc, __uint_as_float(w[j + g]), y[g]);
+    }
+    st_v4(out + off, Vec<DT>::pack(acc));
+  }
+}
+
+template <int DT>
+__global__ void __launch_bounds__(kReduceThreads) combine_reduce_kernel(CombineParams p, int chunks, int vpl) {
+  __shared__ const uint8_t* s_src[kReduceThreads / 32][32];
+  __shared__ uint32_t s_w[kReduceThreads / 32][32];
+  const Shape sh = p.sh;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long item = (long long)blockIdx.x * (kReduceThreads / 32) + warp;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (item >= (long long)sh.W * sh.bs * chunks) return;
+  const size_t tau = (size_t)(item / chunks);
+  const int c = (int)(item % chunks);
+
+  const uint8_t* src = nullptr;
+  uint32_t w = 0;
+  long long r = -1;
+  int d = -1;
+  if (lane < sh.K) {
+    const size_t pk = tau * sh.K + lane;
+    r = p.inv[pk];
+    w = reinterpret_cast<const uint32_t*>(p.scales)[pk];
+    const int cls = classify_pick(p.ids, p.mask, sh, tau, lane);
+    if (cls >= 0) {
+      d = cls / sh.L;
+      const long long row = r - (long long)d * sh.A;
+      if (row >= 0 && row < sh.A) {
+        src = static_cast<const uint8_t*>(p.expert_out) + r * (long long)sh.row_in;
+      } else {
+        set_error(p.status, MOE_ERR_BAD_ASSIST);
+      }
+    } else if (cls == kPickCopy) {
+      src = static_cast<const uint8_t*>(p.x) + tau * (size_t)sh.row_in;
+    } else if (cls == kPickBad) {
+      set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+    }
+  }
+  const uint32_t m = __ballot_sync(0xffffffffu, src != nullptr);
+  if (src) {
+    const int j = __popc(m & lanemask_lt());
+    s_src[warp][j] = src;
+    s_w[warp][j] = w;
+  }
+  __syncwarp();
+  const int n = __popc(m);
+
+  // deferred consistency check of the row map (loads issued now, compared last)
+  int a0 = 0, a1 = 0, a2 = 0, cnt = 0;
+  const bool check = d >= 0 && src != nullptr && c == 0;
+  if (check) {
+    const int32_t* a = p.assist + r * 3;
+    a0 = a[0];
+    a1 = a[1];
+    a2 = a[2];
+    const int LW = sh.L * sh.W;
+    cnt = p.ep_recv_count[(size_t)d * LW + LW - 1];
+  }
+
+  const int nvec = sh.row_in / 16;
+  uint8_t* out = static_cast<uint8_t*>(p.x_out) + tau * (size_t)sh.row_in;
+  const int v0 = c * 32 * vpl;
+  for (int i = 0; i < vpl; ++i) {
+    const int v = v0 + i * 32 + lane;
+    if (v >= nvec) break;
+    reduce_vector<DT>(s_src[warp], s_w[warp], n, (size_t)v * 16, out);
+  }
+
+  if (check) {
+    const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
+    if (a0 != s || a1 != t || a2 != lane || r - (long long)d * sh.A >= cnt)
+      set_error(p.status, MOE_ERR_BAD_ASSIST);
   }
 }
 
@@ -251,14 +310,15 @@ cudaError_t launch_combine_reduce(const CombineParams& p, cudaStream_t st, int n
     return cudaLaunchKernelEx(&L.cfg, combine_reduce_plain_kernel<MOE_BF16>, p);
   }
   const int nvec = sh.row_in / 16;
-  const int vpc = kReduceThreads;  // one vector per thread per chunk
-  const int chunks = (nvec + vpc - 1) / vpc;
-  const long long grid = n_tok * chunks;
+  const int vpl = kReduceVpl;
+  const int chunks = (nvec + 32 * vpl - 1) / (32 * vpl);
+  const long long items = n_tok * chunks;
+  const long long grid = (items + kReduceThreads / 32 - 1) / (kReduceThreads / 32);
   if (grid > 0x7fffffffLL) return cudaErrorInvalidConfiguration;
   PdlLaunch L(dim3((unsigned)grid), dim3(kReduceThreads), 0, st);
-  if (sh.x_dtype == MOE_I32) return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_I32>, p, chunks, vpc);
-  if (sh.x_dtype == MOE_F16) return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_F16>, p, chunks, vpc);
-  return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_BF16>, p, chunks, vpc);
+  if (sh.x_dtype == MOE_I32) return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_I32>, p, chunks, vpl);
+  if (sh.x_dtype == MOE_F16) return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_F16>, p, chunks, vpl);
+  return cudaLaunchKernelEx(&L.cfg, combine_reduce_kernel<MOE_BF16>, p, chunks, vpl);
 }
 
 }  // namespace crs

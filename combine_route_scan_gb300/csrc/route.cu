@@ -9,53 +9,41 @@
 // expand_x grouped by expert, ep_recv_count = running counts over the
 // (local_expert, src_rank) segments, the SDMA / MTE plane rule.
 //
-// One CTA per source rank s. Its picks (t, k) are split into contiguous slices,
-// one per warp, in (t, k) order. A warp walks its slice 32 picks at a time and
-// groups equal expert ids with __match_any_sync: the leader of each group adds
-// the group size to the warp's counter for that expert. A scan of the warp
-// counters over warps gives each warp its starting position per expert; a
-// second walk hands every pick base + (equal ids in earlier lanes). Positions
-// therefore follow (t, k) order exactly and no atomic decides any order.
+// One CTA per source rank s. A warp iteration covers floor(32/K) whole tokens
+// (lane = token-in-group * K + k), so the picks of a token sit in adjacent
+// lanes and a repeated routed id is found with K-1 register shuffles. Tokens
+// are split into contiguous runs, one per warp, in token order. A warp groups
+// equal expert ids with __match_any_sync: the leader of each group adds the
+// group size to the warp's counter for that expert. A scan of the warp counters
+// over warps gives each warp its starting position per expert; a second walk
+// hands every pick base + (equal ids in earlier lanes). Positions therefore
+// follow (t, k) order exactly and no atomic decides any order. The first walk
+// leaves each pick's expert id (or -1) in the rank array; the second walk
+// reads it back and overwrites it with the position.
 //
 // The last CTA to finish (completion counter in the workspace) scans the
-// W*L*W segment counts into ep_recv_count (inclusive) and segment offsets
-// (exclusive), per receiving rank.
+// W*L*W segment counts, tile by tile through shared memory, into ep_recv_count
+// (inclusive) and segment offsets (exclusive), per receiving rank.
 #include "common.cuh"
 
 namespace crs {
 
-constexpr int kRouteThreads = 512;
+constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
-
-// Routed expert of pick (tok, k), or -1 if it is not routed or repeats a routed
-// id of an earlier pick of the same token (an error that is recorded once, in
-// the first walk).
-__device__ __forceinline__ int routed_key(const RouteParams& p, size_t tok, int k, bool record) {
-  const int c = classify_pick(p.ids, p.mask, p.sh, tok, k);
-  if (c == kPickBad) {
-    if (record) set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
-    return -1;
-  }
-  if (c < 0) return -1;
-  for (int k2 = 0; k2 < k; ++k2) {
-    if (classify_pick(p.ids, p.mask, p.sh, tok, k2) == c) {
-      if (record) set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
-      return -1;
-    }
-  }
-  return c;
-}
+constexpr int kScanTile = 4096;
 
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
-  extern __shared__ int32_t wcnt[];  // [kRouteWarps][E], then tot[E]
+  extern __shared__ __align__(16) int32_t rsm[];  // wcnt [kRouteWarps][E], tot [E]; later the scan tiles
   __shared__ long long s_scan[32];
+  __shared__ long long s_total;
   __shared__ int s_last;
   const Shape sh = p.sh;
   const int s = blockIdx.x;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int E = sh.E, K = sh.K;
-  const int n = sh.bs * K;  // picks of source s
-  int32_t* tot = wcnt + kRouteWarps * E;
+  const int G = 32 / K;  // whole tokens per warp iteration
+  int32_t* wcnt = rsm;
+  int32_t* tot = rsm + kRouteWarps * E;
 
   pdl_wait();
   pdl_launch_dependents();
@@ -68,15 +56,33 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   }
   __syncthreads();
 
-  const int per_warp = (n + kRouteWarps - 1) / kRouteWarps;
-  const int lo = min(n, warp * per_warp), hi = min(n, lo + per_warp);
+  const int n_iter = (sh.bs + G - 1) / G;
+  const int per_warp = (n_iter + kRouteWarps - 1) / kRouteWarps;
+  const int it0 = min(n_iter, warp * per_warp), it1 = min(n_iter, it0 + per_warp);
   const size_t tok0 = (size_t)s * sh.bs;
+  const int tl = lane / K, k = lane - tl * K;
+  int32_t* keys = p.rank + tok0 * K;
 
-  // walk 1: per-warp counts per expert
-  for (int b = lo; b < hi; b += 32) {
-    const int pi = b + lane;
+  // walk 1: classify, reject repeated routed ids, count per warp and expert
+  for (int it = it0; it < it1; ++it) {
+    const int t = it * G + tl;
+    const bool valid = tl < G && t < sh.bs;
     int key = -1;
-    if (pi < hi) key = routed_key(p, tok0 + pi / K, pi % K, true);
+    if (valid) {
+      const int c = classify_pick(p.ids, p.mask, sh, tok0 + t, k);
+      if (c == kPickBad) set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+      key = c >= 0 ? c : -1;
+    }
+    bool dup = false;
+    for (int dd = 1; dd < K; ++dd) {
+      const int other = __shfl_up_sync(0xffffffffu, key, dd);
+      if (dd <= k && key >= 0 && other == key) dup = true;
+    }
+    if (dup) {
+      set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+      key = -1;
+    }
+    if (valid) keys[(size_t)t * K + k] = key;
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
     __syncwarp();
@@ -96,13 +102,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     p.cnt[(size_t)e * sh.W + s] = run;
     if (e / sh.L != s) remote += run;
   }
-  // block sum of `remote` (exclusive scan of the last thread + its own value)
   {
     const long long ex = block_exclusive_scan(remote, s_scan);
-    __shared__ long long s_remote;
-    if (tid == kRouteThreads - 1) s_remote = ex + remote;
+    if (tid == kRouteThreads - 1) s_total = ex + remote;
     __syncthreads();
-    remote = s_remote;
+    remote = s_total;
   }
 
   // plane of each segment sent by s (the page's rule with s as the writer):
@@ -128,17 +132,17 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   __syncthreads();
 
   // walk 2: position of every routed pick inside its segment
-  for (int b = lo; b < hi; b += 32) {
-    const int pi = b + lane;
-    int key = -1;
-    if (pi < hi) key = routed_key(p, tok0 + pi / K, pi % K, false);
+  for (int it = it0; it < it1; ++it) {
+    const int t = it * G + tl;
+    const bool valid = tl < G && t < sh.bs;
+    const int key = valid ? keys[(size_t)t * K + k] : -1;
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     int r = -1;
     if (key >= 0) r = wcnt[warp * E + key] + __popc(peers & lanemask_lt());
     __syncwarp();
     if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
     __syncwarp();
-    if (pi < hi) p.rank[tok0 * K + pi] = r;
+    if (valid) keys[(size_t)t * K + k] = r;
   }
 
   // the last CTA turns the counts of all sources into offsets
@@ -154,40 +158,59 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
 
   const int LW = sh.L * sh.W;
   const int N = sh.W * LW;  // == E * W, indexed g = e*W + s = d*LW + le*W + s
-  const int chunk = (N + kRouteThreads - 1) / kRouteThreads;
-  const int j0 = min(N, tid * chunk), j1 = min(N, j0 + chunk);
-  long long local = 0;
-  for (int j = j0; j < j1; ++j) local += __ldcg(p.cnt + j);
-  const long long off = block_exclusive_scan(local, s_scan);
-  long long* pstart = reinterpret_cast<long long*>(wcnt);  // [W] prefix at each rank's start
-  long long run = off;
-  for (int j = j0; j < j1; ++j) {
-    if (j % LW == 0) pstart[j / LW] = run;
-    run += __ldcg(p.cnt + j);
-  }
-  __syncthreads();
-  run = off;
-  for (int j = j0; j < j1; ++j) {
-    const int c = __ldcg(p.cnt + j);
-    const long long before = run - pstart[j / LW];
-    run += c;
-    p.base[j] = (int32_t)before;
-    p.ep_recv_count[j] = (int32_t)(before + c);
-    if ((j + 1) % LW == 0 && before + c > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
+  long long* pstart = reinterpret_cast<long long*>(rsm);  // [W] prefix at each rank's start
+  int32_t* tile = reinterpret_cast<int32_t*>(pstart + sh.W);
+  long long carry = 0;
+  for (int t0 = 0; t0 < N; t0 += kScanTile) {
+    const int n = min(kScanTile, N - t0);
+    for (int j = tid; j < n; j += kRouteThreads) tile[j] = __ldcg(p.cnt + t0 + j);
+    __syncthreads();
+    const int chunk = (n + kRouteThreads - 1) / kRouteThreads;
+    const int j0 = min(n, tid * chunk), j1 = min(n, j0 + chunk);
+    long long local = 0;
+    for (int j = j0; j < j1; ++j) local += tile[j];
+    const long long ex = block_exclusive_scan(local, s_scan);
+    const long long off = carry + ex;
+    long long run = off;
+    for (int j = j0; j < j1; ++j) {
+      if ((t0 + j) % LW == 0) pstart[(t0 + j) / LW] = run;
+      run += tile[j];
+    }
+    if (tid == kRouteThreads - 1) s_total = ex + local;
+    __syncthreads();
+    run = off;
+    for (int j = j0; j < j1; ++j) {
+      const int g = t0 + j;
+      const int c = tile[j];
+      const long long before = run - pstart[g / LW];
+      run += c;
+      p.base[g] = (int32_t)before;
+      p.ep_recv_count[g] = (int32_t)(before + c);
+      if ((g + 1) % LW == 0 && before + c > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
+    }
+    carry += s_total;
+    __syncthreads();
   }
   if (tid == 0) *p.done = 0;  // ready for the next call (stream order)
 }
 
+static size_t route_smem(const Shape& sh) {
+  const size_t walk = (size_t)(kRouteWarps + 1) * sh.E * sizeof(int32_t);
+  const size_t scan = (size_t)sh.W * sizeof(long long) + kScanTile * sizeof(int32_t);
+  return walk > scan ? walk : scan;
+}
+
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st) {
-  const size_t smem = (size_t)(kRouteWarps + 1) * p.sh.E * sizeof(int32_t);
-  static bool attr_set[64] = {};
+  if (p.sh.K > 32) return cudaErrorInvalidValue;
+  const size_t smem = route_smem(p.sh);
+  static size_t attr_bytes[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
-  if (dev < 64 && !attr_set[dev]) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         (kRouteWarps + 1) * 1024 * (int)sizeof(int32_t));
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if (attr_bytes[dev] < smem) {
+    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
-    attr_set[dev] = true;
+    attr_bytes[dev] = smem;
   }
   PdlLaunch L(dim3(p.sh.W), dim3(kRouteThreads), smem, st);
   return cudaLaunchKernelEx(&L.cfg, route_kernel, p);
