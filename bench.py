@@ -353,6 +353,44 @@ def run_ours(args):
     achieved = dom_bytes / (dom_ms * 1e-3) / 1e9
     traffic = committed_traffic(dom, wl.name)
 
+    # the page's split of the two-phase combine: full_op (put + flags + wait +
+    # reduce) and comm_only (put + flags), timed on their own workspace
+    two_phase = None
+    if wl.quant_mode == 0 and wl.h * wl.es % 16 == 0:
+        cfg_tp = M.MoeConfig.from_buffer_copy(cfg)
+        cfg_tp.combine_mode = M.COMBINE_TWO_PHASE
+        cfg_put = M.MoeConfig.from_buffer_copy(cfg)
+        cfg_put.combine_mode = M.COMBINE_PUT_ONLY
+        ws_tp = M.alloc_workspace(cfg_tp)
+        x_tp = torch.empty_like(x)
+
+        def tp_call(c):
+            M.combine(c, out["expand_x"], out["assist_info"], out["ep_recv_count"], ids, scales, mask, x, x_tp,
+                      None, ws_tp)
+
+        Kt = max(1, min(K, 200))
+        res = {}
+        for name, c in (("full_op", cfg_tp), ("comm_only", cfg_put)):
+            for _ in range(3):
+                tp_call(c)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for _ in range(Kt):
+                tp_call(c)
+            b.record(stream)
+            torch.cuda.synchronize()
+            res[name] = a.elapsed_time(b) / Kt
+        st = M.get_device_status(ws_tp)
+        if st != 0:
+            raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the two-phase combine")
+        put_bytes = 2 * acct["P"] * wl.h * wl.es
+        two_phase = {"full_op_ms": res["full_op"], "comm_only_ms": res["comm_only"],
+                     "full_op_GBps": acct["combine"] / (res["full_op"] * 1e-3) / 1e9,
+                     "comm_only_GBps": put_bytes / (res["comm_only"] * 1e-3) / 1e9,
+                     "steps": Kt}
+        del ws_tp
+
     # end to end through the C ABI with host buffers: H2D of the step's inputs
     # from pinned memory, dispatch, combine, D2H of x_out, every step
     host = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).pin_memory())
@@ -441,6 +479,7 @@ def run_ours(args):
         "cpu_baseline": cpu,
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
+        "two_phase_combine": two_phase,
         "gpu_launches": K * (4 if wl.quant_mode == 0 else 2),
         "clocks": clocks,
     }

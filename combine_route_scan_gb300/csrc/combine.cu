@@ -322,7 +322,3 @@ cudaError_t launch_combine_reduce(const CombineParams& p, cudaStream_t st, int n
 }
 
 }  // namespace crs
-
-namespace crs {
-cudaError_t launch_combine_two_phase(const CombineParams&, cudaStream_t, int) { return cudaErrorNotSupported; }
-}  // namespace crs

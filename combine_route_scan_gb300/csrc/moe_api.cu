@@ -249,9 +249,9 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
   cp.timeout_ns = timeout_ns(cfg);
   cp.seg_plane_out = seg_plane;
   if (empty) return MOE_OK;
-  if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
-  if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
   if (cfg->combine_mode == MOE_COMBINE_GATHER) {
+    if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
+    if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
     if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
   } else {
     cp.window = w + L.window;
@@ -259,6 +259,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
     cp.plane = w + L.plane_c;
     cp.bulk_ok = sh.row_in % 16 == 0 && aligned(expert_out, 16);
     cp.put_only = cfg->combine_mode == MOE_COMBINE_PUT_ONLY;
+    if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
     cudaError_t e = launch_combine_two_phase(cp, s, nsm);
     if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return MOE_ERR_CUDA;

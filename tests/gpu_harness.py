@@ -64,8 +64,10 @@ def gpu_dispatch(wl: WL.Workload, dev: dict, plane_policy: int = M.PLANE_RULE,
 
 
 def gpu_combine(wl: WL.Workload, dev: dict, expert_out, assist_info, ep_recv_count, combine_mode=M.COMBINE_GATHER,
-                plane_policy: int = M.PLANE_RULE, ws=None, check_status=True, seg_plane=False):
-    cfg = make_cfg(wl, quant_mode=0, combine_mode=combine_mode, plane_policy=plane_policy)
+                plane_policy: int = M.PLANE_RULE, ws=None, check_status=True, seg_plane=False,
+                bulk_min_bytes: int = M.BULK_MIN_BYTES):
+    cfg = make_cfg(wl, quant_mode=0, combine_mode=combine_mode, plane_policy=plane_policy,
+                   bulk_min_bytes=bulk_min_bytes)
     if ws is None:
         ws = M.alloc_workspace(cfg)
     x_out = torch.empty((wl.ep_world_size, wl.bs, wl.h), dtype=TORCH_DT[wl.x_dtype], device="cuda")

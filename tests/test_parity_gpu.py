@@ -227,3 +227,74 @@ def test_host_argument_errors():
         M.dispatch(cfg, dev["x"], dev["expert_ids"], None, None, out["expand_x"], None,
                    out["assist_info"], out["ep_recv_count"], expand_scales=out["expand_scales"], ws=ws)
     assert ei.value.name == "INVALID_ARG"
+
+
+# ------------------------------------------------------- two-phase combine
+
+@pytest.mark.parametrize("name", ["w2_bs8_h16_k2_e4_i32", "w8_bs8_h16_k2_e64_f16",
+                                  "w8_bs32_h7168_k8_e64_i32", "w16_bs256_h7168_k8_e256_bf16_zipf"])
+@pytest.mark.parametrize("plane_policy", [0, 1, 2])
+def test_two_phase_matches_gather_and_oracle(name, plane_policy):
+    """The page's write-back + status protocol gives the same bytes as the
+    gather combine and the oracle, and picks the oracle's planes."""
+    wl = WL.WORKLOADS[name]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    ref = O.dispatch(wl, inp)
+    x_ref = O.combine(wl, ref["expand_x"], ref["assist_info"], ref["ep_recv_count"], inp)
+    xg, _, _ = H.gpu_combine(wl, dev, got["expand_x"], got["assist_info"], got["ep_recv_count"])
+    xt, _, sp = H.gpu_combine(wl, dev, got["expand_x"], got["assist_info"], got["ep_recv_count"],
+                              combine_mode=M.COMBINE_TWO_PHASE, plane_policy=plane_policy, seg_plane=True)
+    assert torch.equal(xt, xg)
+    H.compare_combine(wl, H.to_host(xt), x_ref)
+    assert np.array_equal(H.to_host(xt).view(np.uint8), x_ref.view(np.uint8))
+    if plane_policy == 0:
+        assert np.array_equal(H.to_host(sp), O.combine_plane(wl, ref["ep_recv_count"]))
+    elif plane_policy == 1:
+        assert H.to_host(sp).sum() == 0
+
+
+def test_two_phase_repeated_calls_and_put_only():
+    wl = WL.WORKLOADS["w16_bs256_h7168_k8_e256_bf16_zipf"]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    cfg = H.make_cfg(wl, combine_mode=M.COMBINE_TWO_PHASE)
+    ws = M.alloc_workspace(cfg)
+    xg, _, _ = H.gpu_combine(wl, dev, got["expand_x"], got["assist_info"], got["ep_recv_count"])
+    cfg_put = H.make_cfg(wl, combine_mode=M.COMBINE_PUT_ONLY)
+    for _ in range(3):
+        x_out = torch.zeros_like(xg)
+        M.combine(cfg, got["expand_x"], got["assist_info"], got["ep_recv_count"], dev["expert_ids"],
+                  dev["expert_scales"], dev["active_mask"], dev["x"], x_out, None, ws)
+        assert M.get_device_status(ws) == 0
+        assert torch.equal(x_out, xg)
+        # put only (the page's comm_only): x_out is not written, the epoch still advances
+        untouched = torch.full_like(xg, 7)
+        M.combine(cfg_put, got["expand_x"], got["assist_info"], got["ep_recv_count"], dev["expert_ids"],
+                  dev["expert_scales"], dev["active_mask"], dev["x"], untouched, None, ws)
+        assert M.get_device_status(ws) == 0
+        assert bool((untouched == 7).all())
+
+
+def test_two_phase_wait_times_out_on_a_missing_flag():
+    """Withhold one row from the put phase (its rank claims one row less): the
+    reduce's bounded wait on that pick's flag runs out and reports TIMEOUT."""
+    wl = WL.WORKLOADS["w8_bs8_h16_k2_e64_f16"]
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    ep = got["ep_recv_count"].clone()
+    d = int(torch.argmax(ep[:, -1]).item())
+    ep[d, -1] -= 1
+    cfg = H.make_cfg(wl, quant_mode=0, combine_mode=M.COMBINE_TWO_PHASE, wait_timeout_us=20000)
+    ws = M.alloc_workspace(cfg)
+    x_out = torch.empty_like(dev["x"])
+    M.combine(cfg, got["expand_x"], got["assist_info"], ep, dev["expert_ids"], dev["expert_scales"],
+              dev["active_mask"], dev["x"], x_out, None, ws)
+    assert M.STATUS[M.get_device_status(ws)] == "TIMEOUT"
+    # the workspace stays usable: a consistent call afterwards is clean
+    M.combine(cfg, got["expand_x"], got["assist_info"], got["ep_recv_count"], dev["expert_ids"],
+              dev["expert_scales"], dev["active_mask"], dev["x"], x_out, None, ws)
+    assert M.get_device_status(ws) == 0
