@@ -29,7 +29,8 @@ BULK_MIN_BYTES = 2 * 1024 * 1024
 
 # Every symbol include/moe.h declares.
 EXPORTS = ("moe_get_workspace_size", "moe_workspace_init", "moe_dispatch", "moe_combine",
-           "moe_dispatch_ffn_combine", "moe_get_device_status", "moe_status_string")
+           "moe_dispatch_ffn_combine", "moe_combine_noalloc", "moe_get_device_status", "moe_status_string")
+NOALLOC_MAX_PICKS = 262144
 
 
 class MoeError(RuntimeError):
@@ -81,11 +82,12 @@ def lib() -> ctypes.CDLL:
         L.moe_dispatch.argtypes = [C, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_combine.argtypes = [C, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_dispatch_ffn_combine.argtypes = [C, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_combine_noalloc.argtypes = [C, P, P, P, P, P, P, P, P, P, P]
         L.moe_get_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.moe_status_string.argtypes = [ctypes.c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
         for f in ("moe_get_workspace_size", "moe_workspace_init", "moe_dispatch", "moe_combine",
-                  "moe_dispatch_ffn_combine", "moe_get_device_status"):
+                  "moe_dispatch_ffn_combine", "moe_combine_noalloc", "moe_get_device_status"):
             getattr(L, f).restype = ctypes.c_int32
         _lib = L
     return _lib
@@ -170,6 +172,16 @@ def dispatch_ffn_combine(cfg: MoeConfig, x, expert_ids, active_mask, expert_scal
                                           _ptr(expert_scales), _ptr(w_gate), _ptr(w_up), _ptr(w_down),
                                           _ptr(x_out), _ptr(ws), ws.numel() * ws.element_size(),
                                           _stream(stream)), "moe_dispatch_ffn_combine")
+
+
+def combine_noalloc(cfg: MoeConfig, expert_out, assist_info, ep_recv_count, expert_ids, expert_scales,
+                    active_mask, x, x_out, status, stream=None):
+    """moe_combine_noalloc: the gather combine for callers that cannot
+    allocate; `status` is a one-element int32 CUDA tensor that receives the
+    first device-side error."""
+    _check(lib().moe_combine_noalloc(ctypes.byref(cfg), _ptr(expert_out), _ptr(assist_info), _ptr(ep_recv_count),
+                                     _ptr(expert_ids), _ptr(expert_scales), _ptr(active_mask), _ptr(x),
+                                     _ptr(x_out), _ptr(status), _stream(stream)), "moe_combine_noalloc")
 
 
 def get_device_status(ws: torch.Tensor, stream=None) -> int:

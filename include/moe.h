@@ -172,6 +172,29 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
                                       const void* w_gate, const void* w_up, const void* w_down,
                                       void* x_out, void* ws, size_t ws_bytes, void* stream);
 
+/* Gather combine without any caller-allocated workspace. The pages have no
+ * counterpart of this entry point: it exists for callers that cannot allocate
+ * device memory, such as a plugin or custom-op host that hands the library
+ * only its input and output buffers, or a serving loop that must not allocate
+ * after start-up (an allocation can synchronise the device or fail under
+ * memory pressure mid-step).
+ * Computes exactly what moe_combine does in MOE_COMBINE_GATHER mode (same
+ * arguments, same bytes out); its pick -> row scratch is a fixed device array
+ * inside the library (1 MiB per device, held until the process exits).
+ *   - W * bs * topk must be <= 262144, else MOE_ERR_INVALID_ARG and nothing is
+ *     enqueued; combine_mode must be MOE_COMBINE_GATHER and quant_mode 0.
+ *   - status: device pointer to one int32 (required); the call sets it to 0
+ *     and the kernels record the first device-side error in it.
+ *   - The first call on a device looks up the scratch's device address with
+ *     that device current; make it before any stream capture.
+ *   - All calls on a device share the scratch: calls that overlap on the GPU
+ *     race and must be serialised by the caller.
+ *   - Calls no cudaMalloc, cudaFree or other allocating routine. */
+moe_status_t moe_combine_noalloc(const moe_config_t* cfg, const void* expert_out, const int32_t* assist_info,
+                                 const int32_t* ep_recv_count, const int32_t* expert_ids,
+                                 const void* expert_scales, const uint8_t* active_mask, const void* x,
+                                 void* x_out, int32_t* status, void* stream);
+
 /* Synchronises `stream`, returns in *status (host) the first device-side error
  * recorded in the workspace since the last read (MOE_OK if none), and clears it. */
 moe_status_t moe_get_device_status(void* ws, void* stream, int32_t* status);

@@ -28,7 +28,7 @@ def declared_functions():
 def test_header_declares_the_abi():
     assert declared_functions() == sorted(
         ["moe_get_workspace_size", "moe_workspace_init", "moe_dispatch", "moe_combine",
-         "moe_dispatch_ffn_combine", "moe_get_device_status", "moe_status_string"])
+         "moe_dispatch_ffn_combine", "moe_combine_noalloc", "moe_get_device_status", "moe_status_string"])
 
 
 def test_library_exports_every_declared_symbol(lib):
