@@ -210,6 +210,29 @@ def dist_env():
     return rank, world, local
 
 
+def rank_seed(wl: WL.Workload, rank: int) -> int:
+    """Every rank draws its own independent batch."""
+    return wl.seed + rank
+
+
+def max_over_ranks(v: float, world: int) -> float:
+    """The slowest rank's value (barrier-bracketed timings are maxed)."""
+    if world <= 1:
+        return v
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if dist.get_backend() == "nccl" else "cpu"
+    t = torch.tensor([v], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_gbps(step_bytes: int, steps: int, max_ms: float, world: int) -> float:
+    """Bytes every rank moved over all timed steps, divided by the slowest
+    rank's time (weak scaling: each rank has its own batch)."""
+    return world * step_bytes * steps / (max_ms * 1e-3) / 1e9
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -269,7 +292,7 @@ def run_ours(args):
     from combine_route_scan_gb300 import moe as M
 
     wl = WL.WORKLOADS[args.workload]
-    inp = WL.make_inputs(wl, seed=wl.seed + rank)
+    inp = WL.make_inputs(wl, seed=rank_seed(wl, rank))
     acct = algorithmic_bytes(wl, inp)
     step_bytes = acct["dispatch"] + acct["combine"]
     tdt = {WL.X_INT32: torch.int32, WL.X_FP16: torch.float16, WL.X_BF16: torch.bfloat16}[wl.x_dtype]
@@ -335,10 +358,7 @@ def run_ours(args):
                 step(cfg, cfg)
             torch.cuda.synchronize()
         h_ext = time.time()
-    if world > 1:
-        t = torch.tensor([total_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        total_ms = float(t.item())
+    total_ms = max_over_ranks(total_ms, world)
     st = M.get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the timed region")
@@ -424,10 +444,7 @@ def run_ours(args):
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / Ke
-    if world > 1:
-        t = torch.tensor([e2e_ms], dtype=torch.float64, device="cuda")
-        dist.all_reduce(t, op=dist.ReduceOp.MAX)
-        e2e_ms = float(t.item())
+    e2e_ms = max_over_ranks(e2e_ms, world)
     st = M.get_device_status(ws)
     if st != 0:
         raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the e2e region")
@@ -454,7 +471,7 @@ def run_ours(args):
             dist.destroy_process_group()
         return 0
     ws_bytes = inp["x"].nbytes * 2 + acct["P"] * wl.h * wl.es * 2
-    value = world * step_bytes * K / (total_ms * 1e-3) / 1e9
+    value = whole_job_gbps(step_bytes, K, total_ms, world)
     tokens = world * wl.ep_world_size * wl.bs
     line = {
         "metric": METRIC, "value": value, "unit": "GB/s", "n_gpus": world, "steps": K, "warmup": args.warmup,
