@@ -31,7 +31,8 @@
  *   - quantMode 2: per token amax = max |x| (fp32), scale = amax / 127 (IEEE
  *     fp32 division), q = clamp(round_half_even(x / scale), -127, 127); amax 0
  *     gives scale 0 and q 0;
- *   - FFN variant: SwiGLU, y = (silu(x Wg) * (x Wu)) Wd, evaluated in fp64.
+ *   - FFN variant: SwiGLU, y = (silu(x Wg^T) * (x Wu^T)) Wd^T with weights stored
+ *     out-major (w_gate, w_up [E][I][h], w_down [E][h][I]), evaluated in fp64.
  *
  * Parity pins: every function here is checked in tests/test_oracle_*.py against
  * brute force, closed forms, hand-worked fixtures or library routines.
@@ -436,47 +437,51 @@ int orc_combine(const orc_cfg* c, const void* expert_out, const int32_t* assist,
 /* ---------------------------------------------------------- expert FFN
  *
  * [MEGA] fuses the expert FFN and its activation between dispatch and combine;
- * the activation is SwiGLU: y = (silu(x Wg) * (x Wu)) Wd, silu(a) = a/(1+e^-a).
+ * the activation is SwiGLU: y = (silu(x Wg^T) * (x Wu^T)) Wd^T,
+ * silu(a) = a/(1+e^-a). Weights are stored out-major, like a linear layer (the
+ * pages leave the layout open): w_gate, w_up [E][I][h], w_down [E][h][I].
  * Evaluated in fp64 from bf16 operands.
- *   x_rows [n][h] bf16 bits, expert [n] (global expert id per row)
- *   w_gate, w_up [E][h][I], w_down [E][I][h] (bf16 bits); y [n][h] fp64
+ *   x_rows [n][h] bf16 bits, expert [n] (global expert id per row); y [n][h] fp64
  */
 int orc_swiglu_rows(int h, int I, int E, int64_t n, const uint16_t* x_rows, const int32_t* expert,
                     const uint16_t* w_gate, const uint16_t* w_up, const uint16_t* w_down,
                     double* y) {
   if (h <= 0 || I <= 0 || E <= 0 || n < 0) return ORC_ERR_INVALID_ARG;
+  double* xv = (double*)malloc(sizeof(double) * h);
   double* a = (double*)malloc(sizeof(double) * I);
-  double* b = (double*)malloc(sizeof(double) * I);
   for (int64_t r = 0; r < n; ++r) {
     int32_t e = expert[r];
-    if (e < 0 || e >= E) { free(a); free(b); return ORC_ERR_BAD_EXPERT_ID; }
+    if (e < 0 || e >= E) { free(xv); free(a); return ORC_ERR_BAD_EXPERT_ID; }
     const uint16_t* xr = x_rows + (size_t)r * h;
-    const uint16_t* wg = w_gate + (size_t)e * h * I;
-    const uint16_t* wu = w_up + (size_t)e * h * I;
-    const uint16_t* wd = w_down + (size_t)e * I * h;
-    for (int i = 0; i < I; ++i) { a[i] = 0.0; b[i] = 0.0; }
-    for (int j = 0; j < h; ++j) {
-      double xv = bf16_to_f32(xr[j]);
-      for (int i = 0; i < I; ++i) {
-        a[i] += xv * bf16_to_f32(wg[(size_t)j * I + i]);
-        b[i] += xv * bf16_to_f32(wu[(size_t)j * I + i]);
+    const uint16_t* wg = w_gate + (size_t)e * I * h;
+    const uint16_t* wu = w_up + (size_t)e * I * h;
+    const uint16_t* wd = w_down + (size_t)e * h * I;
+    for (int j = 0; j < h; ++j) xv[j] = bf16_to_f32(xr[j]);
+    for (int i = 0; i < I; ++i) {
+      double g = 0.0, u = 0.0;
+      for (int j = 0; j < h; ++j) {
+        g += xv[j] * bf16_to_f32(wg[(size_t)i * h + j]);
+        u += xv[j] * bf16_to_f32(wu[(size_t)i * h + j]);
       }
+      a[i] = g / (1.0 + exp(-g)) * u;
     }
-    for (int i = 0; i < I; ++i) a[i] = a[i] / (1.0 + exp(-a[i])) * b[i];
     double* yr = y + (size_t)r * h;
-    for (int j = 0; j < h; ++j) yr[j] = 0.0;
-    for (int i = 0; i < I; ++i)
-      for (int j = 0; j < h; ++j) yr[j] += a[i] * bf16_to_f32(wd[(size_t)i * h + j]);
+    for (int j = 0; j < h; ++j) {
+      double acc = 0.0;
+      for (int i = 0; i < I; ++i) acc += a[i] * bf16_to_f32(wd[(size_t)j * I + i]);
+      yr[j] = acc;
+    }
   }
+  free(xv);
   free(a);
-  free(b);
   return ORC_OK;
 }
 
 /* The whole FFN variant for a set of tokens (dispatch -> expert -> combine):
  *   x_out[token] = sum_k w_k * FFN_{e_k}(x[token])   for routed picks,
  *                + w_k * x[token]                     for copy experts,
- * in fp64. tokens[i] = s*bs + t; out [n_tok][h]. Only bf16 x. */
+ * in fp64. tokens[i] = s*bs + t; out [n_tok][h]. Only bf16 x; weights as in
+ * orc_swiglu_rows. */
 int orc_moe_ffn_tokens(const orc_cfg* c, int I, int64_t n_tok, const int64_t* tokens,
                        const uint16_t* x, const int32_t* ids, const uint8_t* mask,
                        const float* scales, const uint16_t* w_gate, const uint16_t* w_up,

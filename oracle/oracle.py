@@ -162,8 +162,9 @@ def combine_plane(wl, ep_recv_count: np.ndarray, bulk_min_bytes: int = DEFAULT_B
 
 def swiglu_rows(x_rows: np.ndarray, expert: np.ndarray, w_gate: np.ndarray, w_up: np.ndarray,
                 w_down: np.ndarray) -> np.ndarray:
-    """fp64 SwiGLU expert FFN of bf16 rows; x_rows [n, h] uint16 bits, expert [n]."""
-    E, h, I = w_gate.shape
+    """fp64 SwiGLU expert FFN of bf16 rows; x_rows [n, h] uint16 bits, expert [n];
+    w_gate, w_up [E, I, h], w_down [E, h, I] (out-major)."""
+    E, I, h = w_gate.shape
     x_rows = np.ascontiguousarray(x_rows, dtype=np.uint16)
     expert = np.ascontiguousarray(expert, dtype=np.int32)
     n = x_rows.shape[0]

@@ -364,13 +364,14 @@ def pin_conversions(n: int = 20000, seed: int = 3):
 
 
 def pin_swiglu_torch(seed: int = 5):
-    """SwiGLU expert rows against torch fp64 matmul and silu (library routines)."""
+    """SwiGLU expert rows against torch fp64 linear algebra and silu (library
+    routines); weights out-major: w_gate, w_up [E, I, h], w_down [E, h, I]."""
     import torch
     rng = np.random.default_rng(seed)
     E, h, I, n = 3, 16, 8, 7
-    wg = WL.fp32_to_bf16_bits(rng.standard_normal((E, h, I)).astype(np.float32) * np.float32(0.3))
-    wu = WL.fp32_to_bf16_bits(rng.standard_normal((E, h, I)).astype(np.float32) * np.float32(0.3))
-    wd = WL.fp32_to_bf16_bits(rng.standard_normal((E, I, h)).astype(np.float32) * np.float32(0.3))
+    wg = WL.fp32_to_bf16_bits(rng.standard_normal((E, I, h)).astype(np.float32) * np.float32(0.3))
+    wu = WL.fp32_to_bf16_bits(rng.standard_normal((E, I, h)).astype(np.float32) * np.float32(0.3))
+    wd = WL.fp32_to_bf16_bits(rng.standard_normal((E, h, I)).astype(np.float32) * np.float32(0.3))
     x = WL.fp32_to_bf16_bits(rng.standard_normal((n, h)).astype(np.float32))
     ex = rng.integers(0, E, size=n).astype(np.int32)
     y = O.swiglu_rows(x, ex, wg, wu, wd)
@@ -378,9 +379,9 @@ def pin_swiglu_torch(seed: int = 5):
     X, G, U, D = t(x), t(wg), t(wu), t(wd)
     for i in range(n):
         e = int(ex[i])
-        a = X[i] @ G[e]
-        b = X[i] @ U[e]
-        want = (torch.nn.functional.silu(a) * b) @ D[e]
+        a = torch.nn.functional.linear(X[i], G[e])
+        b = torch.nn.functional.linear(X[i], U[e])
+        want = torch.nn.functional.linear(torch.nn.functional.silu(a) * b, D[e])
         assert np.allclose(y[i], want.numpy(), rtol=1e-12, atol=1e-12), i
 
 

@@ -54,10 +54,10 @@ MUTANTS = {
     "plane_remote_counts_local": [("if (s != d) remote += seg_rows", "remote += seg_rows")],
     "dispatch_plane_wrong_den": [("const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));\n  const int64_t den = (int64_t)(W - 1 > 1 ? W - 1 : 1) * L;",
                                   "const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));\n  const int64_t den = (int64_t)W * L;")],
-    "silu_sign": [("a[i] = a[i] / (1.0 + exp(-a[i])) * b[i];", "a[i] = a[i] / (1.0 + exp(a[i])) * b[i];")],
-    "gate_up_swapped": [("a[i] += xv * bf16_to_f32(wg[", "a[i] += xv * bf16_to_f32(wu[")],
-    "down_transposed": [("yr[j] += a[i] * bf16_to_f32(wd[(size_t)i * h + j]);",
-                         "yr[j] += a[i] * bf16_to_f32(wd[(size_t)j * I + i]);")],
+    "silu_sign": [("a[i] = g / (1.0 + exp(-g)) * u;", "a[i] = g / (1.0 + exp(g)) * u;")],
+    "gate_up_swapped": [("g += xv[j] * bf16_to_f32(wg[", "g += xv[j] * bf16_to_f32(wu[")],
+    "down_transposed": [("acc += a[i] * bf16_to_f32(wd[(size_t)j * I + i]);",
+                         "acc += a[i] * bf16_to_f32(wd[(size_t)i * h + j]);")],
 }
 
 

@@ -163,8 +163,8 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
       expert_ids    [W, bs, K]   int32
       active_mask   None, [W, bs] or [W, bs, K] uint8
       expert_scales [W, bs, K]   int32 (int32 x) or float32
-      w_gate, w_up  [E, h, I]    uint16 bf16 bits   (FFN workloads only)
-      w_down        [E, I, h]    uint16 bf16 bits
+      w_gate, w_up  [E, I, h]    uint16 bf16 bits   (FFN workloads only; stored
+      w_down        [E, h, I]    out-major, like a linear layer's weight)
     """
     seed = wl.seed if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -214,7 +214,7 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
 
     if wl.ffn_intermediate > 0:
         I = wl.ffn_intermediate
-        for name, shape in (("w_gate", (E, h, I)), ("w_up", (E, h, I)), ("w_down", (E, I, h))):
+        for name, shape in (("w_gate", (E, I, h)), ("w_up", (E, I, h)), ("w_down", (E, h, I))):
             w = rng.standard_normal(size=shape, dtype=np.float32) * np.float32(0.02)
             out[name] = fp32_to_bf16_bits(w)
     return out
