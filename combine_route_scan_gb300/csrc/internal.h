@@ -36,7 +36,6 @@ struct WsLayout {
   size_t ffn_ep;         // int32 [W][L*W]
   size_t ffn_h1;         // bf16 [W*A][I]
   size_t ffn_y;          // bf16 [W*A][h]
-  size_t ffn_tiles;      // int32 tile table
   size_t total;
 };
 
@@ -108,6 +107,21 @@ struct CombineParams {
   uint64_t timeout_ns;
 };
 
+// Everything the expert-FFN grouped GEMMs need.
+struct FfnLaunch {
+  Shape sh;
+  int I;                   // intermediate size
+  const void* w_gate;      // [E][I][h] bf16
+  const void* w_up;        // [E][I][h] bf16
+  const void* w_down;      // [E][h][I] bf16
+  const void* expand_x;    // [W*A][h] bf16 (dispatch output)
+  void* h1;                // [W*A][I] bf16
+  void* y;                 // [W*A][h] bf16 (expert outputs)
+  const int32_t* ep;       // [W][L*W] running receive counts
+  int* status;
+  uint64_t timeout_ns;
+};
+
 // True when the TMA scatter's shared-memory ring fits for this shape.
 bool scatter_tma_fits(const Shape& sh);
 
@@ -117,6 +131,7 @@ cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t st, int num_sms,
 cudaError_t launch_combine_inverse(const CombineParams& p, cudaStream_t st);
 cudaError_t launch_combine_reduce(const CombineParams& p, cudaStream_t st, int num_sms);
 cudaError_t launch_combine_two_phase(const CombineParams& p, cudaStream_t st, int num_sms);
+cudaError_t launch_ffn(const FfnLaunch& f, cudaStream_t st, int num_sms, void* const* prof_events);
 
 // Launch config helper: programmatic dependent launch on `st`.
 struct PdlLaunch {

@@ -80,6 +80,14 @@ WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
     L.flags = take(picks * 4);
     L.window = take(picks * (size_t)sh.row_in);
   }
+  if (c->ffn_intermediate > 0) {
+    const size_t rows = (size_t)sh.W * sh.A;
+    L.ffn_expand_x = take(rows * sh.h * 2);
+    L.ffn_assist = take(rows * 12);
+    L.ffn_ep = take(segs * 4);
+    L.ffn_h1 = take(rows * (size_t)c->ffn_intermediate * 2);
+    L.ffn_y = take(rows * sh.h * 2);
+  }
   L.total = off;
   return L;
 }
@@ -265,6 +273,103 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
     if (e != cudaSuccess) return MOE_ERR_CUDA;
   }
   if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
+  return MOE_OK;
+}
+
+moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
+                                      const uint8_t* active_mask, const float* expert_scales, const void* w_gate,
+                                      const void* w_up, const void* w_down, void* x_out, void* ws, size_t ws_bytes,
+                                      void* stream) {
+  Shape sh;
+  moe_status_t st = make_shape(cfg, &sh);
+  if (st != MOE_OK) return st;
+  const int I = cfg->ffn_intermediate;
+  if (cfg->x_dtype != MOE_BF16 || cfg->quant_mode != 0 || cfg->combine_mode != MOE_COMBINE_GATHER)
+    return MOE_ERR_UNSUPPORTED;
+  // tensor-core tiles: 128 intermediate rows per gate/up tile, 256 output rows
+  // per down tile, 64-element K blocks
+  if (I <= 0 || I % 128 != 0 || sh.h % 256 != 0) return MOE_ERR_UNSUPPORTED;
+  const bool empty = sh.W * (long long)sh.bs == 0;
+  if (!empty && (!x || !expert_ids || !expert_scales || !w_gate || !w_up || !w_down || !x_out))
+    return MOE_ERR_INVALID_ARG;
+  if (sh.mask_kind != 0 && !active_mask && !empty) return MOE_ERR_INVALID_ARG;
+  if (!aligned(x, 16) || !aligned(x_out, 16) || !aligned(w_gate, 16) || !aligned(w_up, 16) ||
+      !aligned(w_down, 16) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4))
+    return MOE_ERR_INVALID_ARG;
+  WsLayout L;
+  st = check_ws(cfg, sh, ws, ws_bytes, &L);
+  if (st != MOE_OK) return st;
+  uint8_t* w = static_cast<uint8_t*>(ws);
+  WsHeader* hdr = reinterpret_cast<WsHeader*>(w);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  const int nsm = num_sms_of_current_device();
+  if (nsm <= 0) return MOE_ERR_CUDA;
+  int32_t* ep = reinterpret_cast<int32_t*>(w + L.ffn_ep);
+  int32_t* assist = reinterpret_cast<int32_t*>(w + L.ffn_assist);
+  void* ex = w + L.ffn_expand_x;
+
+  // 1. dispatch into the workspace
+  const bool tma = sh.row_in % 16 == 0 && scatter_tma_fits(sh);
+  RouteParams rp{};
+  rp.ids = expert_ids;
+  rp.mask = sh.mask_kind ? active_mask : nullptr;
+  rp.sh = sh;
+  rp.cnt = reinterpret_cast<int32_t*>(w + L.cnt);
+  rp.rank = reinterpret_cast<int32_t*>(w + L.rank);
+  rp.base = reinterpret_cast<int32_t*>(w + L.base);
+  rp.ep_recv_count = ep;
+  rp.plane = w + L.plane_d;
+  rp.plane_policy = cfg->plane_policy;
+  rp.bulk_ok = tma ? 1 : 0;
+  rp.bulk_min_bytes = cfg->bulk_min_bytes;
+  rp.done = &hdr->route_done;
+  rp.status = &hdr->status;
+  if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  ScatterParams sp{};
+  sp.x = x;
+  sp.ids = expert_ids;
+  sp.mask = rp.mask;
+  sp.expand_x = ex;
+  sp.assist = assist;
+  sp.rank = rp.rank;
+  sp.base = rp.base;
+  sp.plane = rp.plane;
+  sp.sh = sh;
+  sp.status = &hdr->status;
+  sp.timeout_ns = timeout_ns(cfg);
+  if (!empty && launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
+  if (empty) return MOE_OK;
+
+  // 2. expert FFN on the tensor cores: h1 = silu(x Wg^T) * (x Wu^T), y = h1 Wd^T
+  FfnLaunch f{};
+  f.sh = sh;
+  f.I = I;
+  f.w_gate = w_gate;
+  f.w_up = w_up;
+  f.w_down = w_down;
+  f.expand_x = ex;
+  f.h1 = w + L.ffn_h1;
+  f.y = w + L.ffn_y;
+  f.ep = ep;
+  f.status = &hdr->status;
+  f.timeout_ns = timeout_ns(cfg);
+  if (launch_ffn(f, s, nsm, cfg->prof_events) != cudaSuccess) return MOE_ERR_CUDA;
+
+  // 3. combine the expert outputs
+  CombineParams cp{};
+  cp.expert_out = f.y;
+  cp.assist = assist;
+  cp.ep_recv_count = ep;
+  cp.ids = expert_ids;
+  cp.scales = expert_scales;
+  cp.mask = rp.mask;
+  cp.x = x;
+  cp.x_out = x_out;
+  cp.inv = reinterpret_cast<int32_t*>(w + L.inv);
+  cp.sh = sh;
+  cp.status = &hdr->status;
+  if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }
 
