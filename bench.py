@@ -38,6 +38,7 @@ import workloads as WL  # noqa: E402
 
 METRIC = "dispatch+combine GB/s and tokens/s on 1 GB300; fraction of 8 TB/s HBM roofline"
 DEFAULT_WORKLOAD = "w16_bs256_h7168_k8_e256_bf16_zipf"
+FFN_WORKLOAD = "w8_bs64_h2048_k8_e128_bf16_ffn"
 HBM_NOMINAL_GBPS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBPS = 6800.0
@@ -53,6 +54,9 @@ def parse_args():
     ap.add_argument("--plane-policy", type=int, default=0)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--e2e-steps", type=int, default=200)
+    ap.add_argument("--ffn-workload", default=FFN_WORKLOAD, choices=sorted(WL.WORKLOADS))
+    ap.add_argument("--no-ffn", action="store_true")
+    ap.add_argument("--ffn-steps", type=int, default=100)
     return ap.parse_args()
 
 
@@ -276,6 +280,58 @@ def run_reference(args):
     return 0
 
 
+def measure_ffn(args, M, torch, stream):
+    """moe_dispatch_ffn_combine on the decode-layer workload: whole call, and
+    the gate/up GEMM alone (CUDA events the library records around it)."""
+    wl = WL.WORKLOADS[args.ffn_workload]
+    inp = WL.make_inputs(wl)
+    I, E, h = wl.ffn_intermediate, wl.moe_expert_num, wl.h
+
+    def dev(a, bf):
+        t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if bf else np.ascontiguousarray(a))
+        return (t.view(torch.bfloat16) if bf else t).cuda()
+
+    x, ids = dev(inp["x"], True), dev(inp["expert_ids"], False)
+    scales = dev(inp["expert_scales"], False)
+    mask = None if inp.get("active_mask") is None else dev(inp["active_mask"], False)
+    wg, wu, wd = (dev(inp[k], True) for k in ("w_gate", "w_up", "w_down"))
+    cfg = M.config(wl.ep_world_size, wl.bs, h, wl.topk, E, torch.bfloat16, zero_expert_num=wl.zero_expert_num,
+                   copy_expert_num=wl.copy_expert_num, mask_kind=wl.mask_kind, ffn_intermediate=I)
+    ws = M.alloc_workspace(cfg)
+    x_out = torch.empty_like(x)
+    for _ in range(3):
+        M.dispatch_ffn_combine(cfg, x, ids, mask, scales, wg, wu, wd, x_out, ws)
+    torch.cuda.synchronize()
+    Kf = max(1, args.ffn_steps)
+    evs = [M.ProfEvents() for _ in range(Kf)]
+    cfgs = [e.attach(cfg) for e in evs]
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    for c in cfgs:
+        M.dispatch_ffn_combine(c, x, ids, mask, scales, wg, wu, wd, x_out, ws)
+    b.record(stream)
+    torch.cuda.synchronize()
+    st = M.get_device_status(ws)
+    if st != 0:
+        raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the FFN variant")
+    call_ms = a.elapsed_time(b) / Kf
+    gu_ms = statistics.mean(e.elapsed_ms() for e in evs)
+    acct = algorithmic_bytes(wl, inp)
+    P = acct["P"]
+    w_bytes = 3 * E * I * h * 2
+    gu_bytes = 2 * E * I * h * 2 + P * h * 2 + P * I * 2   # weights + token rows in + h1 out
+    flops = 2 * P * (3 * I * h)
+    peaks = measured_peaks()
+    return {"workload": wl.name, "ms_per_call": call_ms, "tokens_per_s": wl.ep_world_size * wl.bs / (call_ms * 1e-3),
+            "weight_bytes": w_bytes, "routed_picks": P,
+            "call_GBps": (w_bytes + acct["dispatch"] + acct["combine"]) / (call_ms * 1e-3) / 1e9,
+            "call_TFLOPs": flops / (call_ms * 1e-3) / 1e12,
+            "gate_up_gemm_ms": gu_ms, "gate_up_GBps": gu_bytes / (gu_ms * 1e-3) / 1e9,
+            "gate_up_frac_of_hbm": gu_bytes / (gu_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+            "gate_up_TFLOPs": 2 * P * 2 * I * h / (gu_ms * 1e-3) / 1e12,
+            "steps": Kf}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -411,6 +467,8 @@ def run_ours(args):
                      "steps": Kt}
         del ws_tp
 
+    ffn = None if args.no_ffn or world > 1 else measure_ffn(args, M, torch, stream)
+
     # end to end through the C ABI with host buffers: H2D of the step's inputs
     # from pinned memory, dispatch, combine, D2H of x_out, every step
     host = {k: (None if v is None else torch.from_numpy(np.ascontiguousarray(v)).pin_memory())
@@ -497,6 +555,7 @@ def run_ours(args):
         "e2e": {"value": step_bytes / (e2e_ms * 1e-3) / 1e9 * world, "unit": "GB/s", "ms_per_step": e2e_ms,
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "two_phase_combine": two_phase,
+        "ffn_variant": ffn,
         "gpu_launches": K * (4 if wl.quant_mode == 0 else 2),
         "clocks": clocks,
     }

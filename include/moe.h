@@ -101,7 +101,8 @@ typedef struct {
   int32_t reserved0;        /* must be 0 */
   void* const* prof_events; /* optional host array {start, stop} of cudaEvent_t: recorded
                                on `stream` around the call's main kernel (scatter for
-                               dispatch, reduce for combine); NULL for none */
+                               dispatch, reduce for combine, the gate/up GEMM for
+                               dispatch_ffn_combine); NULL for none */
 } moe_config_t;
 
 /* Workspace bytes for `cfg` (first phase of [DISP]'s two-phase contract), and
@@ -160,11 +161,14 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
 /* Dispatch -> per-expert SwiGLU FFN -> combine in one call ([MEGA] 背景与目标 and
  * 依赖关系: one operator for dispatch, expert FFN with activation, and combine;
  * intermediate_hidden = 512 on A3):
- *   x_out[s][t] = sum_k w_k * ( silu(x Wg[e]) * (x Wu[e]) ) Wd[e]   (routed picks)
- *               + sum_k w_k * x                                       (copy experts)
- * bf16 only, quant_mode 0. The FFN runs on tcgen05 tensor cores with fp32
- * accumulation; the intermediate and expert outputs are rounded to bf16.
- *   w_gate, w_up [E][h][I] bf16, w_down [E][I][h] bf16; expert_scales fp32.
+ *   x_out[s][t] = sum_k w_k * ( silu(x Wg[e]^T) * (x Wu[e]^T) ) Wd[e]^T   (routed picks)
+ *               + sum_k w_k * x                                             (copy experts)
+ * bf16 only, quant_mode 0, combine_mode MOE_COMBINE_GATHER; I a multiple of
+ * 128 and h a multiple of 256 (tensor-core tiles), else MOE_ERR_UNSUPPORTED.
+ * The FFN runs on tcgen05 tensor cores with fp32 accumulation; the
+ * intermediate and expert outputs are rounded to bf16.
+ *   w_gate, w_up [E][I][h] bf16 and w_down [E][h][I] bf16, stored out-major like
+ *   a linear layer's weight (each row is one output feature); expert_scales fp32.
  * The workspace holds the dispatch outputs and intermediates (size from
  * moe_get_workspace_size with ffn_intermediate = I). */
 moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
