@@ -21,10 +21,19 @@
 // leaves each pick's expert id (or -1) in the rank array; the second walk
 // reads it back and overwrites it with the position.
 //
-// The last CTA to finish (completion counter in the workspace) scans the
-// W*L*W segment counts, tile by tile through shared memory, into ep_recv_count
-// (inclusive) and segment offsets (exclusive), per receiving rank.
+// The per-rank scan of the W*L*W segment counts into ep_recv_count (inclusive)
+// and segment offsets (exclusive) then takes one of two forms:
+//   * W <= 16: the W CTAs run as one thread-block cluster. After a cluster
+//     barrier, CTA d reads the counts of segment (le, s) of rank d straight from
+//     CTA s's shared memory (distributed shared memory) and scans rank d's L*W
+//     segments itself: all ranks in parallel, no global fence, no atomic.
+//   * otherwise: the last CTA to finish (completion counter in the workspace)
+//     scans all counts, tile by tile through shared memory.
+#include <cooperative_groups.h>
+
 #include "common.cuh"
+
+namespace cg = cooperative_groups;
 
 namespace crs {
 
@@ -32,6 +41,7 @@ constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kScanTile = 4096;
 
+template <bool CLUSTER>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   extern __shared__ __align__(16) int32_t rsm[];  // wcnt [kRouteWarps][E], tot [E]; later the scan tiles
   __shared__ long long s_scan[32];
@@ -99,7 +109,7 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
       run += c;
     }
     tot[e] = run;
-    p.cnt[(size_t)e * sh.W + s] = run;
+    if (!CLUSTER) p.cnt[(size_t)e * sh.W + s] = run;
     if (e / sh.L != s) remote += run;
   }
   {
@@ -131,6 +141,27 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   }
   __syncthreads();
 
+  if constexpr (CLUSTER) {
+    // every CTA's totals are final once the cluster barrier passes; CTA s now
+    // scans the L*W segments (le, s') of receiving rank d = s (L*W = E <= 1024)
+    cg::cluster_group cluster = cg::this_cluster();
+    cluster.sync();
+    const int d = s, LW = sh.L * sh.W;
+    long long c = 0;
+    if (tid < LW) {
+      const int le = tid / sh.W, sp = tid - le * sh.W;
+      const int32_t* remote_tot = cluster.map_shared_rank(tot, sp);
+      c = remote_tot[d * sh.L + le];
+    }
+    const long long ex = block_exclusive_scan(c, s_scan);
+    if (tid < LW) {
+      const size_t g = (size_t)d * LW + tid;
+      p.base[g] = (int32_t)ex;
+      p.ep_recv_count[g] = (int32_t)(ex + c);
+      if (tid == LW - 1 && ex + c > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
+    }
+  }
+
   // walk 2: position of every routed pick inside its segment
   for (int it = it0; it < it1; ++it) {
     const int t = it * G + tl;
@@ -143,6 +174,11 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
     __syncwarp();
     if (valid) keys[(size_t)t * K + k] = r;
+  }
+
+  if constexpr (CLUSTER) {
+    cg::this_cluster().sync();  // no CTA leaves while others may read its counts
+    return;
   }
 
   // the last CTA turns the counts of all sources into offsets
@@ -200,20 +236,67 @@ static size_t route_smem(const Shape& sh) {
   return walk > scan ? walk : scan;
 }
 
+// Is a cluster of W route CTAs schedulable on this device? Cached per (device, W).
+static bool cluster_route_ok(int dev, int W, size_t smem) {
+  static signed char ok[64][17] = {};
+  if (W > 16) return false;
+  if (ok[dev][W] != 0) return ok[dev][W] > 0;
+  bool good = cudaFuncSetAttribute(route_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+                  cudaSuccess &&
+              cudaFuncSetAttribute(route_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)((kRouteWarps + 1) * 1024 * sizeof(int32_t))) == cudaSuccess;
+  if (good) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(W);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = smem;
+    cudaLaunchAttribute a[1];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = W;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 1;
+    int n = 0;
+    good = cudaOccupancyMaxActiveClusters(&n, route_kernel<true>, &cfg) == cudaSuccess && n >= 1;
+  }
+  cudaGetLastError();  // a refused query leaves no sticky error behind
+  ok[dev][W] = good ? 1 : -1;
+  return good;
+}
+
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st) {
   if (p.sh.K > 32) return cudaErrorInvalidValue;
-  const size_t smem = route_smem(p.sh);
-  static size_t attr_bytes[64] = {};
   int dev = 0;
   cudaGetDevice(&dev);
   if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  const size_t walk = (size_t)(kRouteWarps + 1) * p.sh.E * sizeof(int32_t);
+  if (cluster_route_ok(dev, p.sh.W, walk)) {
+    cudaLaunchConfig_t cfg{};
+    cfg.gridDim = dim3(p.sh.W);
+    cfg.blockDim = dim3(kRouteThreads);
+    cfg.dynamicSmemBytes = walk;
+    cfg.stream = st;
+    cudaLaunchAttribute a[2];
+    a[0].id = cudaLaunchAttributeClusterDimension;
+    a[0].val.clusterDim.x = p.sh.W;
+    a[0].val.clusterDim.y = 1;
+    a[0].val.clusterDim.z = 1;
+    a[1].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+    a[1].val.programmaticStreamSerializationAllowed = 1;
+    cfg.attrs = a;
+    cfg.numAttrs = 2;
+    return cudaLaunchKernelEx(&cfg, route_kernel<true>, p);
+  }
+  const size_t smem = route_smem(p.sh);
+  static size_t attr_bytes[64] = {};
   if (attr_bytes[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e = cudaFuncSetAttribute(route_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_bytes[dev] = smem;
   }
   PdlLaunch L(dim3(p.sh.W), dim3(kRouteThreads), smem, st);
-  return cudaLaunchKernelEx(&L.cfg, route_kernel, p);
+  return cudaLaunchKernelEx(&L.cfg, route_kernel<false>, p);
 }
 
 }  // namespace crs
