@@ -40,6 +40,7 @@ namespace crs {
 constexpr int kRouteThreads = 1024;
 constexpr int kRouteWarps = kRouteThreads / 32;
 constexpr int kScanTile = 4096;
+constexpr int kRegIters = 4;  // warp iterations whose keys walk 1 keeps in registers
 
 template <bool CLUSTER>
 __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
@@ -73,29 +74,74 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   const int tl = lane / K, k = lane - tl * K;
   int32_t* keys = p.rank + tok0 * K;
 
-  // walk 1: classify, reject repeated routed ids, count per warp and expert
-  for (int it = it0; it < it1; ++it) {
-    const int t = it * G + tl;
-    const bool valid = tl < G && t < sh.bs;
-    int key = -1;
-    if (valid) {
-      const int c = classify_pick(p.ids, p.mask, sh, tok0 + t, k);
-      if (c == kPickBad) set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
-      key = c >= 0 ? c : -1;
+  // walk 1: classify, reject repeated routed ids, count per warp and expert.
+  // When a warp has at most kRegIters iterations (the common case), all its
+  // ids and mask bytes are loaded up front so the loads are in flight
+  // together, and the keys stay in registers for walk 2.
+  const bool in_regs = per_warp <= kRegIters;
+  int keyr[kRegIters];
+  if (in_regs) {
+    int raw[kRegIters];
+    bool act[kRegIters];
+#pragma unroll
+    for (int j = 0; j < kRegIters; ++j) {
+      const int t = (it0 + j) * G + tl;
+      const bool valid = it0 + j < it1 && tl < G && t < sh.bs;
+      const size_t tok = tok0 + t;
+      raw[j] = valid ? p.ids[tok * K + k] : -1;
+      act[j] = valid && (sh.mask_kind == 0 || (sh.mask_kind == 1 ? p.mask[tok] != 0 : p.mask[tok * K + k] != 0));
     }
-    bool dup = false;
-    for (int dd = 1; dd < K; ++dd) {
-      const int other = __shfl_up_sync(0xffffffffu, key, dd);
-      if (dd <= k && key >= 0 && other == key) dup = true;
+#pragma unroll
+    for (int j = 0; j < kRegIters; ++j) {
+      if (it0 + j >= it1) {
+        keyr[j] = -1;
+        continue;
+      }
+      int key = -1;
+      if (act[j]) {
+        const int e = raw[j];
+        const long long z = (long long)e - sh.E;
+        if (e < 0 || z >= (long long)sh.Z + sh.C) set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+        else if (e < sh.E) key = e;
+      }
+      bool dup = false;
+      for (int dd = 1; dd < K; ++dd) {
+        const int other = __shfl_up_sync(0xffffffffu, key, dd);
+        if (dd <= k && key >= 0 && other == key) dup = true;
+      }
+      if (dup) {
+        set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+        key = -1;
+      }
+      keyr[j] = key;
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
+      __syncwarp();
     }
-    if (dup) {
-      set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
-      key = -1;
+  } else {
+    for (int it = it0; it < it1; ++it) {
+      const int t = it * G + tl;
+      const bool valid = tl < G && t < sh.bs;
+      int key = -1;
+      if (valid) {
+        const int c = classify_pick(p.ids, p.mask, sh, tok0 + t, k);
+        if (c == kPickBad) set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+        key = c >= 0 ? c : -1;
+      }
+      bool dup = false;
+      for (int dd = 1; dd < K; ++dd) {
+        const int other = __shfl_up_sync(0xffffffffu, key, dd);
+        if (dd <= k && key >= 0 && other == key) dup = true;
+      }
+      if (dup) {
+        set_error(p.status, MOE_ERR_BAD_EXPERT_ID);
+        key = -1;
+      }
+      if (valid) keys[(size_t)t * K + k] = key;
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
+      __syncwarp();
     }
-    if (valid) keys[(size_t)t * K + k] = key;
-    const uint32_t peers = __match_any_sync(0xffffffffu, key);
-    if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
-    __syncwarp();
   }
   __syncthreads();
 
@@ -163,10 +209,19 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   }
 
   // walk 2: position of every routed pick inside its segment
-  for (int it = it0; it < it1; ++it) {
+  for (int j = 0; j < per_warp; ++j) {
+    const int it = it0 + j;
+    if (it >= it1) break;
     const int t = it * G + tl;
     const bool valid = tl < G && t < sh.bs;
-    const int key = valid ? keys[(size_t)t * K + k] : -1;
+    int key = -1;
+    if (in_regs) {
+#pragma unroll
+      for (int q = 0; q < kRegIters; ++q)
+        if (q == j) key = keyr[q];
+    } else if (valid) {
+      key = keys[(size_t)t * K + k];
+    }
     const uint32_t peers = __match_any_sync(0xffffffffu, key);
     int r = -1;
     if (key >= 0) r = wcnt[warp * E + key] + __popc(peers & lanemask_lt());
