@@ -25,6 +25,7 @@ struct WsLayout {
   size_t cnt;      // int32 [E*W]     rows of segment g = e*W + s
   size_t base;     // int32 [E*W]     first row of segment g inside its rank
   size_t plane_d;  // uint8 [E*W]     dispatch plane per segment
+  size_t landed;   // uint32 [E*W]    dispatch rows in place per segment (ready flags)
   size_t rank;     // int32 [W*bs*K]  position of a routed pick inside its segment
   size_t inv;      // int32 [W*bs*K]  combine: flat expert-output row of each pick
   size_t plane_c;  // uint8 [E*W]     two-phase combine plane per segment
@@ -63,6 +64,9 @@ struct RouteParams {
   int64_t bulk_min_bytes;
   uint32_t* done;
   int* status;
+  uint32_t* landed;        // per-segment rows in place (zeroed here when flags are on)
+  uint32_t* seg_ready;     // optional ready flags
+  uint32_t ticket;
 };
 
 struct ScatterParams {
@@ -77,6 +81,10 @@ struct ScatterParams {
   const int32_t* rank;
   const int32_t* base;
   const uint8_t* plane;
+  const int32_t* cnt;      // rows per segment
+  uint32_t* landed;        // per-segment rows in place
+  uint32_t* seg_ready;     // optional ready flags
+  uint32_t ticket;
   Shape sh;
   int* status;
   uint64_t timeout_ns;

@@ -36,7 +36,7 @@ moe_status_t make_shape(const moe_config_t* c, Shape* sh) {
   if (c->bulk_min_bytes < 0) return MOE_ERR_INVALID_ARG;
   if (c->combine_mode < MOE_COMBINE_GATHER || c->combine_mode > MOE_COMBINE_PUT_ONLY) return MOE_ERR_INVALID_ARG;
   if (c->wait_timeout_us <= 0) return MOE_ERR_INVALID_ARG;
-  if (c->ffn_intermediate < 0 || c->reserved0 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->ffn_intermediate < 0 || c->reserved0 != 0 || c->reserved1 != 0) return MOE_ERR_INVALID_ARG;
   const long long picks = (long long)c->ep_world_size * c->bs * c->topk;
   if (picks >= 2147483647LL) return MOE_ERR_INVALID_ARG;
   sh->W = c->ep_world_size;
@@ -73,6 +73,7 @@ WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
   L.cnt = take(segs * 4);
   L.base = take(segs * 4);
   L.plane_d = take(segs);
+  L.landed = take(segs * 4);
   L.rank = take(picks * 4);
   L.inv = take(picks * 4);
   if (c->combine_mode != MOE_COMBINE_GATHER) {
@@ -162,7 +163,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (sh.quant == 2 && !dynamic_scales) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4) ||
       !aligned(assist_info, 4) || !aligned(ep_recv_count, 4) || !aligned(expand_scales, 4) ||
-      !aligned(dynamic_scales, 4))
+      !aligned(dynamic_scales, 4) || !aligned(cfg->seg_ready, 4))
     return MOE_ERR_INVALID_ARG;
   WsLayout L;
   st = check_ws(cfg, sh, ws, ws_bytes, &L);
@@ -190,9 +191,16 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   rp.bulk_min_bytes = cfg->bulk_min_bytes;
   rp.done = &hdr->route_done;
   rp.status = &hdr->status;
+  rp.landed = reinterpret_cast<uint32_t*>(w + L.landed);
+  rp.seg_ready = cfg->seg_ready;
+  rp.ticket = cfg->seg_ready_ticket;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   ScatterParams sp{};
+  sp.cnt = rp.cnt;
+  sp.landed = rp.landed;
+  sp.seg_ready = cfg->seg_ready;
+  sp.ticket = cfg->seg_ready_ticket;
   sp.x = x;
   sp.ids = expert_ids;
   sp.mask = rp.mask;

@@ -155,7 +155,12 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
       run += c;
     }
     tot[e] = run;
-    if (!CLUSTER) p.cnt[(size_t)e * sh.W + s] = run;
+    const size_t g = (size_t)e * sh.W + s;
+    p.cnt[g] = run;
+    if (p.seg_ready) {  // ready flags: count this call's rows from zero; empty segments are ready now
+      p.landed[g] = 0u;
+      if (run == 0) st_release_gpu(p.seg_ready + g, p.ticket);
+    }
     if (e / sh.L != s) remote += run;
   }
   {

@@ -32,12 +32,24 @@ constexpr int kMaxK = 32;
 
 __host__ __device__ __forceinline__ size_t align128(size_t v) { return (v + 127) & ~size_t(127); }
 
-// Per-token destination list, built by warp 0. Double-buffered by token parity.
+// Per-token destination list, built by warp 0. Three of them rotate by token,
+// so the ready-flag publisher can still read the last two tokens' lists.
 struct PickTable {
   long long sm_dst[kMaxK];    // flat expand_x rows (d*A + row) on the store plane
   long long bulk_dst[kMaxK];  // ... on the bulk plane
+  int sm_seg[kMaxK];          // their segments g = e*W + s
+  int bulk_seg[kMaxK];
   int n_sm, n_bulk;
 };
+
+// One more row of segment g is in place; the last one releases the flag.
+// The caller has fenced after the row's stores became visible.
+__device__ __forceinline__ void publish_row(const ScatterParams& p, int g) {
+  if (atomicAdd(p.landed + g, 1u) + 1u == (uint32_t)p.cnt[g]) {
+    __threadfence();
+    st_release_gpu(p.seg_ready + g, p.ticket);
+  }
+}
 
 // Builds the destination list of token `tau` (warp 0 only) and writes the
 // per-row metadata. Returns nothing; results land in `tab`.
@@ -72,8 +84,17 @@ __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, 
   }
   const uint32_t m_sm = __ballot_sync(0xffffffffu, dst >= 0 && !bulk);
   const uint32_t m_bk = __ballot_sync(0xffffffffu, dst >= 0 && bulk);
-  if (dst >= 0 && !bulk) tab.sm_dst[__popc(m_sm & lanemask_lt())] = dst;
-  if (dst >= 0 && bulk) tab.bulk_dst[__popc(m_bk & lanemask_lt())] = dst;
+  const int seg = dst >= 0 ? p.ids[tau * sh.K + lane] * sh.W + s : -1;
+  if (dst >= 0 && !bulk) {
+    const int j = __popc(m_sm & lanemask_lt());
+    tab.sm_dst[j] = dst;
+    tab.sm_seg[j] = seg;
+  }
+  if (dst >= 0 && bulk) {
+    const int j = __popc(m_bk & lanemask_lt());
+    tab.bulk_dst[j] = dst;
+    tab.bulk_seg[j] = seg;
+  }
   if (lane == 0) {
     tab.n_sm = __popc(m_sm);
     tab.n_bulk = __popc(m_bk);
@@ -133,12 +154,34 @@ __device__ __forceinline__ uint2 quant8(int4 v, float scale, bool zero) {
   return make_uint2(out[0], out[1]);
 }
 
+// Ready flags, called by thread 0 right after the first barrier of token i:
+//   * token i-1's store-plane rows: every thread passed the barrier after
+//     storing them, so a fence makes them visible before the count;
+//   * token i-2's bulk-plane rows: its bulk group is complete once at most one
+//     newer group (token i-1's) is pending; then an async-proxy fence.
+__device__ __forceinline__ void publish_earlier(const ScatterParams& p, const PickTable* tabs, int i) {
+  if (i >= 1) {
+    __threadfence();
+    const PickTable& a = tabs[(i - 1) % 3];
+    for (int j = 0; j < a.n_sm; ++j) publish_row(p, a.sm_seg[j]);
+  }
+  if (i >= 2) {
+    const PickTable& b = tabs[(i - 2) % 3];
+    if (b.n_bulk > 0) {
+      bulk_wait_all<1>();
+      fence_proxy_async_global();
+      __threadfence();
+      for (int j = 0; j < b.n_bulk; ++j) publish_row(p, b.bulk_seg[j]);
+    }
+  }
+}
+
 // QUANT: 0 or 2; DT: element type for the quantiser (MOE_F16 / MOE_BF16).
 template <int QUANT, int DT, int STAGES>
 __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
-  __shared__ PickTable tabs[2];
+  __shared__ PickTable tabs[3];
   __shared__ float s_red[2][kScatterWarps];
   __shared__ int s_abort;
 
@@ -177,7 +220,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
     const int stage = i % STAGES;
     const uint32_t parity = (uint32_t)(i / STAGES) & 1u;
-    PickTable& tab = tabs[i & 1];
+    PickTable& tab = tabs[i % 3];
     const uint8_t* row = xin + stage * slot_in;
 
     bool ok = mbar_wait_bounded(&full_bar[stage], parity, p.status, p.timeout_ns);
@@ -195,6 +238,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
       if (lane == 0) s_red[i & 1][warp] = m;
       __syncthreads();
       if (s_abort) break;
+      if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
       float amax = 0.f;
 #pragma unroll
       for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[i & 1][w]);
@@ -233,6 +277,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
       if (warp == 0) build_picks(p, tau, s, t, tab, false, 0.f);
       __syncthreads();
       if (s_abort) break;
+      if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
       const int nb = tab.n_bulk, ns = tab.n_sm;
       if (tid == 0) {
         // refill the slot of the previous token once its bulk group has read it
@@ -256,6 +301,24 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     }
   }
   // all bulk stores of this CTA complete before it exits
+  if (p.seg_ready) {
+    __syncthreads();  // every thread's stores of the last token are issued
+    if (tid == 0 && !s_abort) {
+      bulk_wait_all<0>();
+      fence_proxy_async_global();
+      __threadfence();
+      const int last = my_n - 1;
+      if (last >= 0) {
+        const PickTable& a = tabs[last % 3];
+        for (int j = 0; j < a.n_sm; ++j) publish_row(p, a.sm_seg[j]);
+        for (int j = 0; j < a.n_bulk; ++j) publish_row(p, a.bulk_seg[j]);
+      }
+      if (last >= 1) {
+        const PickTable& b = tabs[(last - 1) % 3];
+        for (int j = 0; j < b.n_bulk; ++j) publish_row(p, b.bulk_seg[j]);
+      }
+    }
+  }
   if (tid == 0) bulk_wait_all<0>();
 }
 
@@ -293,7 +356,10 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
       __syncwarp();
       // both planes are carried by plain stores here
       if (lane == 0) {
-        for (int j = 0; j < tab.n_bulk; ++j) tab.sm_dst[tab.n_sm + j] = tab.bulk_dst[j];
+        for (int j = 0; j < tab.n_bulk; ++j) {
+          tab.sm_dst[tab.n_sm + j] = tab.bulk_dst[j];
+          tab.sm_seg[tab.n_sm + j] = tab.bulk_seg[j];
+        }
         tab.n_sm += tab.n_bulk;
         tab.n_bulk = 0;
       }
@@ -323,6 +389,11 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
         const uint16_t v = xr[j];
         for (int k = 0; k < ns; ++k) out[tab.sm_dst[k] * sh.h + j] = v;
       }
+    }
+    __syncthreads();
+    if (p.seg_ready && tid == 0) {  // every thread's rows of this token are stored
+      __threadfence();
+      for (int k = 0; k < ns; ++k) publish_row(p, tab.sm_seg[k]);
     }
     __syncthreads();
   }

@@ -51,7 +51,8 @@ class MoeConfig(ctypes.Structure):
         ("plane_policy", ctypes.c_int32), ("bulk_min_bytes", ctypes.c_int64),
         ("combine_mode", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
         ("ffn_intermediate", ctypes.c_int32), ("reserved0", ctypes.c_int32),
-        ("prof_events", ctypes.c_void_p),
+        ("prof_events", ctypes.c_void_p), ("seg_ready", ctypes.c_void_p),
+        ("seg_ready_ticket", ctypes.c_uint32), ("reserved1", ctypes.c_int32),
     ]
 
 
@@ -63,7 +64,7 @@ def config(ep_world_size: int, bs: int, h: int, topk: int, moe_expert_num: int, 
     dt = DTYPE_CODE[x_dtype] if isinstance(x_dtype, torch.dtype) else int(x_dtype)
     return MoeConfig(ep_world_size, bs, h, topk, moe_expert_num, zero_expert_num, copy_expert_num, 0,
                      quant_mode, mask_kind, dt, plane_policy, bulk_min_bytes, combine_mode, wait_timeout_us,
-                     ffn_intermediate, 0, None)
+                     ffn_intermediate, 0, None, None, 0, 0)
 
 
 _lib = None
@@ -134,6 +135,15 @@ class ProfEvents:
 
     def elapsed_ms(self) -> float:
         return self.start.elapsed_time(self.stop)
+
+
+def with_seg_ready(cfg: MoeConfig, seg_ready: torch.Tensor, ticket: int) -> MoeConfig:
+    """A copy of cfg whose dispatch stores `ticket` into seg_ready[d][le*W+s]
+    once segment (le, s) of rank d is complete (uint32 CUDA tensor [W, L*W])."""
+    c = MoeConfig.from_buffer_copy(cfg)
+    c.seg_ready = ctypes.c_void_p(_ptr(seg_ready).value)
+    c.seg_ready_ticket = ticket
+    return c
 
 
 def workspace_size(cfg: MoeConfig):

@@ -103,6 +103,17 @@ typedef struct {
                                on `stream` around the call's main kernel (scatter for
                                dispatch, reduce for combine, the gate/up GEMM for
                                dispatch_ffn_combine); NULL for none */
+  uint32_t* seg_ready;      /* optional device array [W][L*W] (moe_dispatch only): the
+                               segment's ready flag ([SHMEM] 实现逻辑: status written only
+                               after its payload is visible). Each entry is set to
+                               seg_ready_ticket with a release store once every row of
+                               segment (le, s) of rank d is in place in expand_x and its
+                               metadata (bulk-plane rows: after their bulk copies completed
+                               and an async-proxy fence); empty segments too. A consumer on
+                               another stream may poll it with acquire loads. NULL: none */
+  uint32_t seg_ready_ticket; /* value this call stores into seg_ready; pick one the array
+                               does not hold yet (e.g. a per-call counter) */
+  int32_t reserved1;        /* must be 0 */
 } moe_config_t;
 
 /* Workspace bytes for `cfg` (first phase of [DISP]'s two-phase contract), and

@@ -40,9 +40,11 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_config_struct_layout_matches_header(lib):
     # 17 int32/int64 fields plus a pointer: offsets follow C layout rules
-    assert ctypes.sizeof(lib.MoeConfig) == 80
+    assert ctypes.sizeof(lib.MoeConfig) == 96
     assert lib.MoeConfig.bulk_min_bytes.offset == 48
     assert lib.MoeConfig.prof_events.offset == 72
+    assert lib.MoeConfig.seg_ready.offset == 80
+    assert lib.MoeConfig.seg_ready_ticket.offset == 88
 
 
 def test_workspace_query_and_capacity(lib):

@@ -298,3 +298,35 @@ def test_two_phase_wait_times_out_on_a_missing_flag():
     M.combine(cfg, got["expand_x"], got["assist_info"], got["ep_recv_count"], dev["expert_ids"],
               dev["expert_scales"], dev["active_mask"], dev["x"], x_out, None, ws)
     assert M.get_device_status(ws) == 0
+
+
+# ------------------------------------------------- dispatch ready flags
+
+@pytest.mark.parametrize("name,policy", [("w16_bs256_h7168_k8_e256_bf16_zipf", 0),
+                                         ("w16_bs256_h7168_k8_e256_bf16_zipf", 2),
+                                         ("w8_bs32_h7168_k8_e64_f16_q2", 2),
+                                         ("w8_bs8_h16_k2_e64_f16", 0),
+                                         ("ragged_h12_f16", 0)])
+def test_dispatch_ready_flags(name, policy):
+    """seg_ready[d][le*W+s] carries the call's ticket once segment (le, s) of
+    rank d is complete, for every segment (empty ones too); flags change no
+    output."""
+    if name == "ragged_h12_f16":
+        wl = WL.Workload(name, 4, 9, 12, 3, 8, WL.X_FP16, mask_kind=2, mask_false_p=0.2, seed=12)
+    else:
+        wl = WL.WORKLOADS[name]
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    L = wl.moe_expert_num // wl.ep_world_size
+    cfg = H.make_cfg(wl, plane_policy=policy, bulk_min_bytes=0 if policy == 0 and wl.h < 1024 else M.BULK_MIN_BYTES)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+    flags = torch.zeros((wl.ep_world_size, L * wl.ep_world_size), dtype=torch.int32, device="cuda")
+    for ticket in (7, 8):
+        c = M.with_seg_ready(cfg, flags, ticket)
+        M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
+                   out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws)
+        assert M.get_device_status(ws) == 0
+        assert bool((flags == ticket).all()), f"ticket {ticket}: {int((flags != ticket).sum())} segments not flagged"
+        H.compare_dispatch(wl, out, ref)
