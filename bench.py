@@ -39,6 +39,7 @@ import workloads as WL  # noqa: E402
 METRIC = "dispatch+combine GB/s and tokens/s on 1 GB300; fraction of 8 TB/s HBM roofline"
 DEFAULT_WORKLOAD = "w16_bs256_h7168_k8_e256_bf16_zipf"
 FFN_WORKLOAD = "w8_bs64_h2048_k8_e128_bf16_ffn"
+SMALL_WORKLOADS = ("w8_bs32_h7168_k8_e64_f16", "w8_bs32_h7168_k8_e64_f16_q2", "w8_bs32_h7168_k8_e64_i32")
 HBM_NOMINAL_GBPS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBPS = 6800.0
@@ -57,6 +58,9 @@ def parse_args():
     ap.add_argument("--ffn-workload", default=FFN_WORKLOAD, choices=sorted(WL.WORKLOADS))
     ap.add_argument("--no-ffn", action="store_true")
     ap.add_argument("--ffn-steps", type=int, default=100)
+    ap.add_argument("--small-workloads", default=",".join(SMALL_WORKLOADS),
+                    help="workloads that fit in L2, timed per call with an L2 flush before each step")
+    ap.add_argument("--small-steps", type=int, default=50)
     return ap.parse_args()
 
 
@@ -332,6 +336,109 @@ def measure_ffn(args, M, torch, stream):
             "steps": Kf}
 
 
+def measure_small(args, M, torch, stream):
+    """Workloads whose working set fits in L2: each step first writes a 512 MB
+    buffer (untimed) so dispatch and combine read and write HBM, then times
+    moe_dispatch and moe_combine separately with CUDA events."""
+    flush = torch.empty(512 * 1024 * 1024, dtype=torch.uint8, device="cuda")
+    res = {}
+    for name in [w for w in args.small_workloads.split(",") if w]:
+        wl = WL.WORKLOADS[name]
+        inp = WL.make_inputs(wl)
+        bf = wl.x_dtype == WL.X_BF16
+        tdt = {WL.X_INT32: torch.int32, WL.X_FP16: torch.float16, WL.X_BF16: torch.bfloat16}[wl.x_dtype]
+
+        def dev(a, as_bf=False):
+            if a is None:
+                return None
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if as_bf else np.ascontiguousarray(a))
+            return (t.view(torch.bfloat16) if as_bf else t).cuda()
+
+        x, ids, scales, mask = dev(inp["x"], bf), dev(inp["expert_ids"]), dev(inp["expert_scales"]), \
+            dev(inp.get("active_mask"))
+        cfg = M.config(wl.ep_world_size, wl.bs, wl.h, wl.topk, wl.moe_expert_num, tdt,
+                       zero_expert_num=wl.zero_expert_num, copy_expert_num=wl.copy_expert_num,
+                       quant_mode=wl.quant_mode, mask_kind=wl.mask_kind)
+        ws = M.alloc_workspace(cfg)
+        out = M.alloc_dispatch_outputs(cfg, tdt)
+        x_out = torch.empty_like(x)
+        n = max(3, args.small_steps)
+        ev = [[torch.cuda.Event(enable_timing=True) for _ in range(3)] for _ in range(n)]
+        for i in range(n + 3):
+            flush.fill_(i & 0xFF)
+            e = ev[i - 3] if i >= 3 else None
+            if e:
+                e[0].record(stream)
+            M.dispatch(cfg, x, ids, mask, scales, out["expand_x"], out["dynamic_scales"], out["assist_info"],
+                       out["ep_recv_count"], out["expand_scales"], None, ws)
+            if e:
+                e[1].record(stream)
+            if wl.quant_mode == 0:
+                M.combine(cfg, out["expand_x"], out["assist_info"], out["ep_recv_count"], ids, scales, mask, x,
+                          x_out, None, ws)
+            if e:
+                e[2].record(stream)
+        torch.cuda.synchronize()
+        st = M.get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {M.STATUS.get(st, st)} in {name}")
+        acct = algorithmic_bytes(wl, inp)
+        d_ms = statistics.median(e[0].elapsed_time(e[1]) for e in ev)
+        r = {"dispatch_ms": d_ms, "dispatch_GBps": acct["dispatch"] / (d_ms * 1e-3) / 1e9,
+             "dispatch_frac_of_8TBps": acct["dispatch"] / (d_ms * 1e-3) / 1e9 / HBM_NOMINAL_GBPS,
+             "dispatch_bytes": acct["dispatch"]}
+        if wl.quant_mode == 0:
+            c_ms = statistics.median(e[1].elapsed_time(e[2]) for e in ev)
+            r.update({"combine_ms": c_ms, "combine_GBps": acct["combine"] / (c_ms * 1e-3) / 1e9,
+                      "combine_frac_of_8TBps": acct["combine"] / (c_ms * 1e-3) / 1e9 / HBM_NOMINAL_GBPS,
+                      "combine_bytes": acct["combine"]})
+        r["steps"] = n
+        r["l2"] = "512 MB written before every step (untimed); median of per-call CUDA-event times"
+        del ws, out
+        # sustained: back-to-back steps rotating over independent buffer sets,
+        # enough of them that a set's data has left the L2 before it is reused
+        step_bytes = acct["dispatch"] + (acct["combine"] if wl.quant_mode == 0 else 0)
+        n_sets = max(2, int(np.ceil(4 * L2_BYTES / step_bytes)))
+        sets = []
+        for _ in range(n_sets):
+            st_ = {"x": x.clone(), "ids": ids.clone(), "scales": scales.clone(),
+                   "mask": None if mask is None else mask.clone(), "x_out": torch.empty_like(x),
+                   "ws": M.alloc_workspace(cfg), "out": M.alloc_dispatch_outputs(cfg, tdt)}
+            sets.append(st_)
+
+        def run_set(b):
+            o = b["out"]
+            M.dispatch(cfg, b["x"], b["ids"], b["mask"], b["scales"], o["expand_x"], o["dynamic_scales"],
+                       o["assist_info"], o["ep_recv_count"], o["expand_scales"], None, b["ws"])
+            if wl.quant_mode == 0:
+                M.combine(cfg, o["expand_x"], o["assist_info"], o["ep_recv_count"], b["ids"], b["scales"], b["mask"],
+                          b["x"], b["x_out"], None, b["ws"])
+
+        for i in range(2 * n_sets):
+            run_set(sets[i % n_sets])
+        torch.cuda.synchronize()
+        ks = max(n_sets, args.small_steps * 4)
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(ks):
+            run_set(sets[i % n_sets])
+        b.record(stream)
+        torch.cuda.synchronize()
+        for b_ in sets:
+            st = M.get_device_status(b_["ws"])
+            if st != 0:
+                raise RuntimeError(f"device status {M.STATUS.get(st, st)} in {name}")
+        sus_ms = a.elapsed_time(b) / ks
+        r["sustained"] = {"ms_per_step": sus_ms, "GBps": step_bytes / (sus_ms * 1e-3) / 1e9,
+                          "frac_of_8TBps": step_bytes / (sus_ms * 1e-3) / 1e9 / HBM_NOMINAL_GBPS,
+                          "steps": ks, "buffer_sets": n_sets,
+                          "what": "dispatch" + (" + combine" if wl.quant_mode == 0 else "")}
+        del sets
+        res[name] = r
+    del flush
+    return res
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -485,6 +592,7 @@ def run_ours(args):
         del ws_tp
 
     ffn = None if args.no_ffn or world > 1 else measure_ffn(args, M, torch, stream)
+    small = None if world > 1 or not args.small_workloads else measure_small(args, M, torch, stream)
 
     # End to end through the C ABI with host buffers: every step copies its
     # inputs from pinned host memory (H2D stream), runs dispatch + combine
@@ -600,6 +708,7 @@ def run_ours(args):
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "two_phase_combine": two_phase,
         "ffn_variant": ffn,
+        "small_workloads": small,
         "gpu_launches": K * (4 if wl.quant_mode == 0 else 2),
         "clocks": clocks,
     }

@@ -37,13 +37,16 @@ namespace cg = cooperative_groups;
 
 namespace crs {
 
-constexpr int kRouteThreads = 1024;
-constexpr int kRouteWarps = kRouteThreads / 32;
+constexpr int kRouteThreadsMax = 1024;
 constexpr int kScanTile = 4096;
 constexpr int kRegIters = 4;  // warp iterations whose keys walk 1 keeps in registers
 
-template <bool CLUSTER>
-__global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
+// THREADS: 256 for sources with at most 1024 picks (every warp then has at most
+// kRegIters iterations and barriers are short), else 1024.
+template <bool CLUSTER, int THREADS>
+__global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
+  constexpr int kRouteThreads = THREADS;
+  constexpr int kRouteWarps = THREADS / 32;
   extern __shared__ __align__(16) int32_t rsm[];  // wcnt [kRouteWarps][E], tot [E]; later the scan tiles
   __shared__ long long s_scan[32];
   __shared__ long long s_total;
@@ -198,18 +201,23 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
     cg::cluster_group cluster = cg::this_cluster();
     cluster.sync();
     const int d = s, LW = sh.L * sh.W;
-    long long c = 0;
-    if (tid < LW) {
-      const int le = tid / sh.W, sp = tid - le * sh.W;
-      const int32_t* remote_tot = cluster.map_shared_rank(tot, sp);
-      c = remote_tot[d * sh.L + le];
-    }
-    const long long ex = block_exclusive_scan(c, s_scan);
-    if (tid < LW) {
-      const size_t g = (size_t)d * LW + tid;
-      p.base[g] = (int32_t)ex;
-      p.ep_recv_count[g] = (int32_t)(ex + c);
-      if (tid == LW - 1 && ex + c > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
+    // thread tid owns the contiguous segments [j0, j1) of rank d
+    const int per = (LW + kRouteThreads - 1) / kRouteThreads;
+    const int j0 = min(LW, tid * per), j1 = min(LW, j0 + per);
+    auto seg_count = [&](int j) -> long long {
+      const int le = j / sh.W, sp = j - le * sh.W;
+      return cluster.map_shared_rank(tot, sp)[d * sh.L + le];
+    };
+    long long local = 0;
+    for (int j = j0; j < j1; ++j) local += seg_count(j);
+    long long run = block_exclusive_scan(local, s_scan);
+    for (int j = j0; j < j1; ++j) {
+      const long long c = seg_count(j);
+      const size_t g = (size_t)d * LW + j;
+      p.base[g] = (int32_t)run;
+      p.ep_recv_count[g] = (int32_t)(run + c);
+      run += c;
+      if (j == LW - 1 && run > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
     }
   }
 
@@ -290,25 +298,26 @@ __global__ void __launch_bounds__(kRouteThreads) route_kernel(RouteParams p) {
   if (tid == 0) *p.done = 0;  // ready for the next call (stream order)
 }
 
-static size_t route_smem(const Shape& sh) {
-  const size_t walk = (size_t)(kRouteWarps + 1) * sh.E * sizeof(int32_t);
+static size_t route_smem(const Shape& sh, int threads) {
+  const size_t walk = (size_t)(threads / 32 + 1) * sh.E * sizeof(int32_t);
   const size_t scan = (size_t)sh.W * sizeof(long long) + kScanTile * sizeof(int32_t);
   return walk > scan ? walk : scan;
 }
 
-// Is a cluster of W route CTAs schedulable on this device? Cached per (device, W).
+// Is a cluster of W route CTAs schedulable on this device? Cached per (device, W, size).
+template <int THREADS>
 static bool cluster_route_ok(int dev, int W, size_t smem) {
   static signed char ok[64][17] = {};
   if (W > 16) return false;
   if (ok[dev][W] != 0) return ok[dev][W] > 0;
-  bool good = cudaFuncSetAttribute(route_kernel<true>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
+  bool good = cudaFuncSetAttribute(route_kernel<true, THREADS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                   cudaSuccess &&
-              cudaFuncSetAttribute(route_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)((kRouteWarps + 1) * 1024 * sizeof(int32_t))) == cudaSuccess;
+              cudaFuncSetAttribute(route_kernel<true, THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                   (int)((THREADS / 32 + 1) * 1024 * sizeof(int32_t))) == cudaSuccess;
   if (good) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(W);
-    cfg.blockDim = dim3(kRouteThreads);
+    cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = smem;
     cudaLaunchAttribute a[1];
     a[0].id = cudaLaunchAttributeClusterDimension;
@@ -318,23 +327,20 @@ static bool cluster_route_ok(int dev, int W, size_t smem) {
     cfg.attrs = a;
     cfg.numAttrs = 1;
     int n = 0;
-    good = cudaOccupancyMaxActiveClusters(&n, route_kernel<true>, &cfg) == cudaSuccess && n >= 1;
+    good = cudaOccupancyMaxActiveClusters(&n, route_kernel<true, THREADS>, &cfg) == cudaSuccess && n >= 1;
   }
   cudaGetLastError();  // a refused query leaves no sticky error behind
   ok[dev][W] = good ? 1 : -1;
   return good;
 }
 
-cudaError_t launch_route(const RouteParams& p, cudaStream_t st) {
-  if (p.sh.K > 32) return cudaErrorInvalidValue;
-  int dev = 0;
-  cudaGetDevice(&dev);
-  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
-  const size_t walk = (size_t)(kRouteWarps + 1) * p.sh.E * sizeof(int32_t);
-  if (cluster_route_ok(dev, p.sh.W, walk)) {
+template <int THREADS>
+static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t st, int dev) {
+  const size_t walk = (size_t)(THREADS / 32 + 1) * p.sh.E * sizeof(int32_t);
+  if (cluster_route_ok<THREADS>(dev, p.sh.W, walk)) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.sh.W);
-    cfg.blockDim = dim3(kRouteThreads);
+    cfg.blockDim = dim3(THREADS);
     cfg.dynamicSmemBytes = walk;
     cfg.stream = st;
     cudaLaunchAttribute a[2];
@@ -346,17 +352,27 @@ cudaError_t launch_route(const RouteParams& p, cudaStream_t st) {
     a[1].val.programmaticStreamSerializationAllowed = 1;
     cfg.attrs = a;
     cfg.numAttrs = 2;
-    return cudaLaunchKernelEx(&cfg, route_kernel<true>, p);
+    return cudaLaunchKernelEx(&cfg, route_kernel<true, THREADS>, p);
   }
-  const size_t smem = route_smem(p.sh);
+  const size_t smem = route_smem(p.sh, THREADS);
   static size_t attr_bytes[64] = {};
   if (attr_bytes[dev] < smem) {
-    cudaError_t e = cudaFuncSetAttribute(route_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    cudaError_t e =
+        cudaFuncSetAttribute(route_kernel<false, THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
     if (e != cudaSuccess) return e;
     attr_bytes[dev] = smem;
   }
-  PdlLaunch L(dim3(p.sh.W), dim3(kRouteThreads), smem, st);
-  return cudaLaunchKernelEx(&L.cfg, route_kernel<false>, p);
+  PdlLaunch L(dim3(p.sh.W), dim3(THREADS), smem, st);
+  return cudaLaunchKernelEx(&L.cfg, route_kernel<false, THREADS>, p);
+}
+
+cudaError_t launch_route(const RouteParams& p, cudaStream_t st) {
+  if (p.sh.K > 32) return cudaErrorInvalidValue;
+  int dev = 0;
+  cudaGetDevice(&dev);
+  if (dev < 0 || dev >= 64) return cudaErrorInvalidDevice;
+  if ((long long)p.sh.bs * p.sh.K <= 1024) return launch_route_t<256>(p, st, dev);
+  return launch_route_t<kRouteThreadsMax>(p, st, dev);
 }
 
 }  // namespace crs
