@@ -433,7 +433,29 @@ def measure_small(args, M, torch, stream):
                           "frac_of_8TBps": step_bytes / (sus_ms * 1e-3) / 1e9 / HBM_NOMINAL_GBPS,
                           "steps": ks, "buffer_sets": n_sets,
                           "what": "dispatch" + (" + combine" if wl.quant_mode == 0 else "")}
-        del sets
+        # the same rotation captured once in a CUDA graph and replayed: no
+        # host launch cost per step
+        graph = torch.cuda.CUDAGraph()
+        with torch.cuda.graph(graph):
+            for i in range(n_sets):
+                run_set(sets[i])
+        graph.replay()
+        torch.cuda.synchronize()
+        reps = max(1, ks // n_sets)
+        a.record(stream)
+        for _ in range(reps):
+            graph.replay()
+        b.record(stream)
+        torch.cuda.synchronize()
+        for b_ in sets:
+            st = M.get_device_status(b_["ws"])
+            if st != 0:
+                raise RuntimeError(f"device status {M.STATUS.get(st, st)} in {name} (graph)")
+        g_ms = a.elapsed_time(b) / (reps * n_sets)
+        r["sustained_graph"] = {"ms_per_step": g_ms, "GBps": step_bytes / (g_ms * 1e-3) / 1e9,
+                                "frac_of_8TBps": step_bytes / (g_ms * 1e-3) / 1e9 / HBM_NOMINAL_GBPS,
+                                "steps": reps * n_sets}
+        del graph, sets
         res[name] = r
     del flush
     return res
@@ -520,6 +542,25 @@ def run_ours(args):
             torch.cuda.synchronize()
         h_ext = time.time()
     total_ms = max_over_ranks(total_ms, world)
+
+    # The same K steps replayed from a CUDA graph of one step (no host launch
+    # cost per step); reported beside region A.
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph):
+        step(cfg, cfg)
+    graph.replay()
+    torch.cuda.synchronize()
+    g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    if world > 1:
+        dist.barrier()
+    torch.cuda.synchronize()
+    g0.record(stream)
+    for k in range(K):
+        graph.replay()
+    g1.record(stream)
+    torch.cuda.synchronize()
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world) / K
+    del graph
 
     # Timed region B (kernel attribution): the same K steps with CUDA events the
     # library records on the launching stream around the scatter and the
@@ -697,6 +738,7 @@ def run_ours(args):
         "dispatch_bytes": acct["dispatch"], "combine_bytes": acct["combine"], "routed_picks": acct["P"],
         "scatter_ms": scatter_ms, "combine_reduce_ms": reduce_ms,
         "instrumented_ms_per_step": instrumented_ms,
+        "graph_ms_per_step": graph_ms,
         "scatter_GBps": acct["scatter"] / (scatter_ms * 1e-3) / 1e9,
         "combine_reduce_GBps": acct["reduce"] / (reduce_ms * 1e-3) / 1e9 if reduce_ms else None,
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",

@@ -60,9 +60,10 @@ __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, 
   long long dst = -1;
   int bulk = 0;
   if (lane < sh.K) {
+    // position and id are independent loads: issue both before using either
     const int r = p.rank[tau * sh.K + lane];
+    const int e = p.ids[tau * sh.K + lane];
     if (r >= 0) {
-      const int e = p.ids[tau * sh.K + lane];
       const int d = e / sh.L;
       const size_t g = (size_t)e * sh.W + s;
       const long long row = (long long)p.base[g] + r;
