@@ -16,7 +16,9 @@ struct WsHeader {
   uint32_t epoch;       // two-phase combine flag epoch (last completed call)
   uint32_t route_done;  // route CTAs finished in the current dispatch
   uint32_t tp_done;     // two-phase combine CTAs finished in the current call
-  uint32_t pad[60];
+  unsigned long long perf_start_inv;  // ~(earliest scatter CTA start), kept with atomicMax
+  uint32_t scatter_done;              // scatter CTAs finished (performance info)
+  uint32_t pad[57];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -26,6 +28,7 @@ struct WsLayout {
   size_t base;     // int32 [E*W]     first row of segment g inside its rank
   size_t plane_d;  // uint8 [E*W]     dispatch plane per segment
   size_t landed;   // uint32 [E*W]    dispatch rows in place per segment (ready flags)
+  size_t perf_end; // uint64 [W]      latest row-store time per source rank (performance info)
   size_t rank;     // int32 [W*bs*K]  position of a routed pick inside its segment
   size_t inv;      // int32 [W*bs*K]  combine: flat expert-output row of each pick
   size_t plane_c;  // uint8 [E*W]     two-phase combine plane per segment
@@ -85,6 +88,9 @@ struct ScatterParams {
   uint32_t* landed;        // per-segment rows in place
   uint32_t* seg_ready;     // optional ready flags
   uint32_t ticket;
+  int64_t* perf;                   // per-rank communication time (user array [W]), or null
+  unsigned long long* perf_end;    // [W] workspace
+  WsHeader* hdr;
   Shape sh;
   int* status;
   uint64_t timeout_ns;

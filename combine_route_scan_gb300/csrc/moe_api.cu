@@ -74,6 +74,7 @@ WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
   L.base = take(segs * 4);
   L.plane_d = take(segs);
   L.landed = take(segs * 4);
+  L.perf_end = take((size_t)sh.W * 8);
   L.rank = take(picks * 4);
   L.inv = take(picks * 4);
   if (c->combine_mode != MOE_COMBINE_GATHER) {
@@ -142,6 +143,8 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.perf_end, 0, (size_t)sh.W * 8, s) != cudaSuccess)
+    return MOE_ERR_CUDA;
   if (L.flags && cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.flags, 0,
                                  (size_t)sh.W * sh.bs * sh.K * 4, s) != cudaSuccess)
     return MOE_ERR_CUDA;
@@ -163,7 +166,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (sh.quant == 2 && !dynamic_scales) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4) ||
       !aligned(assist_info, 4) || !aligned(ep_recv_count, 4) || !aligned(expand_scales, 4) ||
-      !aligned(dynamic_scales, 4) || !aligned(cfg->seg_ready, 4))
+      !aligned(dynamic_scales, 4) || !aligned(cfg->seg_ready, 4) || !aligned(cfg->performance_info, 8))
     return MOE_ERR_INVALID_ARG;
   WsLayout L;
   st = check_ws(cfg, sh, ws, ws_bytes, &L);
@@ -201,6 +204,9 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.landed = rp.landed;
   sp.seg_ready = cfg->seg_ready;
   sp.ticket = cfg->seg_ready_ticket;
+  sp.perf = cfg->performance_info;
+  sp.perf_end = reinterpret_cast<unsigned long long*>(w + L.perf_end);
+  sp.hdr = hdr;
   sp.x = x;
   sp.ids = expert_ids;
   sp.mask = rp.mask;

@@ -177,6 +177,37 @@ __device__ __forceinline__ void publish_earlier(const ScatterParams& p, const Pi
   }
 }
 
+// Per-rank communication time (performance info): the earliest CTA start,
+// the latest row-store time per source rank, and the last CTA to finish adds
+// each rank's span to the caller's array and resets the workspace fields.
+__device__ __forceinline__ void perf_begin(const ScatterParams& p) {
+  atomicMax(&p.hdr->perf_start_inv, ~(unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void perf_mark(const ScatterParams& p, size_t tau) {
+  atomicMax(p.perf_end + tau / p.sh.bs, (unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void perf_finish(const ScatterParams& p, int* s_last) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *s_last = atomicAdd(&p.hdr->scatter_done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    const unsigned long long start = ~atomicAdd(&p.hdr->perf_start_inv, 0ull);
+    for (int s = threadIdx.x; s < p.sh.W; s += blockDim.x) {
+      const unsigned long long end = atomicExch(p.perf_end + s, 0ull);
+      if (end > start) p.perf[s] += (long long)(end - start);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      p.hdr->perf_start_inv = 0ull;
+      p.hdr->scatter_done = 0u;
+    }
+  }
+}
+
 // QUANT: 0 or 2; DT: element type for the quantiser (MOE_F16 / MOE_BF16).
 template <int QUANT, int DT, int STAGES>
 __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterParams p) {
@@ -215,6 +246,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
   }
   pdl_wait();  // routing results are visible from here on
   pdl_launch_dependents();
+  if (p.perf && tid == 0) perf_begin(p);
 
   for (int i = 0; i < my_n; ++i) {
     const size_t tau = blockIdx.x + (size_t)i * G;
@@ -240,6 +272,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
       __syncthreads();
       if (s_abort) break;
       if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
+      if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
       float amax = 0.f;
 #pragma unroll
       for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[i & 1][w]);
@@ -279,6 +312,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
       __syncthreads();
       if (s_abort) break;
       if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
+      if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
       const int nb = tab.n_bulk, ns = tab.n_sm;
       if (tid == 0) {
         // refill the slot of the previous token once its bulk group has read it
@@ -321,6 +355,11 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     }
   }
   if (tid == 0) bulk_wait_all<0>();
+  if (p.perf) {
+    if (tid == 0 && my_n > 0 && !s_abort) perf_mark(p, blockIdx.x + (size_t)(my_n - 1) * G);
+    __shared__ int s_last;
+    perf_finish(p, &s_last);
+  }
 }
 
 // Fallback for rows that are not 16-byte multiples: element-wise copies, all
@@ -334,6 +373,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
   const int n_tok = sh.W * sh.bs;
   pdl_wait();
   pdl_launch_dependents();
+  if (p.perf && tid == 0) perf_begin(p);
   for (size_t tau = blockIdx.x; tau < (size_t)n_tok; tau += gridDim.x) {
     const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
     float scale = 0.f, amax = 0.f;
@@ -396,7 +436,12 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
       __threadfence();
       for (int k = 0; k < ns; ++k) publish_row(p, tab.sm_seg[k]);
     }
+    if (p.perf && tid == 0) perf_mark(p, tau);
     __syncthreads();
+  }
+  if (p.perf) {
+    __shared__ int s_last;
+    perf_finish(p, &s_last);
   }
 }
 

@@ -53,6 +53,7 @@ class MoeConfig(ctypes.Structure):
         ("ffn_intermediate", ctypes.c_int32), ("reserved0", ctypes.c_int32),
         ("prof_events", ctypes.c_void_p), ("seg_ready", ctypes.c_void_p),
         ("seg_ready_ticket", ctypes.c_uint32), ("reserved1", ctypes.c_int32),
+        ("performance_info", ctypes.c_void_p),
     ]
 
 
@@ -64,7 +65,7 @@ def config(ep_world_size: int, bs: int, h: int, topk: int, moe_expert_num: int, 
     dt = DTYPE_CODE[x_dtype] if isinstance(x_dtype, torch.dtype) else int(x_dtype)
     return MoeConfig(ep_world_size, bs, h, topk, moe_expert_num, zero_expert_num, copy_expert_num, 0,
                      quant_mode, mask_kind, dt, plane_policy, bulk_min_bytes, combine_mode, wait_timeout_us,
-                     ffn_intermediate, 0, None, None, 0, 0)
+                     ffn_intermediate, 0, None, None, 0, 0, None)
 
 
 _lib = None
@@ -143,6 +144,14 @@ def with_seg_ready(cfg: MoeConfig, seg_ready: torch.Tensor, ticket: int) -> MoeC
     c = MoeConfig.from_buffer_copy(cfg)
     c.seg_ready = ctypes.c_void_p(_ptr(seg_ready).value)
     c.seg_ready_ticket = ticket
+    return c
+
+
+def with_performance_info(cfg: MoeConfig, perf: torch.Tensor) -> MoeConfig:
+    """A copy of cfg whose dispatch adds each rank's communication time (ns)
+    to perf (int64 CUDA tensor [W])."""
+    c = MoeConfig.from_buffer_copy(cfg)
+    c.performance_info = ctypes.c_void_p(_ptr(perf).value)
     return c
 
 

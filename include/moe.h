@@ -114,6 +114,13 @@ typedef struct {
   uint32_t seg_ready_ticket; /* value this call stores into seg_ready; pick one the array
                                does not hold yet (e.g. a per-call counter) */
   int32_t reserved1;        /* must be 0 */
+  int64_t* performance_info; /* optional device array [W] int64 (moe_dispatch only; [DISP]
+                               参数说明 performanceInfoOptional): each call ADDS to entry s
+                               rank s's communication time in nanoseconds (%globaltimer), from
+                               the earliest payload-CTA start to the moment the stores of rank
+                               s's last token were issued by every thread (for a CTA's final
+                               token: completed). The caller clears it when it wants to.
+                               8-byte aligned, else MOE_ERR_INVALID_ARG. NULL: off */
 } moe_config_t;
 
 /* Workspace bytes for `cfg` (first phase of [DISP]'s two-phase contract), and

@@ -40,11 +40,12 @@ def test_library_exports_every_declared_symbol(lib):
 
 def test_config_struct_layout_matches_header(lib):
     # 17 int32/int64 fields plus a pointer: offsets follow C layout rules
-    assert ctypes.sizeof(lib.MoeConfig) == 96
+    assert ctypes.sizeof(lib.MoeConfig) == 104
     assert lib.MoeConfig.bulk_min_bytes.offset == 48
     assert lib.MoeConfig.prof_events.offset == 72
     assert lib.MoeConfig.seg_ready.offset == 80
     assert lib.MoeConfig.seg_ready_ticket.offset == 88
+    assert lib.MoeConfig.performance_info.offset == 96
 
 
 def test_workspace_query_and_capacity(lib):

@@ -5,6 +5,8 @@ outputs within max |gpu - oracle| <= 1e-3 * max |oracle|. The kernels fix the
 fp32 accumulation order (k ascending, fused multiply-add), so the float
 outputs are also checked for bit equality.
 """
+import time
+
 import numpy as np
 import pytest
 import torch
@@ -331,3 +333,61 @@ def test_dispatch_ready_flags(name, policy):
         assert M.get_device_status(ws) == 0
         assert bool((flags == ticket).all()), f"ticket {ticket}: {int((flags != ticket).sum())} segments not flagged"
         H.compare_dispatch(wl, out, ref)
+
+
+# ------------------------------------------------- dispatch performance info
+
+@pytest.mark.parametrize("name", ["w16_bs256_h7168_k8_e256_bf16_zipf", "w8_bs32_h7168_k8_e64_f16_q2",
+                                  "ragged_h12_f16", "empty_batch"])
+def test_dispatch_performance_info(name):
+    """performance_info[s] gains rank s's communication time (ns) on every
+    call: never negative, never longer than the host-timed calls, growing
+    across calls, zero for an empty batch; outputs are unchanged."""
+    if name == "ragged_h12_f16":
+        wl = WL.Workload(name, 4, 9, 12, 3, 8, WL.X_FP16, mask_kind=2, mask_false_p=0.2, seed=12)
+    elif name == "empty_batch":
+        wl = WL.Workload(name, 4, 0, 256, 2, 8, WL.X_BF16, seed=13)
+    else:
+        wl = WL.WORKLOADS[name]
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    cfg = H.make_cfg(wl)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+    perf = torch.zeros(wl.ep_world_size, dtype=torch.int64, device="cuda")
+    c = M.with_performance_info(cfg, perf)
+    prev = np.zeros(wl.ep_world_size, dtype=np.int64)
+    torch.cuda.synchronize()
+    t0 = time.perf_counter_ns()
+    for _ in range(3):
+        M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
+                   out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws)
+        assert M.get_device_status(ws) == 0
+        cur = perf.cpu().numpy()
+        assert (cur >= prev).all(), (prev, cur)
+        prev = cur
+    elapsed = time.perf_counter_ns() - t0
+    if wl.bs == 0:
+        assert not prev.any()
+        return
+    H.compare_dispatch(wl, out, ref)
+    assert prev.max() <= elapsed, (prev.max(), elapsed)
+    if wl.ep_world_size * wl.bs >= 1024:
+        # a multi-microsecond scatter: every rank's span is measurable
+        assert (prev > 0).all(), prev
+
+
+def test_dispatch_performance_info_alignment():
+    wl = WL.Workload("perf_align", 2, 4, 64, 2, 4, WL.X_FP16, seed=14)
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    cfg = H.make_cfg(wl)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+    buf = torch.zeros(8, dtype=torch.int32, device="cuda")
+    c = M.with_performance_info(cfg, buf[1:])  # 4-byte aligned only
+    with pytest.raises(M.MoeError) as ei:
+        M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
+                   out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws)
+    assert ei.value.name == "INVALID_ARG"
