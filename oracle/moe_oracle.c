@@ -31,6 +31,24 @@
  *   - quantMode 2: per token amax = max |x| (fp32), scale = amax / 127 (IEEE
  *     fp32 division), q = clamp(round_half_even(x / scale), -127, 127); amax 0
  *     gives scale 0 and q 0;
+ *   - the optional scales input ([DISP] 参数说明 scalesOptional and the
+ *     quantMode constraints): one fp32 per element, shaped (1,), (H,) or
+ *     (E, H); for quantMode 1 it is the static quantisation coefficient,
+ *     q = clamp(round_half_even(x * s), -128, 127) (a saturating int8 cast);
+ *     for quantMode 2 and 3 it is the smoothing weight of the pick's expert
+ *     (shape (E, H)), applied as x' = x * s[e] (fp32) before the dynamic
+ *     quantisation, so rows of one token sent to different experts differ;
+ *   - quantMode 3 (per-group dynamic): groups of 128 consecutive elements of a
+ *     row (the last one may be shorter), scale_g = amax_g / FMAX (FMAX = 448
+ *     for FP8 E4M3, 57344 for FP8 E5M2), q = fp8(x / scale_g) rounded to
+ *     nearest even with saturation to +-FMAX; amax_g 0 gives scale 0 and +0;
+ *   - quantMode 4 (MX, the OCP Microscaling v1.0 conversion): blocks of 32
+ *     elements share X = 2^(floor(log2 amax_b) - emax_elem), clamped to
+ *     [2^-127, 2^127] and stored as an E8M0 byte (exponent + 127); elements
+ *     are x / X rounded to nearest even in the element format (FP8 E4M3,
+ *     emax 8; FP8 E5M2, emax 15; FP4 E2M1, emax 2; two FP4 codes per byte,
+ *     the even element in the low nibble) with saturation to the largest
+ *     finite value; a zero block gets byte 0;
  *   - FFN variant: SwiGLU, y = (silu(x Wg^T) * (x Wu^T)) Wd^T with weights stored
  *     out-major (w_gate, w_up [E][I][h], w_down [E][h][I]), evaluated in fp64.
  *
@@ -55,6 +73,10 @@ enum {
 };
 
 enum { ORC_X_INT32 = 0, ORC_X_FP16 = 1, ORC_X_BF16 = 2 };
+/* Element type of a quantised expand_x row. */
+enum { ORC_Y_INT8 = 0, ORC_Y_FP8_E4M3 = 1, ORC_Y_FP8_E5M2 = 2, ORC_Y_FP4_E2M1 = 3 };
+/* Shape of the scales input: none, (1,), (H,), (E, H). */
+enum { ORC_SC_NONE = 0, ORC_SC_SCALAR = 1, ORC_SC_CHANNEL = 2, ORC_SC_EXPERT = 3 };
 enum { PICK_BAD = -1, PICK_INACTIVE = 0, PICK_ZERO = 1, PICK_COPY = 2, PICK_ROUTED = 3 };
 
 typedef struct {
@@ -65,10 +87,12 @@ typedef struct {
   int32_t E;           /* moeExpertNum (routed experts) */
   int32_t Z;           /* zeroExpertNum */
   int32_t C;           /* copyExpertNum */
-  int32_t quant_mode;  /* 0 or 2 */
+  int32_t quant_mode;  /* 0 none, 1 static int8, 2 per-token int8, 3 per-group fp8, 4 MX */
   int32_t mask_kind;   /* 0 none, 1 (bs,), 2 (bs, K) */
   int32_t x_kind;      /* ORC_X_* */
   int64_t bulk_min_bytes; /* plane-2 size threshold (2 MB on the page) */
+  int32_t y_kind;      /* ORC_Y_*: element type of quantised rows (modes 3, 4) */
+  int32_t scales_kind; /* ORC_SC_*: shape of the scales input */
 } orc_cfg;
 
 /* ---------------------------------------------------------------- scalars */
@@ -126,9 +150,38 @@ int orc_check_cfg(const orc_cfg* c) {
   if ((int64_t)c->E + c->Z + c->C >= 2147483647LL) return ORC_ERR_INVALID_ARG;
   if (c->mask_kind < 0 || c->mask_kind > 2) return ORC_ERR_INVALID_ARG;
   if (c->x_kind < 0 || c->x_kind > 2) return ORC_ERR_INVALID_ARG;
-  if (c->quant_mode != 0 && c->quant_mode != 2) return ORC_ERR_UNSUPPORTED;
-  if (c->quant_mode == 2 && c->x_kind == ORC_X_INT32) return ORC_ERR_UNSUPPORTED;
+  if (c->quant_mode < 0 || c->quant_mode > 4) return ORC_ERR_UNSUPPORTED;
+  if (c->y_kind < 0 || c->y_kind > 3 || c->scales_kind < 0 || c->scales_kind > 3) return ORC_ERR_INVALID_ARG;
+  if (c->quant_mode == 0) {
+    if (c->y_kind != ORC_Y_INT8 || c->scales_kind != ORC_SC_NONE) return ORC_ERR_INVALID_ARG;
+    return ORC_OK;
+  }
+  if (c->x_kind == ORC_X_INT32) return ORC_ERR_UNSUPPORTED;
+  switch (c->quant_mode) {
+    case 1: /* static: int8 out, a coefficient of any of the three shapes */
+      if (c->y_kind != ORC_Y_INT8 || c->scales_kind == ORC_SC_NONE) return ORC_ERR_INVALID_ARG;
+      break;
+    case 2: /* per token: int8 out, optional per-expert smoothing */
+      if (c->y_kind != ORC_Y_INT8) return ORC_ERR_INVALID_ARG;
+      if (c->scales_kind != ORC_SC_NONE && c->scales_kind != ORC_SC_EXPERT) return ORC_ERR_INVALID_ARG;
+      break;
+    case 3: /* per group: fp8 out, optional per-expert smoothing */
+      if (c->y_kind != ORC_Y_FP8_E4M3 && c->y_kind != ORC_Y_FP8_E5M2) return ORC_ERR_INVALID_ARG;
+      if (c->scales_kind != ORC_SC_NONE && c->scales_kind != ORC_SC_EXPERT) return ORC_ERR_INVALID_ARG;
+      break;
+    default: /* MX: fp8 or fp4 out, no scales input; fp4 rows pack two codes a byte */
+      if (c->y_kind == ORC_Y_INT8 || c->scales_kind != ORC_SC_NONE) return ORC_ERR_INVALID_ARG;
+      if (c->y_kind == ORC_Y_FP4_E2M1 && c->h % 2) return ORC_ERR_INVALID_ARG;
+      break;
+  }
   return ORC_OK;
+}
+
+/* Bytes of one expand_x row. */
+static int64_t row_out_bytes(const orc_cfg* c) {
+  if (c->quant_mode == 0) return (int64_t)c->h * elem_bytes(c);
+  if (c->quant_mode == 4 && c->y_kind == ORC_Y_FP4_E2M1) return c->h / 2;
+  return c->h;
 }
 
 int64_t orc_capacity(const orc_cfg* c) {
@@ -171,23 +224,130 @@ static int check_mask_order(const orc_cfg* c, const uint8_t* mask) {
   return ORC_OK;
 }
 
-/* Per-token dynamic int8 quantisation (quantMode 2). */
-static float quantize_row(const orc_cfg* c, const void* x, size_t row, int8_t* q) {
-  float amax = 0.0f;
-  for (int j = 0; j < c->h; ++j) {
-    float a = fabsf(load_f(c, x, row * c->h + j));
-    if (a > amax) amax = a;
-  }
-  float scale = amax / 127.0f;
-  for (int j = 0; j < c->h; ++j) {
-    if (amax == 0.0f) { q[j] = 0; continue; }
-    float r = nearbyintf(load_f(c, x, row * c->h + j) / scale);
-    if (r > 127.0f) r = 127.0f;
-    if (r < -127.0f) r = -127.0f;
-    q[j] = (int8_t)r;
-  }
-  return scale;
+/* Format of a small binary float: exponent / mantissa widths, bias, largest
+ * finite magnitude and its code (FP8 E4M3 keeps S.1111.111 for NaN; E5M2 and
+ * E2M1 follow the IEEE pattern; E2M1 has no inf or NaN). */
+typedef struct { int mb, bias; double maxv; int max_code, sign_bit; } minifloat_fmt;
+
+static minifloat_fmt fmt_of(int y_kind) {
+  minifloat_fmt f;
+  if (y_kind == ORC_Y_FP8_E4M3) { f.mb = 3; f.bias = 7; f.maxv = 448.0; f.max_code = 0x7E; f.sign_bit = 0x80; }
+  else if (y_kind == ORC_Y_FP8_E5M2) { f.mb = 2; f.bias = 15; f.maxv = 57344.0; f.max_code = 0x7B; f.sign_bit = 0x80; }
+  else { f.mb = 1; f.bias = 1; f.maxv = 6.0; f.max_code = 0x7; f.sign_bit = 0x8; }
+  return f;
 }
+
+/* Finite fp32 -> the nearest value of the format, ties to the even code,
+ * magnitudes at or above the largest finite value saturate to it. The sign
+ * is kept (a negative value that rounds to zero gives the negative zero). */
+static uint8_t f32_to_minifloat(float v, int y_kind) {
+  minifloat_fmt f = fmt_of(y_kind);
+  int neg = signbit(v) != 0;
+  double a = fabs((double)v);
+  int code;
+  if (a >= f.maxv) {
+    code = f.max_code;
+  } else {
+    int emin = 1 - f.bias;   /* exponent of the smallest normal */
+    int e;
+    if (a < ldexp(1.0, emin)) e = emin;                 /* subnormal: fixed quantum */
+    else { int ex; frexp(a, &ex); e = ex - 1; }          /* a in [2^e, 2^(e+1)) */
+    double quantum = ldexp(1.0, e - f.mb);
+    double n = nearbyint(a / quantum);                  /* exact quotient, RNE */
+    /* subnormals: the code is n itself; normals: biased exponent field plus
+     * the mantissa, and a carry out of the mantissa moves to the next binade */
+    if (e == emin && a < ldexp(1.0, emin)) code = (int)n;
+    else code = ((e + f.bias) << f.mb) + (int)n - (1 << f.mb);
+    if (code > f.max_code) code = f.max_code;
+  }
+  return (uint8_t)(code | (neg ? f.sign_bit : 0));
+}
+
+/* Element j of a row, multiplied by the smoothing / static coefficient that
+ * applies to it (quant_scales is NULL or shaped as scales_kind says). */
+static float scaled_elem(const orc_cfg* c, const void* x, size_t row, int j, int32_t e,
+                         const float* quant_scales) {
+  float v = load_f(c, x, row * c->h + j);
+  switch (c->scales_kind) {
+    case ORC_SC_SCALAR: return v * quant_scales[0];
+    case ORC_SC_CHANNEL: return v * quant_scales[j];
+    case ORC_SC_EXPERT: return v * quant_scales[(size_t)e * c->h + j];
+    default: return v;
+  }
+}
+
+/* Quantise row `row` of x for a pick of expert e (quantMode 1..4). Writes the
+ * row's row_out_bytes(c) bytes to q and its dynamic scales to dyn (mode 2: one
+ * fp32; mode 3: ceil(h/128) fp32; mode 4: ceil(h/32) E8M0 bytes; mode 1:
+ * nothing). */
+static void quantize_pick(const orc_cfg* c, const void* x, size_t row, int32_t e, const float* quant_scales,
+                          uint8_t* q, void* dyn) {
+  const int h = c->h;
+  float* xs = (float*)malloc((size_t)h * sizeof(float));
+  for (int j = 0; j < h; ++j) xs[j] = scaled_elem(c, x, row, j, e, quant_scales);
+  if (c->quant_mode == 1) {
+    for (int j = 0; j < h; ++j) {
+      float r = nearbyintf(xs[j]);
+      if (r > 127.0f) r = 127.0f;
+      if (r < -128.0f) r = -128.0f;
+      q[j] = (uint8_t)(int8_t)r;
+    }
+  } else if (c->quant_mode == 2) {
+    float amax = 0.0f;
+    for (int j = 0; j < h; ++j) if (fabsf(xs[j]) > amax) amax = fabsf(xs[j]);
+    float scale = amax / 127.0f;
+    for (int j = 0; j < h; ++j) {
+      float r = amax == 0.0f ? 0.0f : nearbyintf(xs[j] / scale);
+      if (r > 127.0f) r = 127.0f;
+      if (r < -127.0f) r = -127.0f;
+      q[j] = (uint8_t)(int8_t)r;
+    }
+    if (dyn) ((float*)dyn)[0] = scale;
+  } else if (c->quant_mode == 3) {
+    const float fmax = c->y_kind == ORC_Y_FP8_E4M3 ? 448.0f : 57344.0f;
+    for (int g0 = 0; g0 < h; g0 += 128) {
+      int g1 = g0 + 128 < h ? g0 + 128 : h;
+      float amax = 0.0f;
+      for (int j = g0; j < g1; ++j) if (fabsf(xs[j]) > amax) amax = fabsf(xs[j]);
+      float scale = amax / fmax;
+      for (int j = g0; j < g1; ++j) q[j] = amax == 0.0f ? 0 : f32_to_minifloat(xs[j] / scale, c->y_kind);
+      if (dyn) ((float*)dyn)[g0 / 128] = scale;
+    }
+  } else {
+    const int emax = c->y_kind == ORC_Y_FP8_E4M3 ? 8 : c->y_kind == ORC_Y_FP8_E5M2 ? 15 : 2;
+    if (c->y_kind == ORC_Y_FP4_E2M1) memset(q, 0, (size_t)h / 2);
+    for (int b0 = 0; b0 < h; b0 += 32) {
+      int b1 = b0 + 32 < h ? b0 + 32 : h;
+      float amax = 0.0f;
+      for (int j = b0; j < b1; ++j) if (fabsf(xs[j]) > amax) amax = fabsf(xs[j]);
+      int se = -127;
+      if (amax > 0.0f) {
+        int ex;
+        frexpf(amax, &ex);          /* amax in [2^(ex-1), 2^ex) */
+        se = (ex - 1) - emax;
+        if (se < -127) se = -127;
+        if (se > 127) se = 127;
+      }
+      float X = ldexpf(1.0f, se);
+      for (int j = b0; j < b1; ++j) {
+        uint8_t code = f32_to_minifloat(xs[j] / X, c->y_kind);
+        if (c->y_kind == ORC_Y_FP4_E2M1) q[j / 2] |= (uint8_t)(code << (4 * (j % 2)));
+        else q[j] = code;
+      }
+      if (dyn) ((uint8_t*)dyn)[b0 / 32] = (uint8_t)(se + 127);
+    }
+  }
+  free(xs);
+}
+
+/* Entries of dynamic scales per expand_x row (and their bytes). */
+static int64_t dyn_per_row(const orc_cfg* c) {
+  if (c->quant_mode == 2) return 1;
+  if (c->quant_mode == 3) return (c->h + 127) / 128;
+  if (c->quant_mode == 4) return (c->h + 31) / 32;
+  return 0;
+}
+static int dyn_elem_bytes(const orc_cfg* c) { return c->quant_mode == 4 ? 1 : 4; }
 
 /* ------------------------------------------------------------------ dispatch
  *
@@ -198,18 +358,22 @@ static float quantize_row(const orc_cfg* c, const void* x, size_t row, int8_t* q
  *   x             [W][bs][h]          expert_ids [W][bs][K]
  *   mask          [W][bs] / [W][bs][K] or NULL
  *   scales        [W][bs][K] (int32 for int32 x, else fp32), may be NULL
- *   expand_x      [W][A][h] (int8 for quantMode 2)
- *   dyn_scales    [W][A] fp32, quantMode 2 only (may be NULL otherwise)
+ *   quant_scales  fp32 (1,), (h,) or (E, h) as scales_kind says, or NULL
+ *   expand_x      [W][A][row_out_bytes] (x's type unquantised; int8, fp8 or
+ *                 packed fp4 codes otherwise)
+ *   dyn_scales    [W][A][dyn_per_row] (fp32; E8M0 bytes for quantMode 4), or
+ *                 NULL; quantMode 0 and 1 have none
  *   assist        [W][A][3] int32 = (src_rank, src_token, src_topk)
  *   ep_recv_count [W][L*W] int32
  *   expand_scales [W][A] (the pick's weight), may be NULL
  * Rows at or beyond ep_recv_count[d][L*W-1] are left untouched.
  */
 int orc_dispatch(const orc_cfg* c, const void* x, const int32_t* ids, const uint8_t* mask,
-                 const void* scales, void* expand_x, float* dyn_scales, int32_t* assist,
-                 int32_t* ep_recv_count, void* expand_scales) {
+                 const void* scales, const float* quant_scales, void* expand_x, void* dyn_scales,
+                 int32_t* assist, int32_t* ep_recv_count, void* expand_scales) {
   int st = orc_check_cfg(c);
   if (st) return st;
+  if (c->scales_kind != ORC_SC_NONE && quant_scales == NULL) return ORC_ERR_INVALID_ARG;
   const int W = c->W, bs = c->bs, h = c->h, K = c->K, E = c->E, L = E / W;
   const int64_t A = orc_capacity(c);
   const int es = elem_bytes(c);
@@ -255,22 +419,19 @@ int orc_dispatch(const orc_cfg* c, const void* x, const int32_t* ids, const uint
   }
 
   /* 3. place every routed pick: rows of a segment in (t, k) order */
-  int8_t* qrow = (int8_t*)malloc((size_t)h);
+  const int64_t rob = row_out_bytes(c), nd = dyn_per_row(c), db = dyn_elem_bytes(c);
   for (int s = 0; s < W; ++s)
     for (int t = 0; t < bs; ++t) {
       size_t src = (size_t)s * bs + t;
-      float qscale = 0.0f;
-      int have_q = 0;
       for (int k = 0; k < K; ++k) {
         int32_t e = -1;
         if (classify(c, ids, mask, s, t, k, &e) != PICK_ROUTED) continue;
         int d = e / L;
         size_t g = (size_t)e * W + s;
         size_t row = (size_t)d * A + (size_t)next[g]++;
-        if (c->quant_mode == 2) {
-          if (!have_q) { qscale = quantize_row(c, x, src, qrow); have_q = 1; }
-          memcpy((int8_t*)expand_x + row * h, qrow, (size_t)h);
-          if (dyn_scales) dyn_scales[row] = qscale;
+        if (c->quant_mode != 0) {
+          quantize_pick(c, x, src, e, quant_scales, (uint8_t*)expand_x + row * rob,
+                        dyn_scales ? (char*)dyn_scales + row * nd * db : NULL);
         } else {
           memcpy((char*)expand_x + row * h * es, (const char*)x + src * h * es, (size_t)h * es);
         }
@@ -281,7 +442,6 @@ int orc_dispatch(const orc_cfg* c, const void* x, const int32_t* ids, const uint
           memcpy((char*)expand_scales + row * 4, (const char*)scales + (src * K + k) * 4, 4);
       }
     }
-  free(qrow);
   free(cnt);
   free(next);
   return ORC_OK;
@@ -331,13 +491,13 @@ int orc_combine_plane(const orc_cfg* c, const int32_t* ep_recv_count, uint8_t* p
 }
 
 /* Dispatch, by symmetry: the writer is source s; remote_tokens = rows that s
- * sends to ranks d != s; sizeof(T) is the size of the element written (1 for
- * int8 under quantMode 2). */
+ * sends to ranks d != s; sizeof(T) * h is the size of the row written (h bytes
+ * for int8 and fp8, h / 2 for packed fp4). */
 int orc_dispatch_plane(const orc_cfg* c, const int32_t* ep_recv_count, uint8_t* plane) {
   int st = orc_check_cfg(c);
   if (st) return st;
   const int W = c->W, L = c->E / c->W;
-  const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));
+  const int64_t row_bytes = row_out_bytes(c);
   const int64_t den = (int64_t)(W - 1 > 1 ? W - 1 : 1) * L;
   for (int s = 0; s < W; ++s) {
     int64_t remote = 0;
@@ -522,5 +682,21 @@ float orc_fp16_to_f32(uint16_t b) { return fp16_to_f32(b); }
 
 /* quantMode 2 on one row, exported for the hand-worked quantiser fixtures. */
 float orc_quantize_row(const orc_cfg* c, const void* x_row, int8_t* q) {
-  return quantize_row(c, x_row, 0, q);
+  float scale = 0.0f;
+  if (c->quant_mode != 2 || c->scales_kind != ORC_SC_NONE) return -1.0f;
+  quantize_pick(c, x_row, 0, 0, NULL, (uint8_t*)q, &scale);
+  return scale;
+}
+
+/* One fp32 value in a small float format (ORC_Y_FP8_E4M3 / _E5M2 / FP4_E2M1). */
+uint8_t orc_f32_to_minifloat(float v, int y_kind) { return f32_to_minifloat(v, y_kind); }
+
+/* quantMode 1..4 on one row for a pick of expert e (exported for the pins). */
+int orc_quantize_pick(const orc_cfg* c, const void* x_row, int32_t e, const float* quant_scales,
+                      uint8_t* q, void* dyn) {
+  int st = orc_check_cfg(c);
+  if (st) return st;
+  if (c->quant_mode == 0) return ORC_ERR_INVALID_ARG;
+  quantize_pick(c, x_row, 0, e, quant_scales, q, dyn);
+  return ORC_OK;
 }

@@ -7,9 +7,11 @@ disagrees with:
     the oracle's counting sort;
   * closed forms (identity expert: x_out = x * sum of contributing weights);
   * invariants (counts, bijection of assist_info onto the routed picks);
-  * exact rational arithmetic with IEEE round-to-nearest-even (quantiser);
-  * library routines (numpy float16 and torch bfloat16 conversions, torch
-    fp64 matmul and silu for the SwiGLU expert).
+  * exact rational arithmetic with IEEE round-to-nearest-even (quantisers of
+    every quantMode), with FP8 / FP4 codes found by brute force over each
+    format's table decoded from its definition;
+  * library routines (numpy float16 and torch bfloat16 / float8 conversions,
+    torch fp64 matmul and silu for the SwiGLU expert).
 They are plain functions so that tests/test_oracle_mutants.py can rerun them
 against deliberately broken builds of the oracle.
 """
@@ -125,6 +127,110 @@ def quantize_exact(values) -> tuple:
         r = round_half_even(rn_f32(v / scale)) if v != 0 else 0
         q.append(max(-127, min(127, r)))
     return q, scale
+
+
+# small float formats, decoded from their definitions (sign, biased
+# exponent, mantissa with an implicit leading one; exponent field 0 is
+# subnormal). E4M3 reserves S.1111.111 for NaN and has no infinity; E5M2
+# reserves exponent 31 for inf / NaN; E2M1 has neither.
+MINIFLOAT = {
+    "fp8_e4m3": dict(eb=4, mb=3, bias=7, emax=8, nonfinite=lambda E, M: E == 15 and M == 7),
+    "fp8_e5m2": dict(eb=5, mb=2, bias=15, emax=15, nonfinite=lambda E, M: E == 31),
+    "fp4_e2m1": dict(eb=2, mb=1, bias=1, emax=2, nonfinite=lambda E, M: False),
+}
+
+
+def minifloat_table(fmt: str):
+    """Sorted [(value, code)] of the non-negative finite values of a format."""
+    f = MINIFLOAT[fmt]
+    out = []
+    for code in range(1 << (f["eb"] + f["mb"])):
+        E, M = code >> f["mb"], code & ((1 << f["mb"]) - 1)
+        if f["nonfinite"](E, M):
+            continue
+        if E == 0:
+            v = Fraction(M, 1 << f["mb"]) * Fraction(2) ** (1 - f["bias"])
+        else:
+            v = (1 + Fraction(M, 1 << f["mb"])) * Fraction(2) ** (E - f["bias"])
+        out.append((v, code))
+    return sorted(out)
+
+
+def nearest_code(v, fmt: str, negative: bool = None) -> int:
+    """Brute force: the code of the representable value nearest to v (an exact
+    Fraction or a float), ties to the even code, saturating at the largest
+    finite value; the sign bit follows v's sign (negative=True for -0.0)."""
+    f = MINIFLOAT[fmt]
+    table = minifloat_table(fmt)
+    a = abs(Fraction(v))
+    if negative is None:
+        negative = Fraction(v) < 0
+    best = None
+    for val, code in table:
+        dist = abs(val - a)
+        if best is None or dist < best[0] or (dist == best[0] and code % 2 == 0):
+            best = (dist, code)
+    code = table[-1][1] if a >= table[-1][0] else best[1]
+    return code | ((1 << (f["eb"] + f["mb"])) if negative else 0)
+
+
+def fmax_of(fmt: str) -> Fraction:
+    return minifloat_table(fmt)[-1][0]
+
+
+def row_values(row: np.ndarray, dt: str) -> list:
+    return [float(v) for v in (row.astype(np.float64) if dt == "float16"
+                               else WL.bf16_bits_to_fp32(row).astype(np.float64))]
+
+
+def is_neg(v: float) -> bool:
+    return math.copysign(1.0, v) < 0
+
+
+def group_quant_exact(xs: list, fmt: str):
+    """quantMode 3 on one row of fp32 values (already smoothed), exact
+    arithmetic with IEEE rounding: (codes, scales)."""
+    fm = fmax_of(fmt)
+    codes, scales = [], []
+    for g0 in range(0, len(xs), 128):
+        grp = xs[g0:g0 + 128]
+        amax = max(abs(Fraction(v)) for v in grp)
+        if amax == 0:
+            codes += [0] * len(grp)
+            scales.append(Fraction(0))
+            continue
+        scale = rn_f32(amax / fm)
+        scales.append(scale)
+        for v in grp:
+            if v == 0:
+                codes.append(nearest_code(0, fmt, is_neg(v)))
+            else:
+                codes.append(nearest_code(rn_f32(Fraction(v) / scale), fmt, v < 0))
+    return codes, scales
+
+
+def mx_quant_exact(xs: list, fmt: str):
+    """quantMode 4 (OCP MX) on one row: (codes, E8M0 bytes)."""
+    emax = MINIFLOAT[fmt]["emax"]
+    codes, scale_bytes = [], []
+    for b0 in range(0, len(xs), 32):
+        blk = xs[b0:b0 + 32]
+        amax = max(abs(v) for v in blk)
+        se = -127
+        if amax > 0:
+            se = max(-127, min(127, math.frexp(amax)[1] - 1 - emax))
+        scale_bytes.append(se + 127)
+        X = Fraction(2) ** se
+        for v in blk:
+            codes.append(nearest_code(Fraction(v) / X, fmt, is_neg(v)))
+    return codes, scale_bytes
+
+
+def unpack_fp4(q: np.ndarray) -> list:
+    out = []
+    for b in q.tolist():
+        out += [b & 0xF, b >> 4]
+    return out
 
 
 # -------------------------------------------------------------------- pins
@@ -439,6 +545,167 @@ def pin_errors():
     assert status(base.with_(ep_world_size=1, moe_expert_num=4), inp) == 1
     assert status(base.with_(moe_expert_num=5), inp) == 1
     assert status(base.with_(quant_mode=2), inp) == 2
+    # quantisation rules: modes 1..4 take 16-bit float x; output types and the
+    # scales input as the quantMode constraints say
+    fb = base.with_(x_dtype=WL.X_BF16)
+    finp = WL.make_inputs(fb)
+    assert status(fb.with_(quant_mode=5), finp) == 2
+    assert status(fb.with_(quant_mode=1), finp) == 1                       # static needs a coefficient
+    assert status(fb.with_(quant_mode=1, scales_kind=1), dict(finp, quant_scales=np.ones(1, np.float32))) == 0
+    assert status(fb.with_(quant_mode=2, scales_kind=1), dict(finp, quant_scales=np.ones(1, np.float32))) == 1
+    assert status(fb.with_(quant_mode=3), finp) == 1                       # per-group needs an fp8 type
+    assert status(fb.with_(quant_mode=3, y_dtype="fp4_e2m1"), finp) == 1
+    assert status(fb.with_(quant_mode=3, y_dtype="fp8_e5m2"), finp) == 0
+    assert status(fb.with_(quant_mode=4, y_dtype="fp4_e2m1"), finp) == 0
+    assert status(fb.with_(quant_mode=4, y_dtype="fp4_e2m1", h=15), WL.make_inputs(fb.with_(h=15))) == 1
+    assert status(fb.with_(quant_mode=4, y_dtype="fp8_e4m3", scales_kind=3),
+                  dict(finp, quant_scales=np.ones((4, 16), np.float32))) == 1  # MX takes no scales
+    assert status(fb.with_(quant_mode=2, scales_kind=3), finp) == 1          # scales declared, none given
+
+
+def pin_minifloat_bruteforce(n: int = 1500, seed: int = 13):
+    """fp32 -> FP8 E4M3 / E5M2 / FP4 E2M1 against the brute-force nearest value
+    of each format's decoded table (exact midpoints, just-off midpoints,
+    subnormals, the saturation edge), and FP8 against torch's conversion on
+    values inside the finite range."""
+    import torch
+    rng = np.random.default_rng(seed)
+    for fmt in ("fp8_e4m3", "fp8_e5m2", "fp4_e2m1"):
+        table = minifloat_table(fmt)
+        vals = [float(v) for v, _ in table]
+        mids = [float((a + b) / 2) for (a, _), (b, _) in zip(table, table[1:])]
+        near = [float(np.nextafter(np.float32(m), np.float32(np.inf))) for m in mids] + \
+               [float(np.nextafter(np.float32(m), np.float32(0))) for m in mids if m > 0]
+        top = float(table[-1][0])
+        rand = (rng.uniform(-1, 1, n) * 2.0 ** rng.integers(-12, 18, n)).astype(np.float32).tolist()
+        xs = np.array(vals + mids + near + rand + [0.0, -0.0, top, top * 1.01, top * 4, -top * 3, 1e-30, -1e-30],
+                      dtype=np.float32)
+        xs = np.concatenate([xs, -xs])
+        got = O.f32_to_minifloat(xs, fmt)
+        want = [nearest_code(float(v), fmt, is_neg(float(v))) for v in xs]
+        assert got.tolist() == want, fmt
+        if fmt.startswith("fp8"):
+            tdt = torch.float8_e4m3fn if fmt == "fp8_e4m3" else torch.float8_e5m2
+            inside = xs[np.abs(xs) <= top]
+            lib = torch.from_numpy(inside.copy()).to(tdt).view(torch.uint8).numpy()
+            assert np.array_equal(O.f32_to_minifloat(inside, fmt), lib), fmt
+
+
+def pin_quant_static_hand():
+    g = golden("quant_static_hand.json")
+    for case in g["cases"]:
+        for dt in ("float16", "bfloat16"):
+            x = np.array(case["x"], dtype=np.float32)
+            row = x.astype(np.float16) if dt == "float16" else WL.fp32_to_bf16_bits(x)
+            q, _ = O.quantize_pick(row, 1, dt, expert=case["expert"], scales_kind=case["scales_kind"],
+                                   quant_scales=np.array(case["scales"], dtype=np.float32),
+                                   moe_expert_num=case["E"])
+            assert q.view(np.int8).tolist() == case["q"], (case["name"], dt, q.view(np.int8).tolist())
+
+
+def pin_quant_smooth_reduces(seed: int = 17):
+    """Per-expert smoothing weights that are powers of two make x * s exact in
+    bf16: quantMode 2 / 3 with smoothing for expert e must equal the plain
+    mode on the pre-multiplied row (itself pinned by exact arithmetic)."""
+    rng = np.random.default_rng(seed)
+    h, E = 260, 4
+    x = rng.standard_normal(h).astype(np.float32)
+    row = WL.fp32_to_bf16_bits(x)
+    xf = WL.bf16_bits_to_fp32(row)
+    sm = (2.0 ** rng.integers(-2, 3, size=(E, h))).astype(np.float32)
+    for e in range(E):
+        pre = WL.fp32_to_bf16_bits(xf * sm[e])
+        assert np.array_equal(WL.bf16_bits_to_fp32(pre), xf * sm[e])
+        for mode, y in ((2, ""), (3, "fp8_e4m3"), (3, "fp8_e5m2")):
+            q1, d1 = O.quantize_pick(row, mode, "bfloat16", y, expert=e, quant_scales=sm, scales_kind=3,
+                                     moe_expert_num=E)
+            q0, d0 = O.quantize_pick(pre, mode, "bfloat16", y)
+            assert np.array_equal(q1, q0) and np.array_equal(d1, d0), (e, mode, y)
+    # the smoothing row is the pick's expert's: distinct experts, distinct rows
+    qa, _ = O.quantize_pick(row, 2, "bfloat16", expert=0, quant_scales=sm, scales_kind=3, moe_expert_num=E)
+    qb, _ = O.quantize_pick(row, 2, "bfloat16", expert=1, quant_scales=sm, scales_kind=3, moe_expert_num=E)
+    assert not np.array_equal(qa, qb)
+
+
+def pin_quant_group_exact(seed: int = 19):
+    """quantMode 3 by exact arithmetic: groups of 128 (the last one ragged),
+    fp32 scales amax / FMAX, fp8 codes of the IEEE quotient; zero groups and
+    signed zeros included."""
+    rng = np.random.default_rng(seed)
+    for i, (fmt, dt, h) in enumerate([("fp8_e4m3", "bfloat16", 300), ("fp8_e5m2", "float16", 300),
+                                      ("fp8_e4m3", "float16", 128), ("fp8_e5m2", "bfloat16", 70)]):
+        x = (rng.standard_normal(h) * 10.0 ** rng.integers(-2, 3)).astype(np.float32)
+        if h > 256:
+            x[128:256] = 0.0
+            x[130] = -0.0
+        x[3] = -0.0
+        row = x.astype(np.float16) if dt == "float16" else WL.fp32_to_bf16_bits(x)
+        xs = row_values(row, dt)
+        q, dyn = O.quantize_pick(row, 3, dt, fmt)
+        codes, scales = group_quant_exact(xs, fmt)
+        assert q.tolist() == codes, (i, fmt)
+        assert [Fraction(float(v)) for v in dyn] == scales, (i, fmt)
+
+
+def pin_quant_mx_exact(seed: int = 23):
+    """quantMode 4 against the OCP MX conversion worked exactly: E8M0 bytes
+    from frexp, element codes by brute force (fp4 unpacked low nibble first);
+    zero, power-of-two and ragged blocks included."""
+    rng = np.random.default_rng(seed)
+    for i, (fmt, dt, h) in enumerate([("fp8_e4m3", "bfloat16", 200), ("fp8_e5m2", "float16", 96),
+                                      ("fp4_e2m1", "bfloat16", 200), ("fp4_e2m1", "float16", 64)]):
+        x = (rng.standard_normal(h) * 10.0 ** rng.integers(-3, 3)).astype(np.float32)
+        x[32:64] = 0.0
+        x[40] = -0.0
+        if h > 96:
+            x[64:96] = rng.integers(-8, 9, 32).astype(np.float32) / 4.0
+            x[70] = 2.0      # block amax an exact power of two
+        row = x.astype(np.float16) if dt == "float16" else WL.fp32_to_bf16_bits(x)
+        xs = row_values(row, dt)
+        q, dyn = O.quantize_pick(row, 4, dt, fmt)
+        codes, sbytes = mx_quant_exact(xs, fmt)
+        got = unpack_fp4(q) if fmt == "fp4_e2m1" else q.tolist()
+        assert got == codes, (i, fmt)
+        assert dyn.tolist() == sbytes, (i, fmt)
+
+
+def pin_quant_modes_dispatch(seed: int = 29):
+    """Every quantised mode through dispatch: each routed row (found through
+    assist_info) holds its token's row quantised for the pick's expert, worked
+    out here exactly; the layout equals the unquantised one."""
+    cases = [(1, "", 1), (1, "", 2), (1, "", 3), (2, "", 3), (3, "fp8_e4m3", 0), (3, "fp8_e5m2", 3),
+             (4, "fp8_e4m3", 0), (4, "fp4_e2m1", 0)]
+    for i, (mode, y, sk) in enumerate(cases):
+        wl = WL.Workload(f"qd{i}", 2, 3, 160, 2, 4, WL.X_BF16, quant_mode=mode, y_dtype=y, scales_kind=sk,
+                         mask_kind=2, mask_false_p=0.2, seed=seed + i)
+        inp = WL.make_inputs(wl)
+        d = O.dispatch(wl, inp)
+        base = O.dispatch(wl.with_(quant_mode=0, y_dtype="", scales_kind=0), inp)
+        assert np.array_equal(d["ep_recv_count"], base["ep_recv_count"])
+        assert np.array_equal(d["assist_info"], base["assist_info"])
+        qs = inp.get("quant_scales")
+        for r in range(wl.ep_world_size):
+            for row in range(int(d["ep_recv_count"][r, -1])):
+                s, t, k = d["assist_info"][r, row]
+                e = int(inp["expert_ids"][s, t, k])
+                xs = row_values(inp["x"][s, t], WL.X_BF16)
+                if sk:
+                    sv = {1: lambda j: qs[0], 2: lambda j: qs[j], 3: lambda j: qs[e, j]}[sk]
+                    xs = [float(np.float32(v) * np.float32(sv(j))) for j, v in enumerate(xs)]
+                got = d["expand_x"][r, row]
+                if mode == 1:
+                    want = [max(-128, min(127, round_half_even(Fraction(v)))) for v in xs]
+                    assert got.tolist() == want, (i, r, row)
+                elif mode == 2:
+                    want, scale = quantize_exact(xs)
+                    assert got.tolist() == want and Fraction(float(d["dynamic_scales"][r, row])) == scale
+                elif mode == 3:
+                    codes, scales = group_quant_exact(xs, y)
+                    assert got.tolist() == codes and [Fraction(float(v)) for v in d["dynamic_scales"][r, row]] == scales
+                else:
+                    codes, sbytes = mx_quant_exact(xs, y)
+                    g = unpack_fp4(got) if y == "fp4_e2m1" else got.tolist()
+                    assert g == codes and d["dynamic_scales"][r, row].tolist() == sbytes, (i, r, row)
 
 
 def run_all():
@@ -479,6 +746,12 @@ def run_all():
     d = pin_quant_dispatch(wq, inp)
     pin_invariants(wq, inp, d)
     pin_quant_exact()
+    pin_minifloat_bruteforce(n=300)
+    pin_quant_static_hand()
+    pin_quant_smooth_reduces()
+    pin_quant_group_exact()
+    pin_quant_mx_exact()
+    pin_quant_modes_dispatch()
     pin_conversions(n=4000)
     pin_swiglu_torch()
     pin_ffn_tokens_compose()

@@ -42,9 +42,9 @@ MUTANTS = {
     "combine_routed_weight_dropped": [(
         "acc += w * ((const int32_t*)expert_out)[(size_t)where[tok * K + k] * h + j];",
         "acc += ((const int32_t*)expert_out)[(size_t)where[tok * K + k] * h + j];")],
-    "quant_reciprocal": [("float r = nearbyintf(load_f(c, x, row * c->h + j) / scale);",
-                          "float r = nearbyintf(load_f(c, x, row * c->h + j) * (127.0f / amax));")],
-    "quant_round_away": [("float r = nearbyintf(", "float r = roundf(")],
+    "quant_reciprocal": [("float r = amax == 0.0f ? 0.0f : nearbyintf(xs[j] / scale);",
+                          "float r = amax == 0.0f ? 0.0f : nearbyintf(xs[j] * (127.0f / amax));")],
+    "quant_round_away": [("float r = amax == 0.0f ? 0.0f : nearbyintf(", "float r = amax == 0.0f ? 0.0f : roundf(")],
     "quant_scale_255": [("float scale = amax / 127.0f;", "float scale = amax / 255.0f;")],
     "bf16_truncates": [("u += 0x7FFFu + lsb;", "u += 0u * lsb;")],
     "plane_size_strict": [("bytes >= c->bulk_min_bytes && bytes * den > num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch",
@@ -52,8 +52,24 @@ MUTANTS = {
     "plane_mean_non_strict": [("bytes >= c->bulk_min_bytes && bytes * den > num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch",
                                "bytes >= c->bulk_min_bytes && bytes * den >= num);\n      }\n  }\n  return ORC_OK;\n}\n\n/* Dispatch")],
     "plane_remote_counts_local": [("if (s != d) remote += seg_rows", "remote += seg_rows")],
-    "dispatch_plane_wrong_den": [("const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));\n  const int64_t den = (int64_t)(W - 1 > 1 ? W - 1 : 1) * L;",
-                                  "const int64_t row_bytes = (int64_t)c->h * (c->quant_mode == 2 ? 1 : elem_bytes(c));\n  const int64_t den = (int64_t)W * L;")],
+    "dispatch_plane_wrong_den": [("const int64_t row_bytes = row_out_bytes(c);\n  const int64_t den = (int64_t)(W - 1 > 1 ? W - 1 : 1) * L;",
+                                  "const int64_t row_bytes = row_out_bytes(c);\n  const int64_t den = (int64_t)W * L;")],
+    "static_clamp_symmetric": [("if (r < -128.0f) r = -128.0f;", "if (r < -127.0f) r = -127.0f;")],
+    "smooth_ignored": [("case ORC_SC_EXPERT: return v * quant_scales[(size_t)e * c->h + j];",
+                        "case ORC_SC_EXPERT: return v;")],
+    "smooth_first_expert_row": [("case ORC_SC_EXPERT: return v * quant_scales[(size_t)e * c->h + j];",
+                                 "case ORC_SC_EXPERT: return v * quant_scales[j];")],
+    "group_of_64": [("for (int g0 = 0; g0 < h; g0 += 128) {\n      int g1 = g0 + 128 < h ? g0 + 128 : h;",
+                     "for (int g0 = 0; g0 < h; g0 += 64) {\n      int g1 = g0 + 64 < h ? g0 + 64 : h;")],
+    "e4m3_fmax_240": [("const float fmax = c->y_kind == ORC_Y_FP8_E4M3 ? 448.0f : 57344.0f;",
+                       "const float fmax = c->y_kind == ORC_Y_FP8_E4M3 ? 240.0f : 57344.0f;")],
+    "mx_emax_off_by_one": [("const int emax = c->y_kind == ORC_Y_FP8_E4M3 ? 8 :",
+                            "const int emax = c->y_kind == ORC_Y_FP8_E4M3 ? 7 :")],
+    "mx_scale_ceil": [("se = (ex - 1) - emax;", "se = ex - emax;")],
+    "minifloat_ties_away": [("double n = nearbyint(a / quantum);", "double n = round(a / quantum);")],
+    "minifloat_no_subnormals": [("if (a < ldexp(1.0, emin)) e = emin;", "if (0) e = emin;")],
+    "fp4_nibbles_swapped": [("q[j / 2] |= (uint8_t)(code << (4 * (j % 2)));",
+                             "q[j / 2] |= (uint8_t)(code << (4 * (1 - j % 2)));")],
     "silu_sign": [("a[i] = g / (1.0 + exp(-g)) * u;", "a[i] = g / (1.0 + exp(g)) * u;")],
     "gate_up_swapped": [("g += xv[j] * bf16_to_f32(wg[", "g += xv[j] * bf16_to_f32(wu[")],
     "down_transposed": [("acc += a[i] * bf16_to_f32(wd[(size_t)j * I + i]);",

@@ -100,3 +100,27 @@ def test_skewed_workload_invariants_and_closed_form():
     want = xf * P.contributing_weight_sum(wl, inp)[..., None]
     got = WL.bf16_bits_to_fp32(x_out).astype(np.float64)
     assert np.all(np.abs(got - want) <= np.abs(want) * 2.0 ** -7 + 1e-5)
+
+
+def test_small_float_conversions_bruteforce_and_torch():
+    P.pin_minifloat_bruteforce()
+
+
+def test_static_quant_hand_fixture():
+    P.pin_quant_static_hand()
+
+
+def test_smoothing_reduces_to_plain_modes():
+    P.pin_quant_smooth_reduces()
+
+
+def test_per_group_quant_exact():
+    P.pin_quant_group_exact()
+
+
+def test_mx_quant_exact():
+    P.pin_quant_mx_exact()
+
+
+def test_quant_modes_through_dispatch():
+    P.pin_quant_modes_dispatch()

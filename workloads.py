@@ -44,7 +44,9 @@ class Workload:
     zero_expert_num: int = 0
     copy_expert_num: int = 0
     mask_kind: int = 0          # 0 none, 1 = (bs,), 2 = (bs, K)
-    quant_mode: int = 0         # 0 none, 2 per-token dynamic int8
+    quant_mode: int = 0         # 0 none, 1 static int8, 2 per-token int8, 3 per-group fp8, 4 MX
+    y_dtype: str = ""           # quantised element type for modes 3 / 4: fp8_e4m3, fp8_e5m2, fp4_e2m1
+    scales_kind: int = 0        # scales input: 0 none, 1 (1,), 2 (h,), 3 (E, h)
     ids: str = "uniform"        # "uniform" distinct ids, or "zipf"
     zipf_s: float = 1.2
     special_p: float = 0.0      # probability that a pick becomes a special expert
@@ -165,6 +167,10 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
       expert_scales [W, bs, K]   int32 (int32 x) or float32
       w_gate, w_up  [E, I, h]    uint16 bf16 bits   (FFN workloads only; stored
       w_down        [E, h, I]    out-major, like a linear layer's weight)
+      quant_scales  float32 (1,), (h,) or (E, h) when scales_kind > 0: static
+                    coefficients U[16, 40] (quantMode 1; N(0,1) data then
+                    saturates int8 beyond about 3.2 sigma), smoothing weights
+                    U[0.5, 2] otherwise
     """
     seed = wl.seed if seed is None else seed
     rng = np.random.Generator(np.random.PCG64(seed))
@@ -217,6 +223,11 @@ def make_inputs(wl: Workload, seed: Optional[int] = None) -> dict:
         for name, shape in (("w_gate", (E, I, h)), ("w_up", (E, I, h)), ("w_down", (E, h, I))):
             w = rng.standard_normal(size=shape, dtype=np.float32) * np.float32(0.02)
             out[name] = fp32_to_bf16_bits(w)
+
+    if wl.scales_kind > 0:
+        shape = {1: (1,), 2: (h,), 3: (E, h)}[wl.scales_kind]
+        lo, hi = (16.0, 40.0) if wl.quant_mode == 1 else (0.5, 2.0)
+        out["quant_scales"] = rng.uniform(lo, hi, size=shape).astype(np.float32)
     return out
 
 
