@@ -46,6 +46,9 @@ struct WsLayout {
 struct Shape {
   int W, bs, h, K, E, L, Z, C;
   int mask_kind, quant, x_dtype;
+  int ytype;         // MOE_Y_* of quantised rows
+  int scales_kind;   // MOE_SCALES_* of the scales input
+  int ngroups;       // dynamic-scale entries per row (mode 2: 1; 3: ceil(h/128); 4: ceil(h/32))
   int64_t A;         // rows per rank
   int es;            // element bytes of x
   int row_in;        // h * es
@@ -78,7 +81,8 @@ struct ScatterParams {
   const uint8_t* mask;
   const void* scales;      // may be null
   void* expand_x;
-  float* dyn_scales;       // quant 2
+  void* dyn_scales;        // per-row dynamic scales (fp32; E8M0 bytes for quant 4)
+  const float* qscales;    // scales input (static coefficients / smoothing weights), or null
   int32_t* assist;
   void* expand_scales;     // may be null
   const int32_t* rank;
@@ -138,6 +142,13 @@ struct FfnLaunch {
 
 // True when the TMA scatter's shared-memory ring fits for this shape.
 bool scatter_tma_fits(const Shape& sh);
+// The quantising scatter (quant modes 1, 3, 4 and smoothed 2) and its fit test.
+bool scatter_quant_tma_fits(const Shape& sh);
+cudaError_t launch_scatter_quant(const ScatterParams& p, cudaStream_t st, int num_sms, bool tma);
+// Modes the quantising scatter handles (the plain per-token int8 path does the rest).
+inline bool uses_scatter_quant(const Shape& sh) {
+  return sh.quant == 1 || sh.quant == 3 || sh.quant == 4 || (sh.quant == 2 && sh.scales_kind != MOE_SCALES_NONE);
+}
 
 // Launchers (each returns the launch error, if any).
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st);

@@ -30,13 +30,30 @@ moe_status_t make_shape(const moe_config_t* c, Shape* sh) {
   if (c->const_expert_num != 0) return MOE_ERR_UNSUPPORTED;
   if (c->mask_kind < 0 || c->mask_kind > 2) return MOE_ERR_INVALID_ARG;
   if (c->x_dtype < MOE_I32 || c->x_dtype > MOE_BF16) return MOE_ERR_INVALID_ARG;
-  if (c->quant_mode != 0 && c->quant_mode != 2) return MOE_ERR_UNSUPPORTED;
-  if (c->quant_mode == 2 && c->x_dtype == MOE_I32) return MOE_ERR_UNSUPPORTED;
+  if (c->quant_mode < 0 || c->quant_mode > 4) return MOE_ERR_UNSUPPORTED;
+  if (c->expand_dtype < MOE_Y_DEFAULT || c->expand_dtype > MOE_Y_FP4_E2M1 ||
+      c->scales_kind < MOE_SCALES_NONE || c->scales_kind > MOE_SCALES_EXPERT)
+    return MOE_ERR_INVALID_ARG;
+  if (c->quant_mode == 0) {
+    if (c->expand_dtype != MOE_Y_DEFAULT || c->scales_kind != MOE_SCALES_NONE) return MOE_ERR_INVALID_ARG;
+  } else {
+    if (c->x_dtype == MOE_I32) return MOE_ERR_UNSUPPORTED;
+    const int y = c->expand_dtype, k = c->scales_kind;
+    const bool smooth_ok = k == MOE_SCALES_NONE || k == MOE_SCALES_EXPERT;
+    bool ok;
+    switch (c->quant_mode) {
+      case 1: ok = y == MOE_Y_DEFAULT && k != MOE_SCALES_NONE; break;
+      case 2: ok = y == MOE_Y_DEFAULT && smooth_ok; break;
+      case 3: ok = (y == MOE_Y_FP8_E4M3 || y == MOE_Y_FP8_E5M2) && smooth_ok; break;
+      default: ok = y != MOE_Y_DEFAULT && k == MOE_SCALES_NONE && (y != MOE_Y_FP4_E2M1 || c->h % 2 == 0); break;
+    }
+    if (!ok) return MOE_ERR_INVALID_ARG;
+  }
   if (c->plane_policy < MOE_PLANE_RULE || c->plane_policy > MOE_PLANE_BULK_ALL) return MOE_ERR_INVALID_ARG;
   if (c->bulk_min_bytes < 0) return MOE_ERR_INVALID_ARG;
   if (c->combine_mode < MOE_COMBINE_GATHER || c->combine_mode > MOE_COMBINE_PUT_ONLY) return MOE_ERR_INVALID_ARG;
   if (c->wait_timeout_us <= 0) return MOE_ERR_INVALID_ARG;
-  if (c->ffn_intermediate < 0 || c->reserved0 != 0 || c->reserved1 != 0) return MOE_ERR_INVALID_ARG;
+  if (c->ffn_intermediate < 0) return MOE_ERR_INVALID_ARG;
   const long long picks = (long long)c->ep_world_size * c->bs * c->topk;
   if (picks >= 2147483647LL) return MOE_ERR_INVALID_ARG;
   sh->W = c->ep_world_size;
@@ -55,7 +72,13 @@ moe_status_t make_shape(const moe_config_t* c, Shape* sh) {
   const long long row_in = (long long)c->h * sh->es;
   if (row_in > (1LL << 30)) return MOE_ERR_INVALID_ARG;
   sh->row_in = (int)row_in;
-  sh->row_out = c->quant_mode == 2 ? c->h : sh->row_in;
+  sh->ytype = c->expand_dtype;
+  sh->scales_kind = c->scales_kind;
+  sh->ngroups = c->quant_mode == 2 ? 1 : c->quant_mode == 3 ? (c->h + 127) / 128
+              : c->quant_mode == 4 ? (c->h + 31) / 32 : 0;
+  if (c->quant_mode == 0) sh->row_out = sh->row_in;
+  else if (c->quant_mode == 4 && c->expand_dtype == MOE_Y_FP4_E2M1) sh->row_out = c->h / 2;
+  else sh->row_out = c->h;
   if ((long long)sh->W * sh->A >= 2147483647LL) return MOE_ERR_INVALID_ARG;  // flat rows fit int32
   return MOE_OK;
 }
@@ -152,8 +175,8 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
 }
 
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
-                          const uint8_t* active_mask, const void* expert_scales, void* expand_x,
-                          float* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                          const uint8_t* active_mask, const void* expert_scales, const float* scales,
+                          void* expand_x, void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
                           void* expand_scales, uint8_t* seg_plane, void* ws, size_t ws_bytes, void* stream) {
   Shape sh;
   moe_status_t st = make_shape(cfg, &sh);
@@ -163,10 +186,12 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (!ep_recv_count) return MOE_ERR_INVALID_ARG;
   if (sh.mask_kind != 0 && !active_mask && !empty) return MOE_ERR_INVALID_ARG;
   if (expand_scales && !expert_scales) return MOE_ERR_INVALID_ARG;
-  if (sh.quant == 2 && !dynamic_scales) return MOE_ERR_INVALID_ARG;
+  if (sh.ngroups > 0 && !dynamic_scales && !empty) return MOE_ERR_INVALID_ARG;
+  if ((sh.scales_kind != MOE_SCALES_NONE) != (scales != nullptr)) return MOE_ERR_INVALID_ARG;
   if (!aligned(x, 16) || !aligned(expand_x, 16) || !aligned(expert_ids, 4) || !aligned(expert_scales, 4) ||
       !aligned(assist_info, 4) || !aligned(ep_recv_count, 4) || !aligned(expand_scales, 4) ||
-      !aligned(dynamic_scales, 4) || !aligned(cfg->seg_ready, 4) || !aligned(cfg->performance_info, 8))
+      !aligned(dynamic_scales, 4) || !aligned(scales, 16) || !aligned(cfg->seg_ready, 4) ||
+      !aligned(cfg->performance_info, 8))
     return MOE_ERR_INVALID_ARG;
   WsLayout L;
   st = check_ws(cfg, sh, ws, ws_bytes, &L);
@@ -177,7 +202,9 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   const int nsm = num_sms_of_current_device();
   if (nsm <= 0) return MOE_ERR_CUDA;
 
-  const bool tma = sh.row_in % 16 == 0 && sh.row_out % 16 == 0 && scatter_tma_fits(sh);
+  const bool quant_kernel = uses_scatter_quant(sh);
+  const bool tma = sh.row_in % 16 == 0 && sh.row_out % 16 == 0 &&
+                   (quant_kernel ? scatter_quant_tma_fits(sh) : scatter_tma_fits(sh));
 
   RouteParams rp{};
   rp.ids = expert_ids;
@@ -213,6 +240,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.scales = expert_scales;
   sp.expand_x = expand_x;
   sp.dyn_scales = dynamic_scales;
+  sp.qscales = scales;
   sp.assist = assist_info;
   sp.expand_scales = expand_scales;
   sp.rank = rp.rank;
@@ -222,7 +250,8 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.status = &hdr->status;
   sp.timeout_ns = timeout_ns(cfg);
   if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
-  if (launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
+  const cudaError_t e = quant_kernel ? launch_scatter_quant(sp, s, nsm, tma) : launch_scatter(sp, s, nsm, tma);
+  if (e != cudaSuccess) return MOE_ERR_CUDA;
   if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
   return MOE_OK;
 }

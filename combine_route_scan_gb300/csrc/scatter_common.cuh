@@ -1,0 +1,118 @@
+// Pieces shared by the dispatch payload kernels (scatter.cu, and the
+// quantising variants in scatter_quant.cu): the per-token destination list
+// built by warp 0, ready-flag publication and the per-rank communication
+// timer (aclnnMoeDistributeDispatchV4, 参数说明 performanceInfoOptional).
+#pragma once
+
+#include "common.cuh"
+
+namespace crs {
+
+constexpr int kScatterThreads = 256;
+constexpr int kScatterWarps = kScatterThreads / 32;
+constexpr int kMaxK = 32;
+
+__host__ __device__ __forceinline__ size_t align128(size_t v) { return (v + 127) & ~size_t(127); }
+
+// Per-token destination list, built by warp 0. Three of them rotate by token,
+// so the ready-flag publisher can still read the last two tokens' lists.
+struct PickTable {
+  long long sm_dst[kMaxK];    // flat expand_x rows (d*A + row) on the store plane
+  long long bulk_dst[kMaxK];  // ... on the bulk plane
+  int sm_seg[kMaxK];          // their segments g = e*W + s
+  int bulk_seg[kMaxK];
+  int n_sm, n_bulk;
+};
+
+// One more row of segment g is in place; the last one releases the flag.
+// The caller has fenced after the row's stores became visible.
+__device__ __forceinline__ void publish_row(const ScatterParams& p, int g) {
+  if (atomicAdd(p.landed + g, 1u) + 1u == (uint32_t)p.cnt[g]) {
+    __threadfence();
+    st_release_gpu(p.seg_ready + g, p.ticket);
+  }
+}
+
+// Builds the destination list of token `tau` (warp 0 only) and writes the
+// per-row metadata. Returns nothing; results land in `tab`.
+__device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, int s, int t, PickTable& tab,
+                                            bool write_dyn, float qscale) {
+  const Shape& sh = p.sh;
+  const int lane = threadIdx.x & 31;
+  long long dst = -1;
+  int bulk = 0;
+  if (lane < sh.K) {
+    // position and id are independent loads: issue both before using either
+    const int r = p.rank[tau * sh.K + lane];
+    const int e = p.ids[tau * sh.K + lane];
+    if (r >= 0) {
+      const int d = e / sh.L;
+      const size_t g = (size_t)e * sh.W + s;
+      const long long row = (long long)p.base[g] + r;
+      if (row < sh.A) {
+        dst = (long long)d * sh.A + row;
+        bulk = p.plane[g];
+        int32_t* a = p.assist + dst * 3;
+        a[0] = s;
+        a[1] = t;
+        a[2] = lane;
+        if (p.expand_scales)
+          reinterpret_cast<uint32_t*>(p.expand_scales)[dst] =
+              reinterpret_cast<const uint32_t*>(p.scales)[tau * sh.K + lane];
+        if (write_dyn) static_cast<float*>(p.dyn_scales)[dst] = qscale;
+      } else {
+        set_error(p.status, MOE_ERR_CAPACITY);
+      }
+    }
+  }
+  const uint32_t m_sm = __ballot_sync(0xffffffffu, dst >= 0 && !bulk);
+  const uint32_t m_bk = __ballot_sync(0xffffffffu, dst >= 0 && bulk);
+  const int seg = dst >= 0 ? p.ids[tau * sh.K + lane] * sh.W + s : -1;
+  if (dst >= 0 && !bulk) {
+    const int j = __popc(m_sm & lanemask_lt());
+    tab.sm_dst[j] = dst;
+    tab.sm_seg[j] = seg;
+  }
+  if (dst >= 0 && bulk) {
+    const int j = __popc(m_bk & lanemask_lt());
+    tab.bulk_dst[j] = dst;
+    tab.bulk_seg[j] = seg;
+  }
+  if (lane == 0) {
+    tab.n_sm = __popc(m_sm);
+    tab.n_bulk = __popc(m_bk);
+  }
+}
+
+// Per-rank communication time (performance info): the earliest CTA start,
+// the latest row-store time per source rank, and the last CTA to finish adds
+// each rank's span to the caller's array and resets the workspace fields.
+__device__ __forceinline__ void perf_begin(const ScatterParams& p) {
+  atomicMax(&p.hdr->perf_start_inv, ~(unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void perf_mark(const ScatterParams& p, size_t tau) {
+  atomicMax(p.perf_end + tau / p.sh.bs, (unsigned long long)globaltimer_ns());
+}
+__device__ __forceinline__ void perf_finish(const ScatterParams& p, int* s_last) {
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    __threadfence();
+    *s_last = atomicAdd(&p.hdr->scatter_done, 1u) == gridDim.x - 1;
+  }
+  __syncthreads();
+  if (*s_last) {
+    __threadfence();
+    const unsigned long long start = ~atomicAdd(&p.hdr->perf_start_inv, 0ull);
+    for (int s = threadIdx.x; s < p.sh.W; s += blockDim.x) {
+      const unsigned long long end = atomicExch(p.perf_end + s, 0ull);
+      if (end > start) p.perf[s] += (long long)(end - start);
+    }
+    __syncthreads();
+    if (threadIdx.x == 0) {
+      p.hdr->perf_start_inv = 0ull;
+      p.hdr->scatter_done = 0u;
+    }
+  }
+}
+
+}  // namespace crs

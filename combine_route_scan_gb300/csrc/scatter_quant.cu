@@ -1,0 +1,555 @@
+// Dispatch payload for the quantised modes of aclnnMoeDistributeDispatchV4
+// (参数说明 quantMode / scalesOptional, 约束说明 quantMode相关约束) other than
+// the plain per-token int8 path of scatter.cu:
+//   quantMode 1   static int8: q = clamp(rne(x * s), -128, 127), s of shape
+//                 (1,), (h,) or (E, h) (the pick's expert's row);
+//   quantMode 2   per-token int8 after per-expert smoothing x' = x * s[e];
+//   quantMode 3   per-group FP8: groups of 128, scale_g = amax_g / FMAX,
+//                 q = fp8(x' / scale_g), optional smoothing as for 2;
+//   quantMode 4   MX (OCP Microscaling v1.0): blocks of 32 share the E8M0
+//                 scale X = 2^(floor(log2 amax) - emax), q = x / X in FP8 E4M3,
+//                 FP8 E5M2 or FP4 E2M1 (two codes a byte, even element low).
+// Conversions are the sm_100-family cvt.rn.satfinite instructions (round to
+// nearest even, saturating at the largest finite value).
+//
+// Same skeleton as the plain dispatch: persistent token-major CTAs, the source
+// row staged in shared memory by a TMA bulk load, warp 0 building the
+// destination list. The quantised row ("variant") is written to one of two
+// shared buffers and leaves by TMA bulk copies (bulk-plane segments) or
+// 16-byte stores (store-plane segments). A variant is computed once per token,
+// or once per pick when the per-expert scales make every pick's row different.
+// Each thread quantises 16-byte vectors of 8 elements; a 128-element group is
+// 16 neighbouring lanes and a 32-element MX block 4, reduced with shuffles.
+#include <cuda_bf16.h>
+#include <cuda_fp16.h>
+
+#include "scatter_common.cuh"
+
+namespace crs {
+
+constexpr int kQStages = 2;  // staged source rows
+constexpr int kQSlots = 2;   // quantised-row buffers: one is written while bulk copies read the other
+
+template <int DT>
+__device__ __forceinline__ void unpack8(int4 v, float (&f)[8]) {
+  const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    if (DT == MOE_F16) {
+      const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
+      f[2 * i] = __low2float(h2);
+      f[2 * i + 1] = __high2float(h2);
+    } else {
+      const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
+      f[2 * i] = __low2float(h2);
+      f[2 * i + 1] = __high2float(h2);
+    }
+  }
+}
+
+__device__ __forceinline__ float load_elem(const void* x, size_t i, int dt) {
+  const uint16_t b = static_cast<const uint16_t*>(x)[i];
+  return dt == MOE_F16 ? __half2float(__ushort_as_half(b)) : __bfloat162float(__ushort_as_bfloat16(b));
+}
+
+// Two fp32 values -> two FP8 codes, the first in the low byte.
+template <int YT>
+__device__ __forceinline__ uint32_t cvt_fp8x2(float lo, float hi) {
+  uint16_t r;
+  if (YT == MOE_Y_FP8_E4M3)
+    asm("cvt.rn.satfinite.e4m3x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  else
+    asm("cvt.rn.satfinite.e5m2x2.f32 %0, %1, %2;" : "=h"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+// Two fp32 values -> two FP4 E2M1 codes in one byte, the first in the low nibble.
+__device__ __forceinline__ uint32_t cvt_fp4x2(float lo, float hi) {
+  uint32_t r;
+  asm("{\n\t.reg .b8 t;\n\tcvt.rn.satfinite.e2m1x2.f32 t, %1, %2;\n\tcvt.u32.u8 %0, t;\n\t}"
+      : "=r"(r) : "f"(hi), "f"(lo));
+  return r;
+}
+
+__device__ __forceinline__ uint32_t cvt_y_pair(int yt, float lo, float hi) {
+  if (yt == MOE_Y_FP8_E4M3) return cvt_fp8x2<MOE_Y_FP8_E4M3>(lo, hi);
+  if (yt == MOE_Y_FP8_E5M2) return cvt_fp8x2<MOE_Y_FP8_E5M2>(lo, hi);
+  return cvt_fp4x2(lo, hi);
+}
+
+__device__ __forceinline__ float fp8_max(int yt) { return yt == MOE_Y_FP8_E4M3 ? 448.0f : 57344.0f; }
+__device__ __forceinline__ int elem_emax(int yt) {
+  return yt == MOE_Y_FP8_E4M3 ? 8 : yt == MOE_Y_FP8_E5M2 ? 15 : 2;
+}
+
+// floor(log2(a)) of a finite a > 0, subnormals included (from the bit fields).
+__device__ __forceinline__ int floor_log2(float a) {
+  const uint32_t b = __float_as_uint(a);
+  const int e = (int)((b >> 23) & 0xffu);
+  if (e) return e - 127;
+  return (31 - __clz(b & 0x7fffffu)) - 149;
+}
+
+// MX shared exponent of a block: floor(log2 amax) - emax clamped to [-127, 127];
+// -127 for an all-zero block.
+__device__ __forceinline__ int mx_exponent(float amax, int emax) {
+  if (!(amax > 0.f)) return -127;
+  return max(-127, min(127, floor_log2(amax) - emax));
+}
+
+// 2^k for k in [-127, 127], exactly (2^-127 is subnormal).
+__device__ __forceinline__ float exp2_exact(int k) {
+  return k >= -126 ? __uint_as_float((uint32_t)(k + 127) << 23) : __uint_as_float(0x00400000u);
+}
+
+__device__ __forceinline__ int static_q(float v) { return max(-128, min(127, __float2int_rn(v))); }
+__device__ __forceinline__ int token_q(float v, float scale) {
+  return max(-127, min(127, __float2int_rn(__fdiv_rn(v, scale))));
+}
+
+__device__ __forceinline__ uint2 pack8(const int (&q)[8]) {
+  uint32_t a = 0, b = 0;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    a |= ((uint32_t)q[i] & 0xffu) << (8 * i);
+    b |= ((uint32_t)q[i + 4] & 0xffu) << (8 * i);
+  }
+  return make_uint2(a, b);
+}
+
+// Coefficient / smoothing weights of 8 elements starting at v*8 (16-byte
+// aligned loads: the scales array is 16-byte aligned and h % 8 == 0 here).
+__device__ __forceinline__ void load_scales8(const float* srow, uint32_t v, float (&s)[8]) {
+  const float4 a = __ldg(reinterpret_cast<const float4*>(srow) + 2 * v);
+  const float4 b = __ldg(reinterpret_cast<const float4*>(srow) + 2 * v + 1);
+  s[0] = a.x; s[1] = a.y; s[2] = a.z; s[3] = a.w;
+  s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
+}
+
+// Rows of token i-1 are complete: count them toward their segments' flags.
+__device__ __forceinline__ void publish_token(const ScatterParams& p, const PickTable& a) {
+  bulk_wait_all<0>();
+  fence_proxy_async_global();
+  __threadfence();
+  for (int j = 0; j < a.n_sm; ++j) publish_row(p, a.sm_seg[j]);
+  for (int j = 0; j < a.n_bulk; ++j) publish_row(p, a.bulk_seg[j]);
+}
+
+// MODE: quantMode (1..4); DT: MOE_F16 / MOE_BF16; YT: MOE_Y_* of the output;
+// PE: per-expert scales (a variant per pick).
+template <int MODE, int DT, int YT, bool PE>
+__global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterParams p) {
+  extern __shared__ __align__(128) uint8_t smem[];
+  __shared__ __align__(8) uint64_t full_bar[kQStages];
+  __shared__ PickTable tabs[2];
+  __shared__ float s_red[kScatterWarps];
+  __shared__ int s_abort;
+
+  const Shape sh = p.sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_tok = sh.W * sh.bs;
+  const int G = gridDim.x;
+  const int my_n = blockIdx.x < n_tok ? (n_tok - 1 - (int)blockIdx.x) / G + 1 : 0;
+  const uint32_t row_in = (uint32_t)sh.row_in, row_out = (uint32_t)sh.row_out;
+  const size_t slot_in = align128(row_in), slot_out = align128(row_out);
+  const size_t slot_dyn = align128((size_t)sh.ngroups * 4);
+  uint8_t* xin = smem;
+  uint8_t* qbuf = smem + kQStages * slot_in;
+  uint8_t* dbuf = qbuf + kQSlots * slot_out;
+  const uint8_t* x = static_cast<const uint8_t*>(p.x);
+  uint8_t* out = static_cast<uint8_t*>(p.expand_x);
+  const uint32_t nvec = (uint32_t)sh.h / 8;
+  const int dyn_es = MODE == 4 ? 1 : 4;  // bytes of one dynamic-scale entry
+  const float s0 = (MODE == 1 && sh.scales_kind == MOE_SCALES_SCALAR) ? __ldg(p.qscales) : 1.f;
+  const bool channel = MODE == 1 && sh.scales_kind == MOE_SCALES_CHANNEL;
+
+  if (tid == 0) {
+    for (int i = 0; i < kQStages; ++i) mbar_init(&full_bar[i], 1);
+    mbar_fence_init();
+    s_abort = 0;
+  }
+  __syncthreads();
+  if (tid == 0) {
+    for (int i = 0; i < kQStages && i < my_n; ++i) {
+      const size_t tau = blockIdx.x + (size_t)i * G;
+      mbar_arrive_expect_tx(&full_bar[i], row_in);
+      bulk_g2s(xin + i * slot_in, x + tau * row_in, row_in, &full_bar[i]);
+    }
+  }
+  pdl_wait();  // routing results are visible from here on
+  pdl_launch_dependents();
+  if (p.perf && tid == 0) perf_begin(p);
+
+  int nv = 0;  // variants so far: selects the quantised-row buffer
+  for (int i = 0; i < my_n; ++i) {
+    const size_t tau = blockIdx.x + (size_t)i * G;
+    const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
+    const int stage = i % kQStages;
+    const uint32_t parity = (uint32_t)(i / kQStages) & 1u;
+    PickTable& tab = tabs[i & 1];
+    const uint8_t* row = xin + stage * slot_in;
+
+    const bool ok = mbar_wait_bounded(&full_bar[stage], parity, p.status, p.timeout_ns);
+    if (!ok) s_abort = 1;
+    // the buffer of this token's first variant was last read by the bulk
+    // group two variants back: at most one newer group may still be reading
+    if (tid == 0) bulk_wait_read<1>();
+    if (warp == 0) build_picks(p, tau, s, t, tab, false, 0.f);
+    __syncthreads();
+    if (s_abort) break;
+    if (tid == 0 && i >= 1) {
+      if (p.seg_ready) publish_token(p, tabs[(i - 1) & 1]);
+      if (p.perf) perf_mark(p, tau - G);
+      // the previous token's source slot is free: its reads were generic loads
+      // that all finished before the barrier above
+      const int nxt = i - 1 + kQStages;
+      if (nxt < my_n) {
+        const int ps = (i - 1) % kQStages;
+        const size_t tn = blockIdx.x + (size_t)nxt * G;
+        mbar_arrive_expect_tx(&full_bar[ps], row_in);
+        bulk_g2s(xin + ps * slot_in, x + tn * row_in, row_in, &full_bar[ps]);
+      }
+    }
+    const int nsm = tab.n_sm, nbk = tab.n_bulk;
+    const int nvar = PE ? nsm + nbk : (nsm + nbk > 0 ? 1 : 0);
+    for (int j = 0; j < nvar; ++j) {
+      const int qs = nv & 1;
+      ++nv;
+      uint8_t* q = qbuf + qs * slot_out;
+      uint8_t* dq = dbuf + qs * slot_dyn;
+      if (PE && j > 0) {
+        if (tid == 0) bulk_wait_read<1>();
+        __syncthreads();
+      }
+      const float* srow = nullptr;
+      if (PE) {
+        const int seg = j < nsm ? tab.sm_seg[j] : tab.bulk_seg[j - nsm];
+        srow = p.qscales + (size_t)(seg / sh.W) * sh.h;
+      } else if (channel) {
+        srow = p.qscales;
+      }
+
+      if (MODE == 1) {
+        for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+          float f[8], sc[8];
+          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+          int qv[8];
+          if (srow) {
+            load_scales8(srow, v, sc);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) qv[k] = static_q(__fmul_rn(f[k], sc[k]));
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) qv[k] = static_q(__fmul_rn(f[k], s0));
+          }
+          *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
+        }
+      } else if (MODE == 2) {
+        float m = 0.f;
+        for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+          float f[8], sc[8];
+          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+          load_scales8(srow, v, sc);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(__fmul_rn(f[k], sc[k])));
+        }
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) s_red[warp] = m;
+        __syncthreads();
+        float amax = 0.f;
+#pragma unroll
+        for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
+        const float scale = __fdiv_rn(amax, 127.0f);
+        for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+          float f[8], sc[8];
+          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+          load_scales8(srow, v, sc);
+          int qv[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) qv[k] = amax == 0.f ? 0 : token_q(__fmul_rn(f[k], sc[k]), scale);
+          *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
+        }
+        if (tid == 0) reinterpret_cast<float*>(dq)[0] = scale;
+      } else {
+        // group (mode 3: 16 vectors) or block (mode 4: 4 vectors) per lane run;
+        // every lane of a warp takes part in the shuffles, past-the-end lanes
+        // with zeros
+        constexpr int kLanes = MODE == 3 ? 16 : 4;
+        for (uint32_t base = 0; base < nvec; base += kScatterThreads) {
+          const uint32_t v = base + tid;
+          const bool valid = v < nvec;
+          float f[8];
+          if (valid) {
+            unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+            if (PE) {
+              float sc[8];
+              load_scales8(srow, v, sc);
+#pragma unroll
+              for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
+            }
+          } else {
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = 0.f;
+          }
+          float m = 0.f;
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+#pragma unroll
+          for (int o = kLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+          if (MODE == 3) {
+            const float scale = __fdiv_rn(m, fp8_max(YT));
+            if (valid) {
+              uint32_t c[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k)
+                c[k] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(f[2 * k], scale), __fdiv_rn(f[2 * k + 1], scale));
+              *reinterpret_cast<uint2*>(q + v * 8) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+              if ((v & 15u) == 0) reinterpret_cast<float*>(dq)[v >> 4] = scale;
+            }
+          } else {
+            const int se = mx_exponent(m, elem_emax(YT));
+            const float inv = exp2_exact(-se);
+            if (valid) {
+              uint32_t c[4];
+#pragma unroll
+              for (int k = 0; k < 4; ++k) c[k] = cvt_y_pair(YT, __fmul_rn(f[2 * k], inv), __fmul_rn(f[2 * k + 1], inv));
+              if (YT == MOE_Y_FP4_E2M1)
+                *reinterpret_cast<uint32_t*>(q + v * 4) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+              else
+                *reinterpret_cast<uint2*>(q + v * 8) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+              if ((v & 3u) == 0) dq[v >> 2] = (uint8_t)(se + 127);
+            }
+          }
+        }
+      }
+      fence_proxy_async_smem();
+      __syncthreads();
+
+      // destinations of this variant: the pick (per-expert scales) or all picks
+      const int sm0 = PE ? (j < nsm ? j : 0) : 0, sm1 = PE ? (j < nsm ? j + 1 : 0) : nsm;
+      const int bk0 = PE ? (j < nsm ? 0 : j - nsm) : 0, bk1 = PE ? (j < nsm ? 0 : j - nsm + 1) : nbk;
+      if (tid == 0) {
+        for (int b = bk0; b < bk1; ++b) bulk_s2g(out + tab.bulk_dst[b] * row_out, q, row_out);
+        bulk_commit();
+      }
+      if (sm1 > sm0) {
+        for (uint32_t u = tid; u < row_out / 16; u += kScatterThreads) {
+          const int4 val = *reinterpret_cast<const int4*>(q + u * 16);
+          for (int b = sm0; b < sm1; ++b) st_v4(out + tab.sm_dst[b] * row_out + u * 16, val);
+        }
+      }
+      if (MODE != 1) {
+        const int nd = sh.ngroups;
+        const int ndst = (sm1 - sm0) + (bk1 - bk0);
+        uint8_t* dyn = static_cast<uint8_t*>(p.dyn_scales);
+        for (int idx = tid; idx < ndst * nd; idx += kScatterThreads) {
+          const int b = idx / nd, g = idx % nd;
+          const long long dst = b < sm1 - sm0 ? tab.sm_dst[sm0 + b] : tab.bulk_dst[bk0 + b - (sm1 - sm0)];
+          if (dyn_es == 4)
+            reinterpret_cast<float*>(dyn)[dst * nd + g] = reinterpret_cast<const float*>(dq)[g];
+          else
+            dyn[dst * nd + g] = dq[g];
+        }
+      }
+    }
+  }
+  __syncthreads();  // every thread's stores of the last token are issued
+  if (tid == 0 && !s_abort && my_n > 0) {
+    if (p.seg_ready) publish_token(p, tabs[(my_n - 1) & 1]);
+    bulk_wait_all<0>();
+    if (p.perf) perf_mark(p, blockIdx.x + (size_t)(my_n - 1) * G);
+  }
+  if (tid == 0) bulk_wait_all<0>();
+  if (p.perf) {
+    __shared__ int s_last;
+    perf_finish(p, &s_last);
+  }
+}
+
+// Rows that are not 16-byte multiples: element-wise, one token per CTA at a
+// time, every row by plain stores. Groups / blocks go one per warp.
+template <int MODE>
+__global__ void __launch_bounds__(kScatterThreads) scatter_quant_plain_kernel(ScatterParams p) {
+  __shared__ PickTable tab;
+  __shared__ float s_red[kScatterWarps];
+  const Shape sh = p.sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int n_tok = sh.W * sh.bs;
+  const int h = sh.h, dt = sh.x_dtype, yt = sh.ytype;
+  const bool pe = sh.scales_kind == MOE_SCALES_EXPERT;
+  pdl_wait();
+  pdl_launch_dependents();
+  if (p.perf && tid == 0) perf_begin(p);
+  for (size_t tau = blockIdx.x; tau < (size_t)n_tok; tau += gridDim.x) {
+    const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
+    if (warp == 0) {
+      build_picks(p, tau, s, t, tab, false, 0.f);
+      __syncwarp();
+      if (lane == 0) {  // both planes are carried by plain stores here
+        for (int j = 0; j < tab.n_bulk; ++j) {
+          tab.sm_dst[tab.n_sm + j] = tab.bulk_dst[j];
+          tab.sm_seg[tab.n_sm + j] = tab.bulk_seg[j];
+        }
+        tab.n_sm += tab.n_bulk;
+        tab.n_bulk = 0;
+      }
+    }
+    __syncthreads();
+    const int ns = tab.n_sm;
+    const int nvar = pe ? ns : 1;
+    const size_t xrow = tau * (size_t)h;
+    for (int j = 0; j < nvar; ++j) {
+      const int d0 = pe ? j : 0, d1 = pe ? j + 1 : ns;
+      const float* srow = nullptr;
+      float s0 = 1.f;
+      if (pe) srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * h;
+      else if (sh.scales_kind == MOE_SCALES_CHANNEL) srow = p.qscales;
+      else if (sh.scales_kind == MOE_SCALES_SCALAR) s0 = p.qscales[0];
+      auto elem = [&](int jx) {
+        const float v = load_elem(p.x, xrow + jx, dt);
+        return srow ? __fmul_rn(v, srow[jx]) : (sh.scales_kind == MOE_SCALES_SCALAR ? __fmul_rn(v, s0) : v);
+      };
+      if (MODE == 1) {
+        int8_t* o = static_cast<int8_t*>(p.expand_x);
+        for (int jx = tid; jx < h; jx += kScatterThreads) {
+          const int8_t qv = (int8_t)static_q(elem(jx));
+          for (int b = d0; b < d1; ++b) o[tab.sm_dst[b] * h + jx] = qv;
+        }
+      } else if (MODE == 2) {
+        float m = 0.f;
+        for (int jx = tid; jx < h; jx += kScatterThreads) m = fmaxf(m, fabsf(elem(jx)));
+#pragma unroll
+        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        if (lane == 0) s_red[warp] = m;
+        __syncthreads();
+        float amax = 0.f;
+        for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
+        const float scale = __fdiv_rn(amax, 127.0f);
+        int8_t* o = static_cast<int8_t*>(p.expand_x);
+        for (int jx = tid; jx < h; jx += kScatterThreads) {
+          const int8_t qv = amax == 0.f ? (int8_t)0 : (int8_t)token_q(elem(jx), scale);
+          for (int b = d0; b < d1; ++b) o[tab.sm_dst[b] * h + jx] = qv;
+        }
+        if (tid == 0)
+          for (int b = d0; b < d1; ++b) static_cast<float*>(p.dyn_scales)[tab.sm_dst[b]] = scale;
+        __syncthreads();  // s_red is reused by the next variant
+      } else {
+        const int gsz = MODE == 3 ? 128 : 32;
+        const int ng = sh.ngroups;
+        const bool fp4 = yt == MOE_Y_FP4_E2M1;
+        const int rob = sh.row_out;
+        uint8_t* o = static_cast<uint8_t*>(p.expand_x);
+        for (int g = warp; g < ng; g += kScatterWarps) {
+          const int j0 = g * gsz, j1 = min(h, j0 + gsz);
+          float m = 0.f;
+          for (int jx = j0 + lane; jx < j1; jx += 32) m = fmaxf(m, fabsf(elem(jx)));
+#pragma unroll
+          for (int off = 16; off > 0; off >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
+          if (MODE == 3) {
+            const float scale = __fdiv_rn(m, fp8_max(yt));
+            for (int jx = j0 + lane; jx < j1; jx += 32) {
+              const uint8_t c = m == 0.f ? (uint8_t)0
+                                         : (uint8_t)(cvt_y_pair(yt, __fdiv_rn(elem(jx), scale), 0.f) & 0xffu);
+              for (int b = d0; b < d1; ++b) o[tab.sm_dst[b] * rob + jx] = c;
+            }
+            if (lane == 0)
+              for (int b = d0; b < d1; ++b) static_cast<float*>(p.dyn_scales)[tab.sm_dst[b] * ng + g] = scale;
+          } else {
+            const int se = mx_exponent(m, elem_emax(yt));
+            const float inv = exp2_exact(-se);
+            if (fp4) {
+              for (int jp = j0 / 2 + lane; jp < j1 / 2; jp += 32) {
+                const uint8_t c = (uint8_t)cvt_fp4x2(__fmul_rn(elem(2 * jp), inv), __fmul_rn(elem(2 * jp + 1), inv));
+                for (int b = d0; b < d1; ++b) o[tab.sm_dst[b] * rob + jp] = c;
+              }
+            } else {
+              for (int jx = j0 + lane; jx < j1; jx += 32) {
+                const uint8_t c = (uint8_t)(cvt_y_pair(yt, __fmul_rn(elem(jx), inv), 0.f) & 0xffu);
+                for (int b = d0; b < d1; ++b) o[tab.sm_dst[b] * rob + jx] = c;
+              }
+            }
+            if (lane == 0)
+              for (int b = d0; b < d1; ++b) static_cast<uint8_t*>(p.dyn_scales)[tab.sm_dst[b] * ng + g] = (uint8_t)(se + 127);
+          }
+        }
+      }
+    }
+    __syncthreads();
+    if (p.seg_ready && tid == 0) {  // every thread's rows of this token are stored
+      __threadfence();
+      for (int k = 0; k < ns; ++k) publish_row(p, tab.sm_seg[k]);
+    }
+    if (p.perf && tid == 0) perf_mark(p, tau);
+    __syncthreads();
+  }
+  if (p.perf) {
+    __shared__ int s_last;
+    perf_finish(p, &s_last);
+  }
+}
+
+static size_t quant_smem(const Shape& sh) {
+  return kQStages * align128((size_t)sh.row_in) + kQSlots * align128((size_t)sh.row_out) +
+         kQSlots * align128((size_t)sh.ngroups * 4);
+}
+
+bool scatter_quant_tma_fits(const Shape& sh) { return quant_smem(sh) <= 200 * 1024; }
+
+template <typename KernelT>
+static cudaError_t launch_quant_persistent(KernelT kernel, const ScatterParams& p, cudaStream_t st, int num_sms) {
+  const size_t smem = quant_smem(p.sh);
+  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+  if (e != cudaSuccess) return e;
+  int per_sm = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScatterThreads, smem);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  const int n_tok = p.sh.W * p.sh.bs;
+  const int grid = max(1, min(n_tok, num_sms * per_sm));
+  PdlLaunch L(dim3(grid), dim3(kScatterThreads), smem, st);
+  return cudaLaunchKernelEx(&L.cfg, kernel, p);
+}
+
+template <int DT>
+static cudaError_t launch_quant_dt(const ScatterParams& p, cudaStream_t st, int nsm) {
+  const Shape& sh = p.sh;
+  const bool pe = sh.scales_kind == MOE_SCALES_EXPERT;
+  switch (sh.quant) {
+    case 1:
+      return pe ? launch_quant_persistent(scatter_quant_kernel<1, DT, MOE_Y_DEFAULT, true>, p, st, nsm)
+                : launch_quant_persistent(scatter_quant_kernel<1, DT, MOE_Y_DEFAULT, false>, p, st, nsm);
+    case 2:
+      return launch_quant_persistent(scatter_quant_kernel<2, DT, MOE_Y_DEFAULT, true>, p, st, nsm);
+    case 3:
+      if (sh.ytype == MOE_Y_FP8_E4M3)
+        return pe ? launch_quant_persistent(scatter_quant_kernel<3, DT, MOE_Y_FP8_E4M3, true>, p, st, nsm)
+                  : launch_quant_persistent(scatter_quant_kernel<3, DT, MOE_Y_FP8_E4M3, false>, p, st, nsm);
+      return pe ? launch_quant_persistent(scatter_quant_kernel<3, DT, MOE_Y_FP8_E5M2, true>, p, st, nsm)
+                : launch_quant_persistent(scatter_quant_kernel<3, DT, MOE_Y_FP8_E5M2, false>, p, st, nsm);
+    default:
+      if (sh.ytype == MOE_Y_FP8_E4M3)
+        return launch_quant_persistent(scatter_quant_kernel<4, DT, MOE_Y_FP8_E4M3, false>, p, st, nsm);
+      if (sh.ytype == MOE_Y_FP8_E5M2)
+        return launch_quant_persistent(scatter_quant_kernel<4, DT, MOE_Y_FP8_E5M2, false>, p, st, nsm);
+      return launch_quant_persistent(scatter_quant_kernel<4, DT, MOE_Y_FP4_E2M1, false>, p, st, nsm);
+  }
+}
+
+cudaError_t launch_scatter_quant(const ScatterParams& p, cudaStream_t st, int num_sms, bool tma) {
+  const Shape& sh = p.sh;
+  if (sh.W * sh.bs == 0) return cudaSuccess;
+  if (!tma) {
+    const int grid = max(1, min(sh.W * sh.bs, num_sms * 4));
+    PdlLaunch L(dim3(grid), dim3(kScatterThreads), 0, st);
+    switch (sh.quant) {
+      case 1: return cudaLaunchKernelEx(&L.cfg, scatter_quant_plain_kernel<1>, p);
+      case 2: return cudaLaunchKernelEx(&L.cfg, scatter_quant_plain_kernel<2>, p);
+      case 3: return cudaLaunchKernelEx(&L.cfg, scatter_quant_plain_kernel<3>, p);
+      default: return cudaLaunchKernelEx(&L.cfg, scatter_quant_plain_kernel<4>, p);
+    }
+  }
+  return sh.x_dtype == MOE_F16 ? launch_quant_dt<MOE_F16>(p, st, num_sms) : launch_quant_dt<MOE_BF16>(p, st, num_sms);
+}
+
+}  // namespace crs

@@ -25,6 +25,9 @@ MOE_I32, MOE_F16, MOE_BF16 = 0, 1, 2
 DTYPE_CODE = {torch.int32: MOE_I32, torch.float16: MOE_F16, torch.bfloat16: MOE_BF16}
 PLANE_RULE, PLANE_STORES_ONLY, PLANE_BULK_ALL = 0, 1, 2
 COMBINE_GATHER, COMBINE_TWO_PHASE, COMBINE_PUT_ONLY = 0, 1, 2
+Y_DEFAULT, Y_FP8_E4M3, Y_FP8_E5M2, Y_FP4_E2M1 = 0, 1, 2, 3
+Y_CODE = {"": Y_DEFAULT, "int8": Y_DEFAULT, "fp8_e4m3": Y_FP8_E4M3, "fp8_e5m2": Y_FP8_E5M2, "fp4_e2m1": Y_FP4_E2M1}
+SCALES_NONE, SCALES_SCALAR, SCALES_CHANNEL, SCALES_EXPERT = 0, 1, 2, 3
 BULK_MIN_BYTES = 2 * 1024 * 1024
 
 # Every symbol include/moe.h declares.
@@ -50,9 +53,9 @@ class MoeConfig(ctypes.Structure):
         ("mask_kind", ctypes.c_int32), ("x_dtype", ctypes.c_int32),
         ("plane_policy", ctypes.c_int32), ("bulk_min_bytes", ctypes.c_int64),
         ("combine_mode", ctypes.c_int32), ("wait_timeout_us", ctypes.c_int32),
-        ("ffn_intermediate", ctypes.c_int32), ("reserved0", ctypes.c_int32),
+        ("ffn_intermediate", ctypes.c_int32), ("expand_dtype", ctypes.c_int32),
         ("prof_events", ctypes.c_void_p), ("seg_ready", ctypes.c_void_p),
-        ("seg_ready_ticket", ctypes.c_uint32), ("reserved1", ctypes.c_int32),
+        ("seg_ready_ticket", ctypes.c_uint32), ("scales_kind", ctypes.c_int32),
         ("performance_info", ctypes.c_void_p),
     ]
 
@@ -61,11 +64,13 @@ def config(ep_world_size: int, bs: int, h: int, topk: int, moe_expert_num: int, 
            zero_expert_num: int = 0, copy_expert_num: int = 0, quant_mode: int = 0, mask_kind: int = 0,
            plane_policy: int = PLANE_RULE, bulk_min_bytes: int = BULK_MIN_BYTES,
            combine_mode: int = COMBINE_GATHER, wait_timeout_us: int = 2_000_000,
-           ffn_intermediate: int = 0) -> MoeConfig:
+           ffn_intermediate: int = 0, expand_dtype=Y_DEFAULT, scales_kind: int = SCALES_NONE) -> MoeConfig:
+    """moe_config_t; expand_dtype is a MOE_Y_* code or one of the names in Y_CODE."""
     dt = DTYPE_CODE[x_dtype] if isinstance(x_dtype, torch.dtype) else int(x_dtype)
+    yd = Y_CODE[expand_dtype] if isinstance(expand_dtype, str) else int(expand_dtype)
     return MoeConfig(ep_world_size, bs, h, topk, moe_expert_num, zero_expert_num, copy_expert_num, 0,
                      quant_mode, mask_kind, dt, plane_policy, bulk_min_bytes, combine_mode, wait_timeout_us,
-                     ffn_intermediate, 0, None, None, 0, 0, None)
+                     ffn_intermediate, yd, None, None, 0, scales_kind, None)
 
 
 _lib = None
@@ -81,7 +86,7 @@ def lib() -> ctypes.CDLL:
         P, C = ctypes.c_void_p, ctypes.POINTER(MoeConfig)
         L.moe_get_workspace_size.argtypes = [C, ctypes.POINTER(ctypes.c_size_t), ctypes.POINTER(ctypes.c_int64)]
         L.moe_workspace_init.argtypes = [C, P, ctypes.c_size_t, P]
-        L.moe_dispatch.argtypes = [C, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
+        L.moe_dispatch.argtypes = [C, P, P, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_combine.argtypes = [C, P, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_dispatch_ffn_combine.argtypes = [C, P, P, P, P, P, P, P, P, P, ctypes.c_size_t, P]
         L.moe_combine_noalloc.argtypes = [C, P, P, P, P, P, P, P, P, P, P]
@@ -170,9 +175,12 @@ def workspace_init(cfg: MoeConfig, ws: torch.Tensor, stream=None):
 
 
 def dispatch(cfg: MoeConfig, x, expert_ids, active_mask, expert_scales, expand_x, dynamic_scales,
-             assist_info, ep_recv_count, expand_scales=None, seg_plane=None, ws=None, stream=None):
+             assist_info, ep_recv_count, expand_scales=None, seg_plane=None, ws=None, stream=None, scales=None):
+    """moe_dispatch; `scales` is the fp32 coefficient / smoothing input that
+    cfg.scales_kind describes (None when it is SCALES_NONE)."""
     _check(lib().moe_dispatch(ctypes.byref(cfg), _ptr(x), _ptr(expert_ids), _ptr(active_mask),
-                              _ptr(expert_scales), _ptr(expand_x), _ptr(dynamic_scales), _ptr(assist_info),
+                              _ptr(expert_scales), _ptr(scales), _ptr(expand_x), _ptr(dynamic_scales),
+                              _ptr(assist_info),
                               _ptr(ep_recv_count), _ptr(expand_scales), _ptr(seg_plane), _ptr(ws),
                               ws.numel() * ws.element_size(), _stream(stream)), "moe_dispatch")
 
@@ -227,14 +235,30 @@ def alloc_workspace(cfg: MoeConfig, device="cuda", stream=None) -> torch.Tensor:
 
 def alloc_dispatch_outputs(cfg: MoeConfig, x_dtype: torch.dtype, device="cuda", expand_scales: bool = True,
                            seg_plane: bool = False) -> dict:
+    """expand_x is x's type (quant_mode 0), int8 (1, 2) or uint8 codes (3, 4;
+    [W, A, h/2] for packed FP4); dynamic_scales [W, A] fp32 (2), [W, A,
+    ceil(h/128)] fp32 (3), [W, A, ceil(h/32)] uint8 E8M0 (4), else None."""
     _, A = workspace_size(cfg)
     W, h = cfg.ep_world_size, cfg.h
     L = cfg.moe_expert_num // W
-    q = cfg.quant_mode == 2
+    qm = cfg.quant_mode
     sdt = torch.int32 if x_dtype == torch.int32 else torch.float32
+    if qm == 0:
+        ex = torch.empty((W, A, h), dtype=x_dtype, device=device)
+    elif qm in (1, 2):
+        ex = torch.empty((W, A, h), dtype=torch.int8, device=device)
+    else:
+        ex = torch.empty((W, A, h // 2 if cfg.expand_dtype == Y_FP4_E2M1 else h), dtype=torch.uint8, device=device)
+    dyn = None
+    if qm == 2:
+        dyn = torch.empty((W, A), dtype=torch.float32, device=device)
+    elif qm == 3:
+        dyn = torch.empty((W, A, (h + 127) // 128), dtype=torch.float32, device=device)
+    elif qm == 4:
+        dyn = torch.empty((W, A, (h + 31) // 32), dtype=torch.uint8, device=device)
     return {
-        "expand_x": torch.empty((W, A, h), dtype=torch.int8 if q else x_dtype, device=device),
-        "dynamic_scales": torch.empty((W, A), dtype=torch.float32, device=device) if q else None,
+        "expand_x": ex,
+        "dynamic_scales": dyn,
         "assist_info": torch.empty((W, A, 3), dtype=torch.int32, device=device),
         "ep_recv_count": torch.empty((W, L * W), dtype=torch.int32, device=device),
         "expand_scales": torch.empty((W, A), dtype=sdt, device=device) if expand_scales else None,

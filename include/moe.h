@@ -50,7 +50,7 @@ extern "C" {
 typedef enum {
   MOE_OK = 0,
   MOE_ERR_INVALID_ARG = 1,   /* a value out of the ranges below, a NULL array, misalignment */
-  MOE_ERR_UNSUPPORTED = 2,   /* const experts, quant_mode other than 0/2, int32 x with quant */
+  MOE_ERR_UNSUPPORTED = 2,   /* const experts, quant_mode outside 0..4, int32 x with quant */
   MOE_ERR_WORKSPACE = 3,     /* workspace NULL or smaller than moe_get_workspace_size */
   MOE_ERR_BAD_EXPERT_ID = 4, /* an active id outside [0, E+Z+C), or a routed id twice in a token */
   MOE_ERR_MASK_ORDER = 5,    /* a 1D active mask with a true after a false */
@@ -61,6 +61,25 @@ typedef enum {
 } moe_status_t;
 
 typedef enum { MOE_I32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype_t;
+
+/* Element type of quantised expand_x rows (moe_config_t.expand_dtype; [DISP]
+ * 约束说明 quantMode相关约束: per-group rows are FP8, MX rows FP8 or FP4). */
+enum {
+  MOE_Y_DEFAULT = 0,   /* x's type (quant_mode 0) or int8 (quant_mode 1, 2) */
+  MOE_Y_FP8_E4M3 = 1,  /* OCP FP8 E4M3 (max 448, S.1111.111 = NaN) */
+  MOE_Y_FP8_E5M2 = 2,  /* OCP FP8 E5M2 (max 57344) */
+  MOE_Y_FP4_E2M1 = 3,  /* OCP FP4 E2M1 (max 6), two codes per byte, the even element
+                          in the low nibble; quant_mode 4 only, h even */
+};
+
+/* Shape of the optional `scales` input of moe_dispatch (moe_config_t.scales_kind;
+ * [DISP] 参数说明 scalesOptional and 约束说明 quantMode相关约束). fp32. */
+enum {
+  MOE_SCALES_NONE = 0,
+  MOE_SCALES_SCALAR = 1,   /* (1,): quant_mode 1 only */
+  MOE_SCALES_CHANNEL = 2,  /* (h,): quant_mode 1 only */
+  MOE_SCALES_EXPERT = 3,   /* (E, h): the row of the pick's expert; quant_mode 1, 2, 3 */
+};
 
 /* Which plane carries each (local expert, source) segment ([SHMEM] 方案设计). */
 enum {
@@ -89,7 +108,23 @@ typedef struct {
   int32_t zero_expert_num;  /* Z >= 0: ids [E, E+Z) contribute nothing */
   int32_t copy_expert_num;  /* C >= 0: ids [E+Z, E+Z+C) contribute w * x */
   int32_t const_expert_num; /* must be 0 (the page gives no formula) */
-  int32_t quant_mode;       /* 0: none; 2: per-token dynamic int8 */
+  int32_t quant_mode;       /* [DISP] quantMode; x must be fp16 / bf16 when != 0:
+                               0: none;
+                               1: static int8, q = clamp(rne(x * s), -128, 127), s from
+                                  `scales` (any MOE_SCALES_* but NONE);
+                               2: per-token dynamic int8, x' = x * s[e] when scales_kind
+                                  is MOE_SCALES_EXPERT (per-expert smoothing), scale =
+                                  amax|x'| / 127, q = clamp(rne(x' / scale), -127, 127);
+                               3: per-group dynamic FP8 (expand_dtype E4M3 / E5M2):
+                                  groups of 128 elements, scale_g = amax_g / FMAX,
+                                  q = fp8_satfinite_rne(x' / scale_g); optional smoothing
+                                  as for 2;
+                               4: MX (OCP Microscaling v1.0): blocks of 32 share
+                                  X = 2^(floor(log2 amax) - emax_elem), clamped to
+                                  [2^-127, 2^127], stored as an E8M0 byte; q = x / X in
+                                  expand_dtype (E4M3 / E5M2 / E2M1), RNE, saturating; no
+                                  scales input. A zero group / block gets scale 0 (mode 3)
+                                  or byte 0 (mode 4) and zero codes. */
   int32_t mask_kind;        /* 0: no mask; 1: (BS,) per token; 2: (BS, K) per pick */
   int32_t x_dtype;          /* moe_dtype_t of x, expand_x (quant 0), expert_out, x_out;
                                expert_scales are int32 for MOE_I32, fp32 otherwise */
@@ -98,7 +133,8 @@ typedef struct {
   int32_t combine_mode;     /* MOE_COMBINE_* */
   int32_t wait_timeout_us;  /* bound on every flag wait (two-phase combine), > 0 */
   int32_t ffn_intermediate; /* I for moe_dispatch_ffn_combine, else 0 */
-  int32_t reserved0;        /* must be 0 */
+  int32_t expand_dtype;     /* MOE_Y_*: 0 for quant_mode 0..2; E4M3 / E5M2 for 3;
+                               E4M3 / E5M2 / E2M1 for 4 */
   void* const* prof_events; /* optional host array {start, stop} of cudaEvent_t: recorded
                                on `stream` around the call's main kernel (scatter for
                                dispatch, reduce for combine, the gate/up GEMM for
@@ -113,7 +149,7 @@ typedef struct {
                                another stream may poll it with acquire loads. NULL: none */
   uint32_t seg_ready_ticket; /* value this call stores into seg_ready; pick one the array
                                does not hold yet (e.g. a per-call counter) */
-  int32_t reserved1;        /* must be 0 */
+  int32_t scales_kind;      /* MOE_SCALES_*: shape of moe_dispatch's `scales` input */
   int64_t* performance_info; /* optional device array [W] int64 (moe_dispatch only; [DISP]
                                参数说明 performanceInfoOptional): each call ADDS to entry s
                                rank s's communication time in nanoseconds (%globaltimer), from
@@ -133,26 +169,31 @@ moe_status_t moe_get_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, i
  * reallocating it. Enqueued on `stream`. */
 moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, void* stream);
 
-/* Dispatch ([DISP] 接口功能: expandXOut = AllToAllV(X), quantised first for quantMode 2).
+/* Dispatch ([DISP] 接口功能: expandXOut = AllToAllV(X), quantised first when
+ * quant_mode != 0).
  *
  * Inputs (device, row-major, leading W axis):
  *   x             [W][bs][h] of x_dtype
  *   expert_ids    [W][bs][K] int32
  *   active_mask   NULL, [W][bs] (mask_kind 1) or [W][bs][K] (mask_kind 2) bytes, 0 = false
  *   expert_scales NULL or [W][bs][K] (int32 / fp32); needed iff expand_scales != NULL
+ *   scales        fp32 shaped as scales_kind says ((1,), (h,) or (E, h)), 16-byte
+ *                 aligned; NULL iff scales_kind is MOE_SCALES_NONE
  * Outputs (device):
- *   expand_x       [W][A][h]: rank d's received rows, grouped by local expert, then
- *                  by source rank, then in (token, k) order; int8 for quant_mode 2
- *   dynamic_scales [W][A] fp32, one per row (quant_mode 2; else may be NULL)
+ *   expand_x       [W][A][row bytes]: rank d's received rows, grouped by local expert,
+ *                  then by source rank, then in (token, k) order; x's type for quant_mode
+ *                  0, int8 for 1 and 2, FP8 codes (h bytes) or packed FP4 (h/2 bytes)
+ *   dynamic_scales per row: quant_mode 2: [W][A] fp32; 3: [W][A][ceil(h/128)] fp32;
+ *                  4: [W][A][ceil(h/32)] E8M0 bytes; NULL for quant_mode 0 and 1
  *   assist_info    [W][A][3] int32: (src_rank, src_token, src_topk) of each row
  *   ep_recv_count  [W][L*W] int32: running row count over segments le*W + s of rank d
  *   expand_scales  NULL or [W][A]: the row's weight expert_scales[s][t][k]
  *   seg_plane      NULL or [W][L*W] uint8: 1 where the segment went by bulk copies
- * Alignment: every array 16-byte aligned; rows use TMA only when h*elem bytes
- * (and h for int8 output) are multiples of 16, else plain stores carry all rows. */
+ * Alignment: every array 16-byte aligned; rows use TMA only when the input and
+ * output row bytes are multiples of 16, else plain stores carry all rows. */
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
-                          const uint8_t* active_mask, const void* expert_scales, void* expand_x,
-                          float* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
+                          const uint8_t* active_mask, const void* expert_scales, const float* scales,
+                          void* expand_x, void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
                           void* expand_scales, uint8_t* seg_plane, void* ws, size_t ws_bytes,
                           void* stream);
 

@@ -34,13 +34,16 @@ def device_inputs(wl: WL.Workload, inp: dict) -> dict:
         "expert_ids": to_dev(inp["expert_ids"]),
         "active_mask": to_dev(inp.get("active_mask")),
         "expert_scales": to_dev(inp["expert_scales"]),
+        "quant_scales": to_dev(inp.get("quant_scales")),
     }
 
 
 def make_cfg(wl: WL.Workload, **kw) -> M.MoeConfig:
+    q = kw.pop("quant_mode", wl.quant_mode)
     return M.config(wl.ep_world_size, wl.bs, wl.h, wl.topk, wl.moe_expert_num, TORCH_DT[wl.x_dtype],
                     zero_expert_num=wl.zero_expert_num, copy_expert_num=wl.copy_expert_num,
-                    quant_mode=kw.pop("quant_mode", wl.quant_mode), mask_kind=wl.mask_kind, **kw)
+                    quant_mode=q, mask_kind=wl.mask_kind, expand_dtype=wl.y_dtype if q else "",
+                    scales_kind=wl.scales_kind if q else 0, **kw)
 
 
 def gpu_dispatch(wl: WL.Workload, dev: dict, plane_policy: int = M.PLANE_RULE,
@@ -56,7 +59,7 @@ def gpu_dispatch(wl: WL.Workload, dev: dict, plane_policy: int = M.PLANE_RULE,
                 t.view(torch.uint8).fill_(0xA5)
     M.dispatch(cfg, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
                out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"],
-               out["seg_plane"], ws)
+               out["seg_plane"], ws, scales=dev.get("quant_scales"))
     st = M.get_device_status(ws)
     if check_status:
         assert st == 0, f"device status {M.STATUS.get(st, st)}"
@@ -99,7 +102,7 @@ def compare_dispatch(wl: WL.Workload, got: dict, ref: dict, plane_ref=None):
             assert np.array_equal(es[d, :n].view(np.uint32), ref["expand_scales"][d, :n].view(np.uint32)), \
                 f"expand_scales rank {d}"
         if ds is not None:
-            assert np.array_equal(ds[d, :n].view(np.uint32), ref["dynamic_scales"][d, :n].view(np.uint32)), \
+            assert np.array_equal(ds[d, :n].view(np.uint8), ref["dynamic_scales"][d, :n].view(np.uint8)), \
                 f"dynamic_scales rank {d}"
     if plane_ref is not None and got.get("seg_plane") is not None:
         assert np.array_equal(to_host(got["seg_plane"]), plane_ref), "segment planes"

@@ -73,8 +73,11 @@ def test_workspace_query_and_capacity(lib):
     ("h", 0, "INVALID_ARG"),
     ("bs", -1, "INVALID_ARG"),
     ("const_expert_num", 1, "UNSUPPORTED"),
-    ("quant_mode", 1, "UNSUPPORTED"),
-    ("quant_mode", 3, "UNSUPPORTED"),
+    ("quant_mode", 1, "INVALID_ARG"),      # static quantisation needs a scales input
+    ("quant_mode", 3, "INVALID_ARG"),      # per-group needs an FP8 expand_dtype
+    ("quant_mode", 5, "UNSUPPORTED"),
+    ("expand_dtype", 1, "INVALID_ARG"),    # quantised types only with quant_mode 3 / 4
+    ("scales_kind", 3, "INVALID_ARG"),
     ("mask_kind", 3, "INVALID_ARG"),
     ("x_dtype", 7, "INVALID_ARG"),
     ("plane_policy", 3, "INVALID_ARG"),
@@ -110,3 +113,28 @@ def test_binding_refuses_cpu_tensors(lib):
     x = torch.zeros(2, 8, 16, dtype=torch.int32)
     with pytest.raises(ValueError):
         lib.dispatch(cfg, x, x, None, None, x, None, x, x, ws=x)
+
+
+def test_quant_rules_agree_with_oracle(lib):
+    """The library's host validation of quant_mode / expand_dtype / scales_kind
+    gives the same verdict as the oracle's configuration rules, over every
+    combination (and an odd h, which FP4 rows cannot pack)."""
+    import itertools
+    import torch
+    import workloads as WL
+    from oracle import oracle as O
+    names = {v: k for k, v in O.Y_KIND.items() if k != "int8"}
+    code = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED"}
+    for xdt, q, y, k, h in itertools.product((torch.bfloat16, torch.int32), range(6), range(4), range(4), (64, 63)):
+        cfg = lib.config(4, 8, h, 2, 8, xdt, quant_mode=q, expand_dtype=y, scales_kind=k)
+        try:
+            lib.workspace_size(cfg)
+            got = "OK"
+        except lib.MoeError as e:
+            got = e.name
+        wl = WL.Workload("r", 4, 8, h, 2, 8, WL.X_BF16 if xdt == torch.bfloat16 else WL.X_INT32, quant_mode=q,
+                         y_dtype=names[y], scales_kind=k)
+        cfgo = O.make_cfg(wl)
+        cfgo.y_kind, cfgo.scales_kind = y, k  # also when quant_mode is 0
+        want = code[int(O.lib().orc_check_cfg(ctypes.byref(cfgo)))]
+        assert got == want, (xdt, q, y, k, h, got, want)

@@ -48,9 +48,7 @@ def run_and_compare(wl, inp=None, plane_policy=0, bulk_min_bytes=O.DEFAULT_BULK_
 
 
 def _tma_rows(wl):
-    row_in = wl.h * wl.es
-    row_out = wl.h if wl.quant_mode == 2 else row_in
-    return row_in % 16 == 0 and row_out % 16 == 0
+    return wl.h * wl.es % 16 == 0 and wl.row_out_bytes % 16 == 0
 
 
 @pytest.mark.parametrize("name", SMALL)

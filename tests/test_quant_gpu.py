@@ -1,0 +1,137 @@
+"""Dispatch with quantMode 1 (static int8), 2 with per-expert smoothing, 3
+(per-group FP8) and 4 (MX FP8 / FP4) on the GPU against the oracle: expand_x
+codes, dynamic scales (fp32 bits / E8M0 bytes), assist_info and the receive
+counts are compared byte for byte (both sides round the same fp32 values to
+nearest even, so every code is unique)."""
+import numpy as np
+import pytest
+import torch
+
+import workloads as WL
+from oracle import oracle as O
+
+pytestmark = pytest.mark.gpu
+
+if torch.cuda.is_available():
+    import gpu_harness as H
+    from combine_route_scan_gb300 import build as B
+    from combine_route_scan_gb300 import moe as M
+    B.build()
+
+# (quant_mode, expand type, scales kind)
+MODES = [(1, "", 1), (1, "", 2), (1, "", 3), (2, "", 3), (3, "fp8_e4m3", 0), (3, "fp8_e5m2", 0),
+         (3, "fp8_e4m3", 3), (4, "fp8_e4m3", 0), (4, "fp8_e5m2", 0), (4, "fp4_e2m1", 0)]
+
+
+def mode_id(m):
+    return f"q{m[0]}_{m[1] or 'int8'}_s{m[2]}"
+
+
+def run(wl, plane_policy=M.PLANE_RULE if torch.cuda.is_available() else 0, bulk_min_bytes=None):
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    kw = {} if bulk_min_bytes is None else {"bulk_min_bytes": bulk_min_bytes}
+    got, ws, _ = H.gpu_dispatch(wl, dev, plane_policy=plane_policy, **kw)
+    H.compare_dispatch(wl, got, ref)
+    return got, ref
+
+
+@pytest.mark.parametrize("mode", MODES, ids=mode_id)
+@pytest.mark.parametrize("dt", [WL.X_BF16, WL.X_FP16])
+def test_quant_small_tma_rows(mode, dt):
+    """h = 256: TMA rows, several tokens per CTA, masks and special experts."""
+    q, y, k = mode
+    wl = WL.Workload("qs", 4, 16, 256, 4, 16, dt, zero_expert_num=1, copy_expert_num=1, mask_kind=2,
+                     special_p=0.1, mask_false_p=0.1, quant_mode=q, y_dtype=y, scales_kind=k, seed=31)
+    run(wl)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=mode_id)
+def test_quant_bulk_plane(mode):
+    """Every remote segment on the TMA bulk plane (rows leave from the shared
+    quantised-row buffers by bulk copies)."""
+    q, y, k = mode
+    wl = WL.Workload("qb", 4, 32, 512, 4, 8, WL.X_BF16, ids="zipf", quant_mode=q, y_dtype=y, scales_kind=k, seed=32)
+    run(wl, plane_policy=M.PLANE_BULK_ALL)
+
+
+@pytest.mark.parametrize("mode", MODES, ids=mode_id)
+def test_quant_ragged_rows(mode):
+    """h = 200 (partial last group / block; rows that are not 16-byte
+    multiples go by plain stores) and h = 12 fp16."""
+    q, y, k = mode
+    for h, dt in ((200, WL.X_BF16), (12, WL.X_FP16)):
+        wl = WL.Workload("qr", 4, 9, h, 3, 8, dt, mask_kind=1, quant_mode=q, y_dtype=y, scales_kind=k, seed=33)
+        run(wl)
+
+
+@pytest.mark.parametrize("mode", [(2, "", 3), (3, "fp8_e4m3", 0), (3, "fp8_e5m2", 3), (4, "fp4_e2m1", 0),
+                                  (4, "fp8_e4m3", 0), (1, "", 3)], ids=mode_id)
+def test_quant_decode_shape(mode):
+    """The perf shape of the combine README (W8 bs32 h7168 K8, 8 experts per
+    rank), every row compared."""
+    q, y, k = mode
+    wl = WL.WORKLOADS["w8_bs32_h7168_k8_e64_f16"].with_(quant_mode=q, y_dtype=y, scales_kind=k)
+    run(wl)
+
+
+def test_quant_values_cover_the_ranges():
+    """Scale the inputs so that FP8 E4M3 / MX blocks see saturation, subnormal
+    codes and zero groups, then compare bytes."""
+    wl = WL.Workload("qv", 2, 8, 384, 2, 4, WL.X_BF16, quant_mode=3, y_dtype="fp8_e4m3", seed=34)
+    inp = WL.make_inputs(wl)
+    x = WL.bf16_bits_to_fp32(inp["x"])
+    x[0, 0, :128] = 0.0                       # a zero group
+    x[0, 1, :] *= np.float32(1e-30)           # tiny values
+    x[1, 2, 5] = np.float32(3e4)              # one huge outlier per group
+    inp["x"] = WL.fp32_to_bf16_bits(x)
+    for q, y in ((3, "fp8_e4m3"), (3, "fp8_e5m2"), (4, "fp8_e4m3"), (4, "fp4_e2m1"), (4, "fp8_e5m2")):
+        w = wl.with_(quant_mode=q, y_dtype=y)
+        ref = O.dispatch(w, inp)
+        dev = H.device_inputs(w, inp)
+        got, _, _ = H.gpu_dispatch(w, dev)
+        H.compare_dispatch(w, got, ref)
+
+
+def test_quant_ready_flags_and_performance_info():
+    """The quantising scatter publishes ready flags and per-rank times too."""
+    wl = WL.Workload("qf", 4, 24, 512, 4, 16, WL.X_BF16, quant_mode=3, y_dtype="fp8_e4m3", scales_kind=3, seed=35)
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    L = wl.moe_expert_num // wl.ep_world_size
+    for policy in (M.PLANE_RULE, M.PLANE_BULK_ALL):
+        cfg = H.make_cfg(wl, plane_policy=policy)
+        ws = M.alloc_workspace(cfg)
+        out = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+        flags = torch.zeros((wl.ep_world_size, L * wl.ep_world_size), dtype=torch.int32, device="cuda")
+        perf = torch.zeros(wl.ep_world_size, dtype=torch.int64, device="cuda")
+        c = M.with_performance_info(M.with_seg_ready(cfg, flags, 5), perf)
+        M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
+                   out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws,
+                   scales=dev["quant_scales"])
+        assert M.get_device_status(ws) == 0
+        assert bool((flags == 5).all())
+        assert bool((perf >= 0).all())
+        H.compare_dispatch(wl, out, ref)
+
+
+def test_quant_argument_errors():
+    wl = WL.Workload("qe", 2, 4, 64, 2, 4, WL.X_BF16, quant_mode=1, scales_kind=2, seed=36)
+    inp = WL.make_inputs(wl)
+    dev = H.device_inputs(wl, inp)
+    cfg = H.make_cfg(wl)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, torch.bfloat16)
+    args = (dev["x"], dev["expert_ids"], None, dev["expert_scales"], out["expand_x"], None, out["assist_info"],
+            out["ep_recv_count"], None, None, ws)
+    with pytest.raises(M.MoeError) as ei:  # scales declared but not passed
+        M.dispatch(cfg, *args)
+    assert ei.value.name == "INVALID_ARG"
+    buf = torch.zeros(80, dtype=torch.float32, device="cuda")
+    with pytest.raises(M.MoeError) as ei:  # scales not 16-byte aligned
+        M.dispatch(cfg, *args, scales=buf[1:65])
+    assert ei.value.name == "INVALID_ARG"
+    M.dispatch(cfg, *args, scales=buf[4:68])
+    assert M.get_device_status(ws) == 0
