@@ -40,6 +40,9 @@ METRIC = "dispatch+combine GB/s and tokens/s on 1 GB300; fraction of 8 TB/s HBM 
 DEFAULT_WORKLOAD = "w16_bs256_h7168_k8_e256_bf16_zipf"
 FFN_WORKLOAD = "w8_bs64_h2048_k8_e128_bf16_ffn"
 SMALL_WORKLOADS = ("w8_bs32_h7168_k8_e64_f16", "w8_bs32_h7168_k8_e64_f16_q2", "w8_bs32_h7168_k8_e64_i32")
+# quantised dispatch variants: quantMode, expanded element type, scales input kind
+QUANT_MODES = ("q2_int8_s0", "q1_int8_s1", "q2_int8_s3", "q3_fp8_e4m3_s0", "q3_fp8_e4m3_s3", "q4_fp8_e4m3_s0",
+               "q4_fp4_e2m1_s0")
 HBM_NOMINAL_GBPS = 8000.0
 L2_BYTES = 129 * 1024 * 1024
 FALLBACK_HBM_GBPS = 6800.0
@@ -61,6 +64,9 @@ def parse_args():
     ap.add_argument("--small-workloads", default=",".join(SMALL_WORKLOADS),
                     help="workloads that fit in L2, timed per call with an L2 flush before each step")
     ap.add_argument("--small-steps", type=int, default=50)
+    ap.add_argument("--quant-modes", default=",".join(QUANT_MODES),
+                    help="quantised dispatch variants timed on the main workload (mode/type/scales)")
+    ap.add_argument("--quant-steps", type=int, default=50)
     return ap.parse_args()
 
 
@@ -85,13 +91,17 @@ def algorithmic_bytes(wl: WL.Workload, inp: dict) -> dict:
     W, bs, K, h = wl.ep_world_size, wl.bs, wl.topk, wl.h
     L = wl.moe_expert_num // W
     r_in = h * wl.es
-    r_out = h if wl.quant_mode == 2 else r_in
+    r_out = wl.row_out_bytes
     picks = W * bs * K
     mask = 0 if inp.get("active_mask") is None else inp["active_mask"].size
     ep = W * L * W * 4
     P, Cp, Nt = c["P"], c["copy"], c["tok_routed"]
-    meta = P * (4 + 12 + 4) + (P * 4 if wl.quant_mode == 2 else 0)  # weights read; assist, expand_scales written
-    scatter = Nt * r_in + P * r_out + meta
+    meta = P * (4 + 12 + 4)  # weights read; assist, expand_scales written
+    # dynamic scales written: one fp32 per row (mode 2), per 128-group (3), one byte per 32-block (4)
+    dyn = {2: 4, 3: 4 * ((h + 127) // 128), 4: (h + 31) // 32}.get(wl.quant_mode, 0)
+    # the scales input, read once: (1,), (h,) or (E, h) fp32
+    qs = {1: 4, 2: h * 4, 3: wl.moe_expert_num * h * 4}.get(wl.scales_kind, 0) if wl.quant_mode else 0
+    scatter = Nt * r_in + P * r_out + meta + P * dyn + qs
     dispatch = scatter + picks * 4 + mask + ep
     reduce_ = P * r_in + Cp * r_in + picks * 8 + mask + W * bs * r_in
     combine = reduce_ + P * 12 + ep
@@ -461,6 +471,77 @@ def measure_small(args, M, torch, stream):
     return res
 
 
+def parse_quant_mode(tag: str):
+    """'q3_fp8_e4m3_s0' -> (3, 'fp8_e4m3', 0); 'q1_int8_s1' -> (1, '', 1)."""
+    q, rest = tag.split("_", 1)
+    y, k = rest.rsplit("_s", 1)
+    return int(q[1:]), "" if y == "int8" else y, int(k)
+
+
+def measure_quant(args, M, torch, stream, base: WL.Workload):
+    """moe_dispatch of the main workload with every quantised variant: the
+    payload kernel alone (CUDA events the library records around it) and the
+    whole call. Two output sets alternate, so consecutive steps do not share
+    their written bytes in L2."""
+    res = {}
+    peaks = measured_peaks()
+    for tag in [t for t in args.quant_modes.split(",") if t]:
+        q, y, k = parse_quant_mode(tag)
+        wl = base.with_(quant_mode=q, y_dtype=y, scales_kind=k)
+        inp = WL.make_inputs(wl)
+        bf = wl.x_dtype == WL.X_BF16
+        tdt = torch.bfloat16 if bf else torch.float16
+
+        def dev(a, as_bf=False):
+            if a is None:
+                return None
+            t = torch.from_numpy(np.ascontiguousarray(a).view(np.int16) if as_bf else np.ascontiguousarray(a))
+            return (t.view(torch.bfloat16) if as_bf else t).cuda()
+
+        x, ids, esc, mask = dev(inp["x"], bf), dev(inp["expert_ids"]), dev(inp["expert_scales"]), \
+            dev(inp.get("active_mask"))
+        qs = dev(inp.get("quant_scales"))
+        cfg = M.config(wl.ep_world_size, wl.bs, wl.h, wl.topk, wl.moe_expert_num, tdt,
+                       zero_expert_num=wl.zero_expert_num, copy_expert_num=wl.copy_expert_num, quant_mode=q,
+                       mask_kind=wl.mask_kind, expand_dtype=y, scales_kind=k)
+        ws = M.alloc_workspace(cfg)
+        outs = [M.alloc_dispatch_outputs(cfg, tdt) for _ in range(2)]
+
+        def call(c, i):
+            o = outs[i & 1]
+            M.dispatch(c, x, ids, mask, esc, o["expand_x"], o["dynamic_scales"], o["assist_info"],
+                       o["ep_recv_count"], o["expand_scales"], None, ws, scales=qs)
+
+        for i in range(3):
+            call(cfg, i)
+        torch.cuda.synchronize()
+        n = max(3, args.quant_steps)
+        evs = [M.ProfEvents() for _ in range(n)]
+        cfgs = [e.attach(cfg) for e in evs]
+        a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        a.record(stream)
+        for i in range(n):
+            call(cfg, i)
+        b.record(stream)
+        for i, c in enumerate(cfgs):
+            call(c, i)
+        torch.cuda.synchronize()
+        st = M.get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {M.STATUS.get(st, st)} in quant variant {tag}")
+        acct = algorithmic_bytes(wl, inp)
+        call_ms = a.elapsed_time(b) / n
+        sc_ms = statistics.mean(e.elapsed_ms() for e in evs)
+        res[tag] = {"dispatch_ms": call_ms, "dispatch_GBps": acct["dispatch"] / (call_ms * 1e-3) / 1e9,
+                    "scatter_ms": sc_ms, "scatter_GBps": acct["scatter"] / (sc_ms * 1e-3) / 1e9,
+                    "scatter_frac_of_measured_hbm": acct["scatter"] / (sc_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+                    "scatter_bytes": acct["scatter"], "row_out_bytes": wl.row_out_bytes, "steps": n}
+        del ws, outs
+    return {"workload": base.name, "variants": res,
+            "note": "q2_int8_s0 is the per-token int8 kernel of the plain dispatch; the others run the quantising "
+                    "scatter (a variant per pick when s3 = per-expert scales)"}
+
+
 def run_ours(args):
     import torch
     import torch.distributed as dist
@@ -634,6 +715,7 @@ def run_ours(args):
 
     ffn = None if args.no_ffn or world > 1 else measure_ffn(args, M, torch, stream)
     small = None if world > 1 or not args.small_workloads else measure_small(args, M, torch, stream)
+    quant = None if world > 1 or not args.quant_modes else measure_quant(args, M, torch, stream, wl)
 
     # End to end through the C ABI with host buffers: every step copies its
     # inputs from pinned host memory (H2D stream), runs dispatch + combine
@@ -751,6 +833,7 @@ def run_ours(args):
         "two_phase_combine": two_phase,
         "ffn_variant": ffn,
         "small_workloads": small,
+        "quant_dispatch": quant,
         "gpu_launches": K * (4 if wl.quant_mode == 0 else 2),
         "clocks": clocks,
     }

@@ -142,13 +142,10 @@ struct FfnLaunch {
 
 // True when the TMA scatter's shared-memory ring fits for this shape.
 bool scatter_tma_fits(const Shape& sh);
-// The quantising scatter (quant modes 1, 3, 4 and smoothed 2) and its fit test.
+// The quantising scatter (every quant_mode but 0) and its fit test.
 bool scatter_quant_tma_fits(const Shape& sh);
 cudaError_t launch_scatter_quant(const ScatterParams& p, cudaStream_t st, int num_sms, bool tma);
-// Modes the quantising scatter handles (the plain per-token int8 path does the rest).
-inline bool uses_scatter_quant(const Shape& sh) {
-  return sh.quant == 1 || sh.quant == 3 || sh.quant == 4 || (sh.quant == 2 && sh.scales_kind != MOE_SCALES_NONE);
-}
+inline bool uses_scatter_quant(const Shape& sh) { return sh.quant != 0; }
 
 // Launchers (each returns the launch error, if any).
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st);

@@ -1,83 +1,26 @@
-// Dispatch payload: expandXOut = AllToAllV(X) (aclnnMoeDistributeDispatchV4,
-// 接口功能), with per-token dynamic int8 quantisation first for quantMode 2
-// (参数说明), and the two data planes of the combine_doubleplane README
-// (方案设计) applied to the dispatch direction: plain SM stores for local,
-// small or average segments, TMA bulk copies for large remote ones.
+// Dispatch payload without quantisation: expandXOut = AllToAllV(X)
+// (aclnnMoeDistributeDispatchV4, 接口功能), with the two data planes of the
+// combine_doubleplane README (方案设计) applied to the dispatch direction:
+// plain SM stores for local, small or average segments, TMA bulk copies for
+// large remote ones. (The quantised modes run in scatter_quant.cu.)
 //
 // Token-major and persistent: each CTA walks tokens blockIdx.x, +grid, ...
 // A ring of STAGES shared-memory slots is filled by TMA bulk loads
 // (cp.async.bulk global->shared, completion on an mbarrier), so every source
 // row is read from HBM exactly once however many ranks it goes to. For each
 // token, warp 0 builds the list of destination rows (rank d, row base + rank)
-// and writes assist_info / expand_scales / dynamic_scales; then
+// and writes assist_info / expand_scales; then
 //   * bulk-plane picks: one thread issues cp.async.bulk shared->global of the
 //     whole row (no multicast), one bulk group per token, at most STAGES groups
 //     in flight (the page's bounded backlog: quiet every 256 issues);
 //   * store-plane picks: all threads copy the row from shared memory with
 //     16-byte st.global.v4, coalesced.
-// quantMode 2: amax over the staged row (exact fp32 max), scale = amax / 127
-// (IEEE division), q = clamp(rint(x / scale), -127, 127) (IEEE division,
-// round half to even); the int8 row goes to a second shared slot that the
-// bulk plane reads after a generic->async proxy fence.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
 #include "scatter_common.cuh"
 
 namespace crs {
-
-// |x| max of 8 packed 16-bit floats.
-template <int DT>
-__device__ __forceinline__ float absmax8(int4 v) {
-  const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
-  float m = 0.f;
-#pragma unroll
-  for (int i = 0; i < 4; ++i) {
-    float a, b;
-    if (DT == MOE_F16) {
-      const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
-      a = __low2float(h2);
-      b = __high2float(h2);
-    } else {
-      const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-      a = __low2float(h2);
-      b = __high2float(h2);
-    }
-    m = fmaxf(m, fmaxf(fabsf(a), fabsf(b)));
-  }
-  return m;
-}
-
-__device__ __forceinline__ int quant1(float x, float scale) {
-  int q = __float2int_rn(__fdiv_rn(x, scale));
-  return max(-127, min(127, q));
-}
-
-// 8 packed 16-bit floats -> 8 int8 packed in a uint2.
-template <int DT>
-__device__ __forceinline__ uint2 quant8(int4 v, float scale, bool zero) {
-  const uint32_t w[4] = {(uint32_t)v.x, (uint32_t)v.y, (uint32_t)v.z, (uint32_t)v.w};
-  uint32_t out[2] = {0u, 0u};
-  if (!zero) {
-#pragma unroll
-    for (int i = 0; i < 4; ++i) {
-      float a, b;
-      if (DT == MOE_F16) {
-        const __half2 h2 = *reinterpret_cast<const __half2*>(&w[i]);
-        a = __low2float(h2);
-        b = __high2float(h2);
-      } else {
-        const __nv_bfloat162 h2 = *reinterpret_cast<const __nv_bfloat162*>(&w[i]);
-        a = __low2float(h2);
-        b = __high2float(h2);
-      }
-      const uint32_t qa = (uint32_t)(quant1(a, scale) & 0xff);
-      const uint32_t qb = (uint32_t)(quant1(b, scale) & 0xff);
-      out[i >> 1] |= (qa | (qb << 8)) << ((i & 1) * 16);
-    }
-  }
-  return make_uint2(out[0], out[1]);
-}
 
 // Ready flags, called by thread 0 right after the first barrier of token i:
 //   * token i-1's store-plane rows: every thread passed the barrier after
@@ -101,24 +44,21 @@ __device__ __forceinline__ void publish_earlier(const ScatterParams& p, const Pi
   }
 }
 
-// QUANT: 0 or 2; DT: element type for the quantiser (MOE_F16 / MOE_BF16).
-template <int QUANT, int DT, int STAGES>
+template <int STAGES>
 __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ PickTable tabs[3];
-  __shared__ float s_red[2][kScatterWarps];
   __shared__ int s_abort;
 
   const Shape sh = p.sh;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int n_tok = sh.W * sh.bs;
   const int G = gridDim.x;
   const int my_n = blockIdx.x < n_tok ? (n_tok - 1 - (int)blockIdx.x) / G + 1 : 0;
   const uint32_t row_in = (uint32_t)sh.row_in, row_out = (uint32_t)sh.row_out;
-  const size_t slot_in = align128(row_in), slot_out = align128(row_out);
+  const size_t slot_in = align128(row_in);
   uint8_t* xin = smem;                         // [STAGES][slot_in]
-  uint8_t* qbuf = smem + STAGES * slot_in;     // [STAGES][slot_out] (quant only)
   const uint8_t* x = static_cast<const uint8_t*>(p.x);
   uint8_t* out = static_cast<uint8_t*>(p.expand_x);
 
@@ -152,79 +92,29 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     bool ok = mbar_wait_bounded(&full_bar[stage], parity, p.status, p.timeout_ns);
     if (!ok) s_abort = 1;
 
-    if (QUANT == 2) {
-      // the int8 slot of this stage was last read by the bulk group of token
-      // i - STAGES: keep at most STAGES-1 newer groups outstanding
-      if (tid == 0) bulk_wait_read<STAGES - 1>();
-      float m = 0.f;
-      for (uint32_t v = tid; v < row_in / 16; v += kScatterThreads)
-        m = fmaxf(m, absmax8<DT>(*reinterpret_cast<const int4*>(row + v * 16)));
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) s_red[i & 1][warp] = m;
-      __syncthreads();
-      if (s_abort) break;
-      if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
-      if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
-      float amax = 0.f;
-#pragma unroll
-      for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[i & 1][w]);
-      const float scale = __fdiv_rn(amax, 127.0f);
-      const bool zero = amax == 0.f;
-      if (warp == 0) build_picks(p, tau, s, t, tab, true, scale);
-      uint8_t* q = qbuf + stage * slot_out;
-      // each thread turns 16 inputs (two 16-byte vectors) into one 16-byte int8 vector
-      for (uint32_t u = tid; u < row_out / 16; u += kScatterThreads) {
-        const int4 a = *reinterpret_cast<const int4*>(row + u * 32);
-        const int4 b = *reinterpret_cast<const int4*>(row + u * 32 + 16);
-        const uint2 qa = quant8<DT>(a, scale, zero), qb = quant8<DT>(b, scale, zero);
-        *reinterpret_cast<int4*>(q + u * 16) = make_int4((int)qa.x, (int)qa.y, (int)qb.x, (int)qb.y);
+    if (warp == 0) build_picks(p, tau, s, t, tab);
+    __syncthreads();
+    if (s_abort) break;
+    if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
+    if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
+    const int nb = tab.n_bulk, ns = tab.n_sm;
+    if (tid == 0) {
+      // refill the slot of the previous token once its bulk group has read it
+      const int nxt = i - 1 + STAGES;
+      if (i >= 1 && nxt < my_n) {
+        bulk_wait_read<0>();
+        const int ps = (i - 1) % STAGES;
+        const size_t tn = blockIdx.x + (size_t)nxt * G;
+        mbar_arrive_expect_tx(&full_bar[ps], row_in);
+        bulk_g2s(xin + ps * slot_in, x + tn * row_in, row_in, &full_bar[ps]);
       }
-      fence_proxy_async_smem();
-      __syncthreads();
-      const int nb = tab.n_bulk, ns = tab.n_sm;
-      if (tid == 0) {
-        for (int j = 0; j < nb; ++j) bulk_s2g(out + tab.bulk_dst[j] * row_out, q, row_out);
-        bulk_commit();
-        // refill the x slot of the previous token (read only by generic loads,
-        // all finished before the barrier above)
-        const int nxt = i - 1 + STAGES;
-        if (i >= 1 && nxt < my_n) {
-          const int ps = (i - 1) % STAGES;
-          const size_t tn = blockIdx.x + (size_t)nxt * G;
-          mbar_arrive_expect_tx(&full_bar[ps], row_in);
-          bulk_g2s(xin + ps * slot_in, x + tn * row_in, row_in, &full_bar[ps]);
-        }
-      }
-      for (uint32_t u = tid; u < row_out / 16; u += kScatterThreads) {
-        const int4 v = *reinterpret_cast<const int4*>(q + u * 16);
-        for (int j = 0; j < ns; ++j) st_v4(out + tab.sm_dst[j] * row_out + u * 16, v);
-      }
-    } else {
-      if (warp == 0) build_picks(p, tau, s, t, tab, false, 0.f);
-      __syncthreads();
-      if (s_abort) break;
-      if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
-      if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
-      const int nb = tab.n_bulk, ns = tab.n_sm;
-      if (tid == 0) {
-        // refill the slot of the previous token once its bulk group has read it
-        const int nxt = i - 1 + STAGES;
-        if (i >= 1 && nxt < my_n) {
-          bulk_wait_read<0>();
-          const int ps = (i - 1) % STAGES;
-          const size_t tn = blockIdx.x + (size_t)nxt * G;
-          mbar_arrive_expect_tx(&full_bar[ps], row_in);
-          bulk_g2s(xin + ps * slot_in, x + tn * row_in, row_in, &full_bar[ps]);
-        }
-        for (int j = 0; j < nb; ++j) bulk_s2g(out + tab.bulk_dst[j] * row_out, row, row_out);
-        bulk_commit();
-      }
-      if (ns > 0) {
-        for (uint32_t v = tid; v < row_in / 16; v += kScatterThreads) {
-          const int4 val = *reinterpret_cast<const int4*>(row + v * 16);
-          for (int j = 0; j < ns; ++j) st_v4(out + tab.sm_dst[j] * row_out + v * 16, val);
-        }
+      for (int j = 0; j < nb; ++j) bulk_s2g(out + tab.bulk_dst[j] * row_out, row, row_out);
+      bulk_commit();
+    }
+    if (ns > 0) {
+      for (uint32_t v = tid; v < row_in / 16; v += kScatterThreads) {
+        const int4 val = *reinterpret_cast<const int4*>(row + v * 16);
+        for (int j = 0; j < ns; ++j) st_v4(out + tab.sm_dst[j] * row_out + v * 16, val);
       }
     }
   }
@@ -257,10 +147,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
 
 // Fallback for rows that are not 16-byte multiples: element-wise copies, all
 // segments on the store plane.
-template <int QUANT>
 __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterParams p) {
   __shared__ PickTable tab;
-  __shared__ float s_red[kScatterWarps];
   const Shape sh = p.sh;
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   const int n_tok = sh.W * sh.bs;
@@ -269,24 +157,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
   if (p.perf && tid == 0) perf_begin(p);
   for (size_t tau = blockIdx.x; tau < (size_t)n_tok; tau += gridDim.x) {
     const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
-    float scale = 0.f, amax = 0.f;
-    if (QUANT == 2) {
-      const uint16_t* xr = static_cast<const uint16_t*>(p.x) + tau * sh.h;
-      float m = 0.f;
-      for (int j = tid; j < sh.h; j += kScatterThreads) {
-        const float v = sh.x_dtype == MOE_F16 ? __half2float(__ushort_as_half(xr[j]))
-                                              : __bfloat162float(__ushort_as_bfloat16(xr[j]));
-        m = fmaxf(m, fabsf(v));
-      }
-#pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) s_red[warp] = m;
-      __syncthreads();
-      for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
-      scale = __fdiv_rn(amax, 127.0f);
-    }
     if (warp == 0) {
-      build_picks(p, tau, s, t, tab, QUANT == 2, scale);
+      build_picks(p, tau, s, t, tab);
       __syncwarp();
       // both planes are carried by plain stores here
       if (lane == 0) {
@@ -300,16 +172,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
     }
     __syncthreads();
     const int ns = tab.n_sm;
-    if (QUANT == 2) {
-      const uint16_t* xr = static_cast<const uint16_t*>(p.x) + tau * sh.h;
-      int8_t* out = static_cast<int8_t*>(p.expand_x);
-      for (int j = tid; j < sh.h; j += kScatterThreads) {
-        const float v = sh.x_dtype == MOE_F16 ? __half2float(__ushort_as_half(xr[j]))
-                                              : __bfloat162float(__ushort_as_bfloat16(xr[j]));
-        const int8_t q = amax == 0.f ? (int8_t)0 : (int8_t)quant1(v, scale);
-        for (int k = 0; k < ns; ++k) out[tab.sm_dst[k] * sh.h + j] = q;
-      }
-    } else if (sh.es == 4) {
+    if (sh.es == 4) {
       const uint32_t* xr = static_cast<const uint32_t*>(p.x) + tau * sh.h;
       uint32_t* out = static_cast<uint32_t*>(p.expand_x);
       for (int j = tid; j < sh.h; j += kScatterThreads) {
@@ -355,9 +218,7 @@ static cudaError_t launch_persistent(KernelT kernel, const ScatterParams& p, cud
 
 // Shared-memory budget of the TMA scatter for `stages` slots.
 static size_t scatter_smem(const Shape& sh, int stages) {
-  size_t b = (size_t)stages * align128((size_t)sh.row_in);
-  if (sh.quant == 2) b += (size_t)stages * align128((size_t)sh.row_out);
-  return b;
+  return (size_t)stages * align128((size_t)sh.row_in);
 }
 
 bool scatter_tma_fits(const Shape& sh) { return scatter_smem(sh, 2) <= 200 * 1024; }
@@ -368,20 +229,12 @@ cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t st, int num_sms,
   if (!tma) {
     const int grid = max(1, min(sh.W * sh.bs, num_sms * 4));
     PdlLaunch L(dim3(grid), dim3(kScatterThreads), 0, st);
-    if (sh.quant == 2) return cudaLaunchKernelEx(&L.cfg, scatter_plain_kernel<2>, p);
-    return cudaLaunchKernelEx(&L.cfg, scatter_plain_kernel<0>, p);
+    return cudaLaunchKernelEx(&L.cfg, scatter_plain_kernel, p);
   }
   const bool four = scatter_smem(sh, 4) <= 110 * 1024;
   const size_t smem = scatter_smem(sh, four ? 4 : 2);
-  if (sh.quant == 2) {
-    if (sh.x_dtype == MOE_F16)
-      return four ? launch_persistent(scatter_tma_kernel<2, MOE_F16, 4>, p, st, num_sms, smem)
-                  : launch_persistent(scatter_tma_kernel<2, MOE_F16, 2>, p, st, num_sms, smem);
-    return four ? launch_persistent(scatter_tma_kernel<2, MOE_BF16, 4>, p, st, num_sms, smem)
-                : launch_persistent(scatter_tma_kernel<2, MOE_BF16, 2>, p, st, num_sms, smem);
-  }
-  return four ? launch_persistent(scatter_tma_kernel<0, MOE_F16, 4>, p, st, num_sms, smem)
-              : launch_persistent(scatter_tma_kernel<0, MOE_F16, 2>, p, st, num_sms, smem);
+  return four ? launch_persistent(scatter_tma_kernel<4>, p, st, num_sms, smem)
+              : launch_persistent(scatter_tma_kernel<2>, p, st, num_sms, smem);
 }
 
 }  // namespace crs

@@ -35,8 +35,7 @@ __device__ __forceinline__ void publish_row(const ScatterParams& p, int g) {
 
 // Builds the destination list of token `tau` (warp 0 only) and writes the
 // per-row metadata. Returns nothing; results land in `tab`.
-__device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, int s, int t, PickTable& tab,
-                                            bool write_dyn, float qscale) {
+__device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, int s, int t, PickTable& tab) {
   const Shape& sh = p.sh;
   const int lane = threadIdx.x & 31;
   long long dst = -1;
@@ -59,7 +58,6 @@ __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, 
         if (p.expand_scales)
           reinterpret_cast<uint32_t*>(p.expand_scales)[dst] =
               reinterpret_cast<const uint32_t*>(p.scales)[tau * sh.K + lane];
-        if (write_dyn) static_cast<float*>(p.dyn_scales)[dst] = qscale;
       } else {
         set_error(p.status, MOE_ERR_CAPACITY);
       }

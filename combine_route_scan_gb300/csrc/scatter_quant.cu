@@ -1,9 +1,10 @@
 // Dispatch payload for the quantised modes of aclnnMoeDistributeDispatchV4
 // (参数说明 quantMode / scalesOptional, 约束说明 quantMode相关约束) other than
-// the plain per-token int8 path of scatter.cu:
+// the unquantised copy of scatter.cu:
 //   quantMode 1   static int8: q = clamp(rne(x * s), -128, 127), s of shape
 //                 (1,), (h,) or (E, h) (the pick's expert's row);
-//   quantMode 2   per-token int8 after per-expert smoothing x' = x * s[e];
+//   quantMode 2   per-token int8, optionally after per-expert smoothing
+//                 x' = x * s[e]: scale = amax / 127, q = clamp(rne(x' / scale), -127, 127);
 //   quantMode 3   per-group FP8: groups of 128, scale_g = amax_g / FMAX,
 //                 q = fp8(x' / scale_g), optional smoothing as for 2;
 //   quantMode 4   MX (OCP Microscaling v1.0): blocks of 32 share the E8M0
@@ -194,7 +195,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
     // the buffer of this token's first variant was last read by the bulk
     // group two variants back: at most one newer group may still be reading
     if (tid == 0) bulk_wait_read<1>();
-    if (warp == 0) build_picks(p, tau, s, t, tab, false, 0.f);
+    if (warp == 0) build_picks(p, tau, s, t, tab);
     __syncthreads();
     if (s_abort) break;
     if (tid == 0 && i >= 1) {
@@ -247,11 +248,16 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
       } else if (MODE == 2) {
         float m = 0.f;
         for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-          float f[8], sc[8];
+          float f[8];
           unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-          load_scales8(srow, v, sc);
+          if (PE) {
+            float sc[8];
+            load_scales8(srow, v, sc);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(__fmul_rn(f[k], sc[k])));
+            for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
+          }
+#pragma unroll
+          for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
         }
 #pragma unroll
         for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
@@ -262,12 +268,17 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
         for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
         const float scale = __fdiv_rn(amax, 127.0f);
         for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-          float f[8], sc[8];
+          float f[8];
           unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-          load_scales8(srow, v, sc);
+          if (PE) {
+            float sc[8];
+            load_scales8(srow, v, sc);
+#pragma unroll
+            for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
+          }
           int qv[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) qv[k] = amax == 0.f ? 0 : token_q(__fmul_rn(f[k], sc[k]), scale);
+          for (int k = 0; k < 8; ++k) qv[k] = amax == 0.f ? 0 : token_q(f[k], scale);
           *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
         }
         if (tid == 0) reinterpret_cast<float*>(dq)[0] = scale;
@@ -384,7 +395,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_plain_kernel(Sc
   for (size_t tau = blockIdx.x; tau < (size_t)n_tok; tau += gridDim.x) {
     const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
     if (warp == 0) {
-      build_picks(p, tau, s, t, tab, false, 0.f);
+      build_picks(p, tau, s, t, tab);
       __syncwarp();
       if (lane == 0) {  // both planes are carried by plain stores here
         for (int j = 0; j < tab.n_bulk; ++j) {
@@ -520,7 +531,8 @@ static cudaError_t launch_quant_dt(const ScatterParams& p, cudaStream_t st, int 
       return pe ? launch_quant_persistent(scatter_quant_kernel<1, DT, MOE_Y_DEFAULT, true>, p, st, nsm)
                 : launch_quant_persistent(scatter_quant_kernel<1, DT, MOE_Y_DEFAULT, false>, p, st, nsm);
     case 2:
-      return launch_quant_persistent(scatter_quant_kernel<2, DT, MOE_Y_DEFAULT, true>, p, st, nsm);
+      return pe ? launch_quant_persistent(scatter_quant_kernel<2, DT, MOE_Y_DEFAULT, true>, p, st, nsm)
+                : launch_quant_persistent(scatter_quant_kernel<2, DT, MOE_Y_DEFAULT, false>, p, st, nsm);
     case 3:
       if (sh.ytype == MOE_Y_FP8_E4M3)
         return pe ? launch_quant_persistent(scatter_quant_kernel<3, DT, MOE_Y_FP8_E4M3, true>, p, st, nsm)
