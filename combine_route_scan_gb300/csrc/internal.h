@@ -122,6 +122,7 @@ struct CombineParams {
   int bulk_ok;
   int64_t bulk_min_bytes;
   int put_only;
+  int tp_rows;             // two-phase: rows per warp batch (1..32)
   uint64_t timeout_ns;
 };
 

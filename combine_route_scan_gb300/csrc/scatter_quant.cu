@@ -136,6 +136,105 @@ __device__ __forceinline__ void publish_token(const ScatterParams& p, const Pick
   for (int j = 0; j < a.n_bulk; ++j) publish_row(p, a.bulk_seg[j]);
 }
 
+// Per-expert scales, store-plane picks: every pick's row is different, so
+// each is quantised straight from the staged source row into its destination
+// (8-byte stores from registers, coalesced across the warp), with no shared
+// buffer and no barrier per pick; per-token int8 needs one barrier for all
+// picks' row maxima together.
+template <int MODE, int DT, int YT>
+__device__ __forceinline__ void quant_store_picks(const ScatterParams& p, const PickTable& tab, const uint8_t* row,
+                                                  uint8_t* out, uint32_t nvec, float (*s_pm)[kScatterWarps]) {
+  const Shape& sh = p.sh;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const uint32_t row_out = (uint32_t)sh.row_out;
+  const int n = tab.n_sm;
+  if (MODE == 2) {
+    for (int j = 0; j < n; ++j) {
+      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
+      float m = 0.f;
+      for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+        float f[8], sc[8];
+        unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+        load_scales8(srow, v, sc);
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(__fmul_rn(f[k], sc[k])));
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (lane == 0) s_pm[j][warp] = m;
+    }
+    __syncthreads();
+    for (int j = 0; j < n; ++j) {
+      float amax = 0.f;
+#pragma unroll
+      for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_pm[j][w]);
+      const float scale = __fdiv_rn(amax, 127.0f);
+      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
+      uint8_t* dst = out + tab.sm_dst[j] * row_out;
+      for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+        float f[8], sc[8];
+        unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+        load_scales8(srow, v, sc);
+        int qv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qv[k] = amax == 0.f ? 0 : token_q(__fmul_rn(f[k], sc[k]), scale);
+        *reinterpret_cast<uint2*>(dst + v * 8) = pack8(qv);
+      }
+      if (tid == 0) static_cast<float*>(p.dyn_scales)[tab.sm_dst[j]] = scale;
+    }
+  } else if (MODE == 1) {
+    for (int j = 0; j < n; ++j) {
+      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
+      uint8_t* dst = out + tab.sm_dst[j] * row_out;
+      for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+        float f[8], sc[8];
+        unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+        load_scales8(srow, v, sc);
+        int qv[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) qv[k] = static_q(__fmul_rn(f[k], sc[k]));
+        *reinterpret_cast<uint2*>(dst + v * 8) = pack8(qv);
+      }
+    }
+  } else {  // MODE 3: groups of 16 vectors, 16 lanes
+    const int nd = sh.ngroups;
+    for (int j = 0; j < n; ++j) {
+      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
+      uint8_t* dst = out + tab.sm_dst[j] * row_out;
+      float* dyn = static_cast<float*>(p.dyn_scales) + tab.sm_dst[j] * nd;
+      for (uint32_t base = 0; base < nvec; base += kScatterThreads) {
+        const uint32_t v = base + tid;
+        const bool valid = v < nvec;
+        float f[8];
+        if (valid) {
+          float sc[8];
+          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+          load_scales8(srow, v, sc);
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
+        } else {
+#pragma unroll
+          for (int k = 0; k < 8; ++k) f[k] = 0.f;
+        }
+        float m = 0.f;
+#pragma unroll
+        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+        const float scale = __fdiv_rn(m, fp8_max(YT));
+        if (valid) {
+          uint32_t c[4];
+#pragma unroll
+          for (int k = 0; k < 4; ++k)
+            c[k] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(f[2 * k], scale), __fdiv_rn(f[2 * k + 1], scale));
+          *reinterpret_cast<uint2*>(dst + v * 8) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+          if ((v & 15u) == 0) dyn[v >> 4] = scale;
+        }
+      }
+    }
+  }
+}
+
 // MODE: quantMode (1..4); DT: MOE_F16 / MOE_BF16; YT: MOE_Y_* of the output;
 // PE: per-expert scales (a variant per pick).
 template <int MODE, int DT, int YT, bool PE>
@@ -144,6 +243,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
   __shared__ __align__(8) uint64_t full_bar[kQStages];
   __shared__ PickTable tabs[2];
   __shared__ float s_red[kScatterWarps];
+  __shared__ float s_pm[PE && MODE == 2 ? kMaxK : 1][kScatterWarps];
   __shared__ int s_abort;
 
   const Shape sh = p.sh;
@@ -212,13 +312,17 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
       }
     }
     const int nsm = tab.n_sm, nbk = tab.n_bulk;
-    const int nvar = PE ? nsm + nbk : (nsm + nbk > 0 ? 1 : 0);
-    for (int j = 0; j < nvar; ++j) {
+    // per-expert scales: store-plane picks straight to their rows; then one
+    // variant per bulk-plane pick. Otherwise one variant for all picks.
+    if (PE && nsm > 0) quant_store_picks<MODE, DT, YT>(p, tab, row, out, nvec, s_pm);
+    const int j0 = PE ? nsm : 0;
+    const int j1 = PE ? nsm + nbk : (nsm + nbk > 0 ? 1 : 0);
+    for (int j = j0; j < j1; ++j) {
       const int qs = nv & 1;
       ++nv;
       uint8_t* q = qbuf + qs * slot_out;
       uint8_t* dq = dbuf + qs * slot_dyn;
-      if (PE && j > 0) {
+      if (PE && j > j0) {
         if (tid == 0) bulk_wait_read<1>();
         __syncthreads();
       }

@@ -3,7 +3,9 @@
 //
 // Phase 1 (put, the page's comm_only): every expert-output row of rank d goes
 // back to its source's combine window, slot (s, t, k) = what assist_info
-// names, and the slot's ready flag is set to the call's epoch:
+// names, and the slot's ready flag is set to the call's epoch. Warps take
+// batches of R consecutive rows of one rank (R = 32, one per lane, or fewer
+// for small calls, so that all warps have rows to move):
 //   * store plane: the warp copies the row with 16-byte loads / stores, then
 //     fences and release-stores the flags of its rows;
 //   * bulk plane (segments the page's rule picks, writer = rank d): lane 0
@@ -106,13 +108,14 @@ __global__ void __launch_bounds__(kTpThreads, 1) two_phase_kernel(CombineParams 
     mbar_init(&bars[warp][1], 1);
     mbar_fence_init();
   }
-  // per rank: rows received from other ranks, and the number of 32-row batches
+  // per rank: rows received from other ranks, and the number of R-row batches
+  const int R = p.tp_rows;
   for (int d = tid; d < W; d += kTpThreads) {
     long long own = 0;
     for (int le = 0; le < sh.L; ++le) own += seg_rows(p.ep_recv_count, d, LW, le * W + d);
     const long long cnt = p.ep_recv_count[(size_t)d * LW + LW - 1];
     remote[d] = cnt - own;
-    bprefix[d + 1] = (int)((cnt + 31) / 32);
+    bprefix[d + 1] = (int)((cnt + R - 1) / R);
   }
   __syncthreads();
   if (tid == 0) {
@@ -149,10 +152,10 @@ __global__ void __launch_bounds__(kTpThreads, 1) two_phase_kernel(CombineParams 
     }
     const int d = lo;
     const long long cnt = p.ep_recv_count[(size_t)d * LW + LW - 1];
-    const long long r = (long long)(b - bprefix[d]) * 32 + lane;
+    const long long r = (long long)(b - bprefix[d]) * R + lane;
     long long q = -1;  // window slot of this lane's row
     int bulk = 0;
-    if (r < cnt) {
+    if (lane < R && r < cnt) {
       const long long fr = (long long)d * sh.A + r;
       const int s = p.assist[fr * 3 + 0], t = p.assist[fr * 3 + 1], k = p.assist[fr * 3 + 2];
       if (s >= 0 && s < W && t >= 0 && t < sh.bs && k >= 0 && k < sh.K) {
@@ -171,7 +174,7 @@ __global__ void __launch_bounds__(kTpThreads, 1) two_phase_kernel(CombineParams 
     }
     const uint32_t m_sm = __ballot_sync(0xffffffffu, q >= 0 && !bulk);
     const uint32_t m_bk = __ballot_sync(0xffffffffu, q >= 0 && bulk);
-    const long long row0 = (long long)d * sh.A + (long long)(b - bprefix[d]) * 32;
+    const long long row0 = (long long)d * sh.A + (long long)(b - bprefix[d]) * R;
 
     // store plane: the whole warp copies each row
     for (uint32_t m = m_sm; m; m &= m - 1) {
@@ -341,6 +344,13 @@ cudaError_t launch_combine_two_phase(const CombineParams& p, cudaStream_t st, in
   e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTpThreads, smem);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // rows per warp batch: up to 32 (one per lane), fewer when the call has
+  // fewer picks than 32 per warp, so that every warp gets rows to move
+  CombineParams q = p;
+  const long long picks = (long long)sh.W * sh.bs * sh.K;
+  const long long warps = (long long)num_sms * per_sm * kTpWarps;
+  q.tp_rows = 32;
+  while (q.tp_rows > 1 && picks < (long long)q.tp_rows * warps) q.tp_rows >>= 1;
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(num_sms * per_sm);
   cfg.blockDim = dim3(kTpThreads);
@@ -351,7 +361,7 @@ cudaError_t launch_combine_two_phase(const CombineParams& p, cudaStream_t st, in
   attr[0].val.cooperative = 1;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  return cudaLaunchKernelEx(&cfg, kern, p);
+  return cudaLaunchKernelEx(&cfg, kern, q);
 }
 
 }  // namespace crs
