@@ -67,6 +67,8 @@ def parse_args():
     ap.add_argument("--quant-modes", default=",".join(QUANT_MODES),
                     help="quantised dispatch variants timed on the main workload (mode/type/scales)")
     ap.add_argument("--quant-steps", type=int, default=50)
+    ap.add_argument("--only-quant", action="store_true",
+                    help="time only the quantised dispatch variants (for profiling); prints their JSON")
     return ap.parse_args()
 
 
@@ -558,6 +560,9 @@ def run_ours(args):
     from combine_route_scan_gb300 import moe as M
 
     wl = WL.WORKLOADS[args.workload]
+    if args.only_quant:
+        print(json.dumps(measure_quant(args, M, torch, torch.cuda.current_stream(), wl)))
+        return 0
     inp = WL.make_inputs(wl, seed=rank_seed(wl, rank))
     acct = algorithmic_bytes(wl, inp)
     step_bytes = acct["dispatch"] + acct["combine"]

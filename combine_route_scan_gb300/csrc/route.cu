@@ -23,10 +23,14 @@
 //
 // The per-rank scan of the W*L*W segment counts into ep_recv_count (inclusive)
 // and segment offsets (exclusive) then takes one of two forms:
-//   * W <= 16: the W CTAs run as one thread-block cluster. After a cluster
-//     barrier, CTA d reads the counts of segment (le, s) of rank d straight from
-//     CTA s's shared memory (distributed shared memory) and scans rank d's L*W
-//     segments itself: all ranks in parallel, no global fence, no atomic.
+//   * W <= 16: the W CTAs run as one thread-block cluster. Each thread arrives
+//     at a split cluster barrier (release) as soon as its totals are in shared
+//     memory, does its global stores, then waits; CTA d then reads the counts
+//     of segment (le, s) of rank d once from CTA s's shared memory
+//     (distributed shared memory), arrives at a second barrier that only
+//     guards those reads, and scans rank d's L*W segments: all ranks in
+//     parallel, no global fence, no atomic. The second wait sits at the very
+//     end, so no CTA exits while another may still read its counts.
 //   * otherwise: the last CTA to finish (completion counter in the workspace)
 //     scans all counts, tile by tile through shared memory.
 #include <cooperative_groups.h>
@@ -40,6 +44,18 @@ namespace crs {
 constexpr int kRouteThreadsMax = 1024;
 constexpr int kScanTile = 4096;
 constexpr int kRegIters = 4;  // warp iterations whose keys walk 1 keeps in registers
+
+// Split cluster barrier: arrive (release: this thread's earlier writes become
+// visible to the cluster; relaxed: no ordering) and wait (acquire).
+__device__ __forceinline__ void cluster_arrive_release() {
+  asm volatile("barrier.cluster.arrive.release.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_arrive_relaxed() {
+  asm volatile("barrier.cluster.arrive.relaxed.aligned;" ::: "memory");
+}
+__device__ __forceinline__ void cluster_wait_acquire() {
+  asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
+}
 
 // THREADS: 256 for sources with at most 1024 picks (every warp then has at most
 // kRegIters iterations and barriers are short), else 1024.
@@ -158,14 +174,12 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
       run += c;
     }
     tot[e] = run;
-    const size_t g = (size_t)e * sh.W + s;
-    p.cnt[g] = run;
-    if (p.seg_ready) {  // ready flags: count this call's rows from zero; empty segments are ready now
-      p.landed[g] = 0u;
-      if (run == 0) st_release_gpu(p.seg_ready + g, p.ticket);
-    }
     if (e / sh.L != s) remote += run;
   }
+  // cluster form: this thread's totals are released to the other CTAs now; the
+  // global stores below come after the arrive, so the barrier does not wait
+  // for them
+  if constexpr (CLUSTER) cluster_arrive_release();
   {
     const long long ex = block_exclusive_scan(remote, s_scan);
     if (tid == kRouteThreads - 1) s_total = ex + remote;
@@ -173,14 +187,20 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     remote = s_total;
   }
 
-  // plane of each segment sent by s (the page's rule with s as the writer):
-  // bulk iff remote, non-empty, >= bulk_min_bytes and above the mean remote
-  // segment; rows*den > remote is the page's cross multiply with the row size
-  // divided out of both sides.
+  // counts and plane of each segment sent by s (the page's rule with s as the
+  // writer): bulk iff remote, non-empty, >= bulk_min_bytes and above the mean
+  // remote segment; rows*den > remote is the page's cross multiply with the
+  // row size divided out of both sides.
   const long long den = (long long)(sh.W - 1 > 1 ? sh.W - 1 : 1) * sh.L;
   for (int e = tid; e < E; e += kRouteThreads) {
     const int d = e / sh.L;
     const long long rows = tot[e];
+    const size_t g = (size_t)e * sh.W + s;
+    p.cnt[g] = (int32_t)rows;
+    if (p.seg_ready) {  // ready flags: count this call's rows from zero; empty segments are ready now
+      p.landed[g] = 0u;
+      if (rows == 0) st_release_gpu(p.seg_ready + g, p.ticket);
+    }
     int use = 0;
     if (p.bulk_ok && d != s && rows > 0) {
       if (p.plane_policy == MOE_PLANE_BULK_ALL) {
@@ -189,36 +209,49 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
         use = rows * sh.row_out >= p.bulk_min_bytes && rows * den > remote;
       }
     }
-    const size_t g = (size_t)e * sh.W + s;
     p.plane[g] = (uint8_t)use;
     if (p.seg_plane_out) p.seg_plane_out[g] = (uint8_t)use;
   }
-  __syncthreads();
 
   if constexpr (CLUSTER) {
-    // every CTA's totals are final once the cluster barrier passes; CTA s now
-    // scans the L*W segments (le, s') of receiving rank d = s (L*W = E <= 1024)
+    // every CTA's totals are visible once the wait passes; CTA s then scans
+    // the L*W segments (le, s') of receiving rank d = s (L*W = E <= 1024),
+    // reading each count once from CTA s''s shared memory
+    cluster_wait_acquire();
     cg::cluster_group cluster = cg::this_cluster();
-    cluster.sync();
     const int d = s, LW = sh.L * sh.W;
-    // thread tid owns the contiguous segments [j0, j1) of rank d
+    constexpr int kPer = (kRouteThreadsMax + kRouteThreads - 1) / kRouteThreads;
+    // thread tid owns the contiguous segments [j0, j1) of rank d (at most kPer)
     const int per = (LW + kRouteThreads - 1) / kRouteThreads;
     const int j0 = min(LW, tid * per), j1 = min(LW, j0 + per);
-    auto seg_count = [&](int j) -> long long {
-      const int le = j / sh.W, sp = j - le * sh.W;
-      return cluster.map_shared_rank(tot, sp)[d * sh.L + le];
-    };
+    long long cv[kPer];
     long long local = 0;
-    for (int j = j0; j < j1; ++j) local += seg_count(j);
-    long long run = block_exclusive_scan(local, s_scan);
-    for (int j = j0; j < j1; ++j) {
-      const long long c = seg_count(j);
-      const size_t g = (size_t)d * LW + j;
-      p.base[g] = (int32_t)run;
-      p.ep_recv_count[g] = (int32_t)(run + c);
-      run += c;
-      if (j == LW - 1 && run > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int j = j0 + q;
+      cv[q] = 0;
+      if (j < j1) {
+        const int le = j / sh.W, sp = j - le * sh.W;
+        cv[q] = cluster.map_shared_rank(tot, sp)[d * sh.L + le];
+      }
+      local += cv[q];
     }
+    // done reading other CTAs' memory; the matching wait is at the very end
+    cluster_arrive_relaxed();
+    long long run = block_exclusive_scan(local, s_scan);
+#pragma unroll
+    for (int q = 0; q < kPer; ++q) {
+      const int j = j0 + q;
+      if (j < j1) {
+        const size_t g = (size_t)d * LW + j;
+        p.base[g] = (int32_t)run;
+        p.ep_recv_count[g] = (int32_t)(run + cv[q]);
+        run += cv[q];
+        if (j == LW - 1 && run > sh.A) set_error(p.status, MOE_ERR_CAPACITY);
+      }
+    }
+  } else {
+    __syncthreads();
   }
 
   // walk 2: position of every routed pick inside its segment
@@ -245,7 +278,7 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   }
 
   if constexpr (CLUSTER) {
-    cg::this_cluster().sync();  // no CTA leaves while others may read its counts
+    cluster_wait_acquire();  // no CTA leaves while others may still read its counts
     return;
   }
 
