@@ -184,8 +184,10 @@ __device__ __forceinline__ void reduce_vector(const uint8_t* const* src, const u
   }
 }
 
+// At most 64 registers a thread: four CTAs (32 warps) per SM keep enough
+// loads in flight to cover HBM latency.
 template <int DT>
-__global__ void __launch_bounds__(kReduceThreads) combine_reduce_kernel(CombineParams p, int chunks, int vpl) {
+__global__ void __launch_bounds__(kReduceThreads, 4) combine_reduce_kernel(CombineParams p, int chunks, int vpl) {
   __shared__ const uint8_t* s_src[kReduceThreads / 32][32];
   __shared__ uint32_t s_w[kReduceThreads / 32][32];
   const Shape sh = p.sh;
@@ -310,7 +312,9 @@ cudaError_t launch_combine_reduce(const CombineParams& p, cudaStream_t st, int n
     return cudaLaunchKernelEx(&L.cfg, combine_reduce_plain_kernel<MOE_BF16>, p);
   }
   const int nvec = sh.row_in / 16;
-  const int vpl = kReduceVpl;
+  // smaller work items when the batch is too small to give every SM ~16 warps
+  int vpl = kReduceVpl;
+  while (vpl > 1 && n_tok * ((nvec + 32 * vpl - 1) / (32 * vpl)) < (long long)num_sms * 16) vpl >>= 1;
   const int chunks = (nvec + 32 * vpl - 1) / (32 * vpl);
   const long long items = n_tok * chunks;
   const long long grid = (items + kReduceThreads / 32 - 1) / (kReduceThreads / 32);
