@@ -15,12 +15,14 @@
 //
 // Same skeleton as the plain dispatch: persistent token-major CTAs, the source
 // row staged in shared memory by a TMA bulk load, warp 0 building the
-// destination list. The quantised row ("variant") is written to one of two
-// shared buffers and leaves by TMA bulk copies (bulk-plane segments) or
-// 16-byte stores (store-plane segments). A variant is computed once per token,
-// or once per pick when the per-expert scales make every pick's row different.
-// Each thread quantises 16-byte vectors of 8 elements; a 128-element group is
-// 16 neighbouring lanes and a 32-element MX block 4, reduced with shuffles.
+// destination list. A quantised row ("variant") is computed once per token,
+// or once per pick when per-expert scales make every pick's row different.
+// When no pick of it goes by bulk copies, each thread stores its codes straight
+// from registers to every destination; otherwise the variant is written to one
+// of two shared buffers and leaves by TMA bulk copies (bulk-plane segments)
+// and 16-byte stores (store-plane segments). Each thread quantises 16-byte
+// vectors of 8 elements; a 128-element group is 16 neighbouring lanes and a
+// 32-element MX block 4, reduced with shuffles.
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
@@ -136,99 +138,153 @@ __device__ __forceinline__ void publish_token(const ScatterParams& p, const Pick
   for (int j = 0; j < a.n_bulk; ++j) publish_row(p, a.bulk_seg[j]);
 }
 
-// Per-expert scales, store-plane picks: every pick's row is different, so
-// each is quantised straight from the staged source row into its destination
-// (8-byte stores from registers, coalesced across the warp), with no shared
-// buffer and no barrier per pick; per-token int8 needs one barrier for all
-// picks' row maxima together.
-template <int MODE, int DT, int YT>
-__device__ __forceinline__ void quant_store_picks(const ScatterParams& p, const PickTable& tab, const uint8_t* row,
-                                                  uint8_t* out, uint32_t nvec, float (*s_pm)[kScatterWarps]) {
-  const Shape& sh = p.sh;
+// Where a quantised row goes: the shared buffers q (codes) and dq (dynamic
+// scales) that bulk copies and 16-byte stores read afterwards, or
+// straight from registers to the global destination rows dst[0..n), 8-byte
+// stores (4 for FP4) coalesced across the warp.
+struct RowSink {
+  uint8_t* q;
+  uint8_t* dq;
+  const long long* dst;
+  int n;
+  uint8_t* out;
+  uint8_t* dyn;
+  uint32_t row_out;
+  int nd;
+};
+
+// SINK: kShared (the shared buffers), kOne (the single destination dst[0]),
+// kMany (destinations dst[0..n)).
+enum { kShared = 0, kOne = 1, kMany = 2 };
+
+template <int SINK, typename V>
+__device__ __forceinline__ void put(const RowSink& k, uint32_t off, V v) {
+  if (SINK == kShared) {
+    *reinterpret_cast<V*>(k.q + off) = v;
+  } else if (SINK == kOne) {
+    *reinterpret_cast<V*>(k.out + k.dst[0] * k.row_out + off) = v;
+  } else {
+    for (int b = 0; b < k.n; ++b) *reinterpret_cast<V*>(k.out + k.dst[b] * k.row_out + off) = v;
+  }
+}
+template <int SINK, typename T>
+__device__ __forceinline__ void put_dyn(const RowSink& k, int g, T v) {
+  if (SINK == kShared) {
+    reinterpret_cast<T*>(k.dq)[g] = v;
+  } else if (SINK == kOne) {
+    reinterpret_cast<T*>(k.dyn)[k.dst[0] * k.nd + g] = v;
+  } else {
+    for (int b = 0; b < k.n; ++b) reinterpret_cast<T*>(k.dyn)[k.dst[b] * k.nd + g] = v;
+  }
+}
+
+// Quantises the staged row (elements times srow, or s0 for a (1,) coefficient)
+// into the sink. Every thread of the CTA calls it (per-token int8 reduces the
+// row maximum through s_red with one barrier).
+template <int MODE, int DT, int YT, int SINK>
+__device__ __forceinline__ void quantize_variant(const uint8_t* row, const float* srow, float s0, const RowSink& k,
+                                                 uint32_t nvec, float* s_red) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
-  const uint32_t row_out = (uint32_t)sh.row_out;
-  const int n = tab.n_sm;
-  if (MODE == 2) {
-    for (int j = 0; j < n; ++j) {
-      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
-      float m = 0.f;
-      for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-        float f[8], sc[8];
-        unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+  if (MODE == 1) {
+    for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+      float f[8], sc[8];
+      unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+      if (srow) {
+        load_scales8(srow, v, sc);
+      } else {
+#pragma unroll
+        for (int i = 0; i < 8; ++i) sc[i] = s0;
+      }
+      int qv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) qv[i] = static_q(__fmul_rn(f[i], sc[i]));
+      put<SINK>(k, v * 8, pack8(qv));
+    }
+  } else if (MODE == 2) {
+    float m = 0.f;
+    for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+      float f[8];
+      unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+      if (srow) {
+        float sc[8];
         load_scales8(srow, v, sc);
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(__fmul_rn(f[k], sc[k])));
+        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
       }
 #pragma unroll
-      for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-      if (lane == 0) s_pm[j][warp] = m;
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
     }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (lane == 0) s_red[warp] = m;
     __syncthreads();
-    for (int j = 0; j < n; ++j) {
-      float amax = 0.f;
+    float amax = 0.f;
 #pragma unroll
-      for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_pm[j][w]);
-      const float scale = __fdiv_rn(amax, 127.0f);
-      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
-      uint8_t* dst = out + tab.sm_dst[j] * row_out;
-      for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-        float f[8], sc[8];
-        unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+    for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
+    const float scale = __fdiv_rn(amax, 127.0f);
+    for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+      float f[8];
+      unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+      if (srow) {
+        float sc[8];
         load_scales8(srow, v, sc);
-        int qv[8];
 #pragma unroll
-        for (int k = 0; k < 8; ++k) qv[k] = amax == 0.f ? 0 : token_q(__fmul_rn(f[k], sc[k]), scale);
-        *reinterpret_cast<uint2*>(dst + v * 8) = pack8(qv);
+        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
       }
-      if (tid == 0) static_cast<float*>(p.dyn_scales)[tab.sm_dst[j]] = scale;
+      int qv[8];
+#pragma unroll
+      for (int i = 0; i < 8; ++i) qv[i] = amax == 0.f ? 0 : token_q(f[i], scale);
+      put<SINK>(k, v * 8, pack8(qv));
     }
-  } else if (MODE == 1) {
-    for (int j = 0; j < n; ++j) {
-      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
-      uint8_t* dst = out + tab.sm_dst[j] * row_out;
-      for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-        float f[8], sc[8];
+    if (tid == 0) put_dyn<SINK, float>(k, 0, scale);
+  } else {
+    // a group (mode 3: 16 vectors) or block (mode 4: 4 vectors) is a run of
+    // neighbouring lanes; every lane of a warp takes part in the shuffles,
+    // past-the-end lanes with zeros
+    constexpr int kLanes = MODE == 3 ? 16 : 4;
+    for (uint32_t base = 0; base < nvec; base += kScatterThreads) {
+      const uint32_t v = base + tid;
+      const bool valid = v < nvec;
+      float f[8];
+      if (valid) {
         unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-        load_scales8(srow, v, sc);
-        int qv[8];
-#pragma unroll
-        for (int k = 0; k < 8; ++k) qv[k] = static_q(__fmul_rn(f[k], sc[k]));
-        *reinterpret_cast<uint2*>(dst + v * 8) = pack8(qv);
-      }
-    }
-  } else {  // MODE 3: groups of 16 vectors, 16 lanes
-    const int nd = sh.ngroups;
-    for (int j = 0; j < n; ++j) {
-      const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
-      uint8_t* dst = out + tab.sm_dst[j] * row_out;
-      float* dyn = static_cast<float*>(p.dyn_scales) + tab.sm_dst[j] * nd;
-      for (uint32_t base = 0; base < nvec; base += kScatterThreads) {
-        const uint32_t v = base + tid;
-        const bool valid = v < nvec;
-        float f[8];
-        if (valid) {
+        if (srow) {
           float sc[8];
-          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
           load_scales8(srow, v, sc);
 #pragma unroll
-          for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
-        } else {
-#pragma unroll
-          for (int k = 0; k < 8; ++k) f[k] = 0.f;
+          for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
         }
-        float m = 0.f;
+      } else {
 #pragma unroll
-        for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
+        for (int i = 0; i < 8; ++i) f[i] = 0.f;
+      }
+      float m = 0.f;
 #pragma unroll
-        for (int o = 8; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+#pragma unroll
+      for (int o = kLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+      if (MODE == 3) {
         const float scale = __fdiv_rn(m, fp8_max(YT));
         if (valid) {
           uint32_t c[4];
 #pragma unroll
-          for (int k = 0; k < 4; ++k)
-            c[k] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(f[2 * k], scale), __fdiv_rn(f[2 * k + 1], scale));
-          *reinterpret_cast<uint2*>(dst + v * 8) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-          if ((v & 15u) == 0) dyn[v >> 4] = scale;
+          for (int i = 0; i < 4; ++i)
+            c[i] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(f[2 * i], scale), __fdiv_rn(f[2 * i + 1], scale));
+          put<SINK>(k, v * 8, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+          if ((v & 15u) == 0) put_dyn<SINK, float>(k, (int)(v >> 4), scale);
+        }
+      } else {
+        const int se = mx_exponent(m, elem_emax(YT));
+        const float inv = exp2_exact(-se);
+        if (valid) {
+          uint32_t c[4];
+#pragma unroll
+          for (int i = 0; i < 4; ++i) c[i] = cvt_y_pair(YT, __fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
+          if (YT == MOE_Y_FP4_E2M1)
+            put<SINK>(k, v * 4, c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24));
+          else
+            put<SINK>(k, v * 8, make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16)));
+          if ((v & 3u) == 0) put_dyn<SINK, uint8_t>(k, (int)(v >> 2), (uint8_t)(se + 127));
         }
       }
     }
@@ -236,18 +292,17 @@ __device__ __forceinline__ void quant_store_picks(const ScatterParams& p, const 
 }
 
 // MODE: quantMode (1..4); DT: MOE_F16 / MOE_BF16; YT: MOE_Y_* of the output;
-// PE: per-expert scales (a variant per pick).
+// PE: per-expert scales (every pick's row is different).
 template <int MODE, int DT, int YT, bool PE>
 __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kQStages];
   __shared__ PickTable tabs[2];
-  __shared__ float s_red[kScatterWarps];
-  __shared__ float s_pm[PE && MODE == 2 ? kMaxK : 1][kScatterWarps];
+  __shared__ float s_red[2][kScatterWarps];  // alternate by variant: a fast warp never overwrites a maximum still read
   __shared__ int s_abort;
 
   const Shape sh = p.sh;
-  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int tid = threadIdx.x, warp = tid >> 5;
   const int n_tok = sh.W * sh.bs;
   const int G = gridDim.x;
   const int my_n = blockIdx.x < n_tok ? (n_tok - 1 - (int)blockIdx.x) / G + 1 : 0;
@@ -259,10 +314,12 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
   uint8_t* dbuf = qbuf + kQSlots * slot_out;
   const uint8_t* x = static_cast<const uint8_t*>(p.x);
   uint8_t* out = static_cast<uint8_t*>(p.expand_x);
+  uint8_t* dyn = static_cast<uint8_t*>(p.dyn_scales);
   const uint32_t nvec = (uint32_t)sh.h / 8;
+  const int nd = sh.ngroups;
   const int dyn_es = MODE == 4 ? 1 : 4;  // bytes of one dynamic-scale entry
   const float s0 = (MODE == 1 && sh.scales_kind == MOE_SCALES_SCALAR) ? __ldg(p.qscales) : 1.f;
-  const bool channel = MODE == 1 && sh.scales_kind == MOE_SCALES_CHANNEL;
+  const float* chan = (MODE == 1 && sh.scales_kind == MOE_SCALES_CHANNEL) ? p.qscales : nullptr;
 
   if (tid == 0) {
     for (int i = 0; i < kQStages; ++i) mbar_init(&full_bar[i], 1);
@@ -281,7 +338,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
   pdl_launch_dependents();
   if (p.perf && tid == 0) perf_begin(p);
 
-  int nv = 0;  // variants so far: selects the quantised-row buffer
+  int nv = 0;   // variants through the shared buffers so far (selects the buffer)
+  int nvr = 0;  // variants so far (selects the s_red half)
   for (int i = 0; i < my_n; ++i) {
     const size_t tau = blockIdx.x + (size_t)i * G;
     const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
@@ -292,8 +350,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
 
     const bool ok = mbar_wait_bounded(&full_bar[stage], parity, p.status, p.timeout_ns);
     if (!ok) s_abort = 1;
-    // the buffer of this token's first variant was last read by the bulk
-    // group two variants back: at most one newer group may still be reading
+    // the buffer of this token's first shared variant was last read by the
+    // bulk group two variants back: at most one newer group may still read
     if (tid == 0) bulk_wait_read<1>();
     if (warp == 0) build_picks(p, tau, s, t, tab);
     __syncthreads();
@@ -312,155 +370,62 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
       }
     }
     const int nsm = tab.n_sm, nbk = tab.n_bulk;
-    // per-expert scales: store-plane picks straight to their rows; then one
-    // variant per bulk-plane pick. Otherwise one variant for all picks.
-    if (PE && nsm > 0) quant_store_picks<MODE, DT, YT>(p, tab, row, out, nvec, s_pm);
+    // measured on GB300: FP4 rows (4-byte codes a thread) and per-group rows
+    // (a scale per 128 elements and destination) leave faster through the
+    // shared buffer as 16-byte stores and coalesced scale rows
+    const bool direct = nbk == 0 && YT != MOE_Y_FP4_E2M1 && MODE != 3;
+
+    // store-plane picks straight from registers: each pick on its own with
+    // per-expert scales, else one pass for all of them when the token has no
+    // bulk-plane pick (no shared buffer, no barrier)
+    if (PE) {
+      for (int j = 0; j < nsm; ++j) {
+        const RowSink k{nullptr, nullptr, &tab.sm_dst[j], 1, out, dyn, row_out, nd};
+        quantize_variant<MODE, DT, YT, kOne>(row, p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h, s0, k, nvec,
+                                             s_red[nvr++ & 1]);
+      }
+    } else if (direct && nsm > 0) {
+      const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
+      quantize_variant<MODE, DT, YT, kMany>(row, chan, s0, k, nvec, s_red[nvr++ & 1]);
+    }
+
+    // variants through the shared buffers: one per bulk-plane pick (per-expert
+    // scales), or one for all picks when some go by bulk copies
     const int j0 = PE ? nsm : 0;
-    const int j1 = PE ? nsm + nbk : (nsm + nbk > 0 ? 1 : 0);
+    const int j1 = PE ? nsm + nbk : (!direct && nsm + nbk > 0 ? 1 : 0);
     for (int j = j0; j < j1; ++j) {
       const int qs = nv & 1;
       ++nv;
       uint8_t* q = qbuf + qs * slot_out;
       uint8_t* dq = dbuf + qs * slot_dyn;
-      if (PE && j > j0) {
+      if (j > j0) {
         if (tid == 0) bulk_wait_read<1>();
         __syncthreads();
       }
-      const float* srow = nullptr;
-      if (PE) {
-        const int seg = j < nsm ? tab.sm_seg[j] : tab.bulk_seg[j - nsm];
-        srow = p.qscales + (size_t)(seg / sh.W) * sh.h;
-      } else if (channel) {
-        srow = p.qscales;
-      }
-
-      if (MODE == 1) {
-        for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-          float f[8], sc[8];
-          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-          int qv[8];
-          if (srow) {
-            load_scales8(srow, v, sc);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) qv[k] = static_q(__fmul_rn(f[k], sc[k]));
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) qv[k] = static_q(__fmul_rn(f[k], s0));
-          }
-          *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
-        }
-      } else if (MODE == 2) {
-        float m = 0.f;
-        for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-          float f[8];
-          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-          if (PE) {
-            float sc[8];
-            load_scales8(srow, v, sc);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
-          }
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
-        }
-#pragma unroll
-        for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-        if (lane == 0) s_red[warp] = m;
-        __syncthreads();
-        float amax = 0.f;
-#pragma unroll
-        for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
-        const float scale = __fdiv_rn(amax, 127.0f);
-        for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-          float f[8];
-          unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-          if (PE) {
-            float sc[8];
-            load_scales8(srow, v, sc);
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
-          }
-          int qv[8];
-#pragma unroll
-          for (int k = 0; k < 8; ++k) qv[k] = amax == 0.f ? 0 : token_q(f[k], scale);
-          *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
-        }
-        if (tid == 0) reinterpret_cast<float*>(dq)[0] = scale;
-      } else {
-        // group (mode 3: 16 vectors) or block (mode 4: 4 vectors) per lane run;
-        // every lane of a warp takes part in the shuffles, past-the-end lanes
-        // with zeros
-        constexpr int kLanes = MODE == 3 ? 16 : 4;
-        for (uint32_t base = 0; base < nvec; base += kScatterThreads) {
-          const uint32_t v = base + tid;
-          const bool valid = v < nvec;
-          float f[8];
-          if (valid) {
-            unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-            if (PE) {
-              float sc[8];
-              load_scales8(srow, v, sc);
-#pragma unroll
-              for (int k = 0; k < 8; ++k) f[k] = __fmul_rn(f[k], sc[k]);
-            }
-          } else {
-#pragma unroll
-            for (int k = 0; k < 8; ++k) f[k] = 0.f;
-          }
-          float m = 0.f;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) m = fmaxf(m, fabsf(f[k]));
-#pragma unroll
-          for (int o = kLanes / 2; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
-          if (MODE == 3) {
-            const float scale = __fdiv_rn(m, fp8_max(YT));
-            if (valid) {
-              uint32_t c[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k)
-                c[k] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(f[2 * k], scale), __fdiv_rn(f[2 * k + 1], scale));
-              *reinterpret_cast<uint2*>(q + v * 8) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-              if ((v & 15u) == 0) reinterpret_cast<float*>(dq)[v >> 4] = scale;
-            }
-          } else {
-            const int se = mx_exponent(m, elem_emax(YT));
-            const float inv = exp2_exact(-se);
-            if (valid) {
-              uint32_t c[4];
-#pragma unroll
-              for (int k = 0; k < 4; ++k) c[k] = cvt_y_pair(YT, __fmul_rn(f[2 * k], inv), __fmul_rn(f[2 * k + 1], inv));
-              if (YT == MOE_Y_FP4_E2M1)
-                *reinterpret_cast<uint32_t*>(q + v * 4) = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
-              else
-                *reinterpret_cast<uint2*>(q + v * 8) = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
-              if ((v & 3u) == 0) dq[v >> 2] = (uint8_t)(se + 127);
-            }
-          }
-        }
-      }
+      const float* srow = PE ? p.qscales + (size_t)(tab.bulk_seg[j - nsm] / sh.W) * sh.h : chan;
+      const RowSink k{q, dq, nullptr, 0, out, dyn, row_out, nd};
+      quantize_variant<MODE, DT, YT, kShared>(row, srow, s0, k, nvec, s_red[nvr++ & 1]);
       fence_proxy_async_smem();
       __syncthreads();
 
-      // destinations of this variant: the pick (per-expert scales) or all picks
-      const int sm0 = PE ? (j < nsm ? j : 0) : 0, sm1 = PE ? (j < nsm ? j + 1 : 0) : nsm;
-      const int bk0 = PE ? (j < nsm ? 0 : j - nsm) : 0, bk1 = PE ? (j < nsm ? 0 : j - nsm + 1) : nbk;
+      // destinations: the bulk pick (per-expert scales) or every pick
+      const int bk0 = PE ? j - nsm : 0, bk1 = PE ? j - nsm + 1 : nbk;
+      const int ns = PE ? 0 : nsm;
       if (tid == 0) {
         for (int b = bk0; b < bk1; ++b) bulk_s2g(out + tab.bulk_dst[b] * row_out, q, row_out);
         bulk_commit();
       }
-      if (sm1 > sm0) {
+      if (ns > 0) {
         for (uint32_t u = tid; u < row_out / 16; u += kScatterThreads) {
           const int4 val = *reinterpret_cast<const int4*>(q + u * 16);
-          for (int b = sm0; b < sm1; ++b) st_v4(out + tab.sm_dst[b] * row_out + u * 16, val);
+          for (int b = 0; b < ns; ++b) st_v4(out + tab.sm_dst[b] * row_out + u * 16, val);
         }
       }
       if (MODE != 1) {
-        const int nd = sh.ngroups;
-        const int ndst = (sm1 - sm0) + (bk1 - bk0);
-        uint8_t* dyn = static_cast<uint8_t*>(p.dyn_scales);
+        const int ndst = ns + (bk1 - bk0);
         for (int idx = tid; idx < ndst * nd; idx += kScatterThreads) {
           const int b = idx / nd, g = idx % nd;
-          const long long dst = b < sm1 - sm0 ? tab.sm_dst[sm0 + b] : tab.bulk_dst[bk0 + b - (sm1 - sm0)];
+          const long long dst = b < ns ? tab.sm_dst[b] : tab.bulk_dst[bk0 + b - ns];
           if (dyn_es == 4)
             reinterpret_cast<float*>(dyn)[dst * nd + g] = reinterpret_cast<const float*>(dq)[g];
           else
