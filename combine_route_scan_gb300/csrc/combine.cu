@@ -6,7 +6,9 @@
 // pick gives nothing (aclnnMoeDistributeDispatchV4, 参数说明).
 //
 // GB300 form (one HBM, so no write-back pass is needed): an inverse-map kernel
-// turns assist_info (row -> pick) into pick -> row, then a gather kernel reads
+// turns assist_info (row -> pick) into pick -> row (unless the dispatch that
+// produced these very assist_info / ep_recv_count buffers already left that
+// map in the workspace), then a gather kernel reads
 // each token's K rows with 16-byte loads and reduces them in fp32, k
 // ascending, one fused multiply-add per pick, and rounds once to the output
 // type. The reduce checks every pick it reads against assist_info, so a row
@@ -29,6 +31,13 @@ __global__ void __launch_bounds__(kInvThreads) combine_inverse_kernel(CombinePar
   const int LW = sh.L * sh.W;
   pdl_wait();
   pdl_launch_dependents();
+  // the dispatch that wrote these assist_info / ep_recv_count buffers also
+  // wrote the map (the reduce still checks every pick against assist_info);
+  // callers without a workspace (moe_combine_noalloc) have no header
+  const WsHeader* h = p.hdr;
+  if (h && h->inv_valid && h->inv_assist == (unsigned long long)(uintptr_t)p.assist &&
+      h->inv_ep == (unsigned long long)(uintptr_t)p.ep_recv_count)
+    return;
   long long count = p.ep_recv_count[(size_t)d * LW + LW - 1];
   if (count < 0 || count > sh.A) {
     if (threadIdx.x == 0 && blockIdx.x == 0) set_error(p.status, MOE_ERR_BAD_ASSIST);

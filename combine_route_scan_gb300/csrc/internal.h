@@ -18,7 +18,10 @@ struct WsHeader {
   uint32_t tp_done;     // two-phase combine CTAs finished in the current call
   unsigned long long perf_start_inv;  // ~(earliest scatter CTA start), kept with atomicMax
   uint32_t scatter_done;              // scatter CTAs finished (performance info)
-  uint32_t pad[57];
+  uint32_t inv_valid;                 // the inv region holds the pick -> row map of the last dispatch ...
+  unsigned long long inv_assist;      // ... whose assist_info and ep_recv_count were these buffers
+  unsigned long long inv_ep;
+  uint32_t pad[52];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -73,6 +76,8 @@ struct RouteParams {
   uint32_t* landed;        // per-segment rows in place (zeroed here when flags are on)
   uint32_t* seg_ready;     // optional ready flags
   uint32_t ticket;
+  WsHeader* hdr;           // records which assist_info / ep_recv_count the pick -> row map belongs to
+  const int32_t* assist_out;
 };
 
 struct ScatterParams {
@@ -92,6 +97,7 @@ struct ScatterParams {
   uint32_t* landed;        // per-segment rows in place
   uint32_t* seg_ready;     // optional ready flags
   uint32_t ticket;
+  int32_t* inv;                    // pick -> flat row map (workspace), written for every routed pick
   int64_t* perf;                   // per-rank communication time (user array [W]), or null
   unsigned long long* perf_end;    // [W] workspace
   WsHeader* hdr;

@@ -224,6 +224,8 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   rp.landed = reinterpret_cast<uint32_t*>(w + L.landed);
   rp.seg_ready = cfg->seg_ready;
   rp.ticket = cfg->seg_ready_ticket;
+  rp.hdr = hdr;
+  rp.assist_out = assist_info;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
 
   ScatterParams sp{};
@@ -231,6 +233,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.landed = rp.landed;
   sp.seg_ready = cfg->seg_ready;
   sp.ticket = cfg->seg_ready_ticket;
+  sp.inv = reinterpret_cast<int32_t*>(w + L.inv);
   sp.perf = cfg->performance_info;
   sp.perf_end = reinterpret_cast<unsigned long long*>(w + L.perf_end);
   sp.hdr = hdr;
@@ -367,6 +370,8 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   rp.bulk_min_bytes = cfg->bulk_min_bytes;
   rp.done = &hdr->route_done;
   rp.status = &hdr->status;
+  rp.hdr = hdr;
+  rp.assist_out = assist;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
   ScatterParams sp{};
   sp.x = x;
@@ -374,6 +379,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   sp.mask = rp.mask;
   sp.expand_x = ex;
   sp.assist = assist;
+  sp.inv = reinterpret_cast<int32_t*>(w + L.inv);
   sp.rank = rp.rank;
   sp.base = rp.base;
   sp.plane = rp.plane;
@@ -411,7 +417,8 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   cp.inv = reinterpret_cast<int32_t*>(w + L.inv);
   cp.sh = sh;
   cp.status = &hdr->status;
-  if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  cp.hdr = hdr;
+  // the scatter above wrote the pick -> row map: no inverse pass
   if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
   return MOE_OK;
 }

@@ -78,6 +78,11 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   pdl_wait();
   pdl_launch_dependents();
 
+  if (s == 0 && tid == 0 && p.hdr) {  // the scatter that follows writes the pick -> row map
+    p.hdr->inv_assist = (unsigned long long)(uintptr_t)p.assist_out;
+    p.hdr->inv_ep = (unsigned long long)(uintptr_t)p.ep_recv_count;
+    p.hdr->inv_valid = 1u;
+  }
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
   if (sh.mask_kind == 1) {
     const uint8_t* m = p.mask + (size_t)s * sh.bs;

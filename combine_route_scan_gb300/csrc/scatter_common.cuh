@@ -51,6 +51,7 @@ __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, 
       if (row < sh.A) {
         dst = (long long)d * sh.A + row;
         bulk = p.plane[g];
+        if (p.inv) p.inv[tau * sh.K + lane] = (int32_t)dst;
         int32_t* a = p.assist + dst * 3;
         a[0] = s;
         a[1] = t;

@@ -389,3 +389,57 @@ def test_dispatch_performance_info_alignment():
         M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
                    out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws)
     assert ei.value.name == "INVALID_ARG"
+
+
+# ------------------------------------- pick -> row map left by the dispatch
+
+def _combine_same_ws(wl, dev, got, ws, assist=None, ep=None):
+    cfg = H.make_cfg(wl, quant_mode=0)
+    x_out = torch.empty((wl.ep_world_size, wl.bs, wl.h), dtype=H.TORCH_DT[wl.x_dtype], device="cuda")
+    M.combine(cfg, got["expand_x"], got["assist_info"] if assist is None else assist,
+              got["ep_recv_count"] if ep is None else ep, dev["expert_ids"], dev["expert_scales"],
+              dev["active_mask"], dev["x"], x_out, None, ws)
+    return x_out, M.get_device_status(ws)
+
+
+@pytest.mark.parametrize("name", ["w16_bs256_h7168_k8_e256_bf16_zipf", "w8_bs8_h16_k2_e64_i32", "ragged_h12_f16"])
+def test_combine_reuses_the_dispatch_row_map(name):
+    """Dispatch and combine on one workspace: the combine takes the map the
+    scatter wrote (no inverse pass) and matches the oracle byte for byte."""
+    if name == "ragged_h12_f16":
+        wl = WL.Workload(name, 4, 9, 12, 3, 8, WL.X_FP16, mask_kind=2, mask_false_p=0.2, zero_expert_num=1,
+                         copy_expert_num=1, special_p=0.2, seed=41)
+    else:
+        wl = WL.WORKLOADS[name]
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    x_ref = O.combine(wl, ref["expand_x"], ref["assist_info"], ref["ep_recv_count"], inp)
+    dev = H.device_inputs(wl, inp)
+    got, ws, _ = H.gpu_dispatch(wl, dev)
+    x_out, st = _combine_same_ws(wl, dev, got, ws)
+    assert st == 0
+    assert np.array_equal(H.to_host(x_out).view(np.uint8), x_ref.view(np.uint8))
+
+
+def test_row_map_follows_the_buffers():
+    """Two dispatches on one workspace into different output buffers: a
+    combine of the first one's buffers rebuilds its map and is still right;
+    a row map changed in place after the dispatch is reported, not used."""
+    wl = WL.WORKLOADS["w8_bs8_h16_k2_e64_i32"]
+    inp_a = WL.make_inputs(wl)
+    inp_b = WL.make_inputs(wl, seed=99)
+    dev_a, dev_b = H.device_inputs(wl, inp_a), H.device_inputs(wl, inp_b)
+    got_a, ws, _ = H.gpu_dispatch(wl, dev_a)
+    got_b, _, _ = H.gpu_dispatch(wl, dev_b, ws=ws)
+    ref_a = O.dispatch(wl, inp_a)
+    x_ref = O.combine(wl, ref_a["expand_x"], ref_a["assist_info"], ref_a["ep_recv_count"], inp_a)
+    x_out, st = _combine_same_ws(wl, dev_a, got_a, ws)
+    assert st == 0 and np.array_equal(H.to_host(x_out), x_ref)
+    # B's buffers are the ones the workspace's map belongs to; now break B's
+    # assist_info in place (same pointer): the reduce's check must catch it
+    got_b2, ws2, _ = H.gpu_dispatch(wl, dev_b)
+    ep = H.to_host(got_b2["ep_recv_count"])
+    d = int(np.argmax(ep[:, -1]))
+    got_b2["assist_info"][d, 0, 1] = (got_b2["assist_info"][d, 0, 1] + 1) % wl.bs
+    _, st = _combine_same_ws(wl, dev_b, got_b2, ws2)
+    assert M.STATUS[st] == "BAD_ASSIST"
