@@ -178,16 +178,30 @@ def measured_peaks() -> dict:
     return {"hbm_gbs": FALLBACK_HBM_GBPS, "source": "fallback"}
 
 
+# the source files each profiled kernel is built from
+KERNEL_SOURCES = {
+    "scatter": ("scatter.cu", "scatter_common.cuh", "common.cuh", "internal.h"),
+    "scatter_quant": ("scatter_quant.cu", "scatter_common.cuh", "common.cuh", "internal.h"),
+    "combine_reduce": ("combine.cu", "common.cuh", "internal.h"),
+}
+
+
+def source_hash(kernel: str) -> str:
+    """First 16 hex digits of the sha256 over the kernel's source files."""
+    h = hashlib.sha256()
+    for name in KERNEL_SOURCES[kernel]:
+        with open(os.path.join(ROOT, "combine_route_scan_gb300", "csrc", name), "rb") as f:
+            h.update(f.read())
+    return h.hexdigest()[:16]
+
+
 def committed_traffic(kernel: str, workload: str):
     """DRAM bytes per launch from the committed ncu summary, if it was taken on
-    the current kernel source (its hash is recorded beside the figure)."""
+    the current kernel sources (their hash is recorded beside the figure)."""
     p = os.path.join(ROOT, "profiles", f"{kernel}_{workload}.md")
     if not os.path.exists(p):
         return None
-    src = os.path.join(ROOT, "combine_route_scan_gb300", "csrc",
-                       {"scatter": "scatter.cu", "combine_reduce": "combine.cu"}[kernel])
-    with open(src, "rb") as f:
-        h = hashlib.sha256(f.read()).hexdigest()[:16]
+    h = source_hash(kernel)
     vals = {}
     with open(p) as f:
         for line in f:
@@ -718,6 +732,38 @@ def run_ours(args):
                      "steps": Kt}
         del ws_tp
 
+    # the optional dispatch outputs: per-segment ready flags and per-rank
+    # communication time, each timed on its own against the plain call
+    options = None
+    if world == 1:
+        L_ = wl.moe_expert_num // wl.ep_world_size
+        flags = torch.zeros((wl.ep_world_size, L_ * wl.ep_world_size), dtype=torch.int32, device="cuda")
+        perf = torch.zeros(wl.ep_world_size, dtype=torch.int64, device="cuda")
+        variants = {"plain": lambda i: cfg,
+                    "seg_ready": lambda i: M.with_seg_ready(cfg, flags, 1000 + i),
+                    "performance_info": lambda i: M.with_performance_info(cfg, perf)}
+        Ko = max(1, min(K, 200))
+        options = {}
+        for name, mk in variants.items():
+            cfgs = [mk(i) for i in range(Ko + 3)]
+            for i in range(3):
+                M.dispatch(cfgs[i], x, ids, mask, scales, out["expand_x"], out["dynamic_scales"], out["assist_info"],
+                           out["ep_recv_count"], out["expand_scales"], None, ws)
+            torch.cuda.synchronize()
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            for i in range(Ko):
+                M.dispatch(cfgs[3 + i], x, ids, mask, scales, out["expand_x"], out["dynamic_scales"],
+                           out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws)
+            b.record(stream)
+            torch.cuda.synchronize()
+            options[name + "_dispatch_ms"] = a.elapsed_time(b) / Ko
+        st = M.get_device_status(ws)
+        if st != 0:
+            raise RuntimeError(f"device status {M.STATUS.get(st, st)} with the dispatch options")
+        options["per_rank_comm_us_mean"] = float(perf.double().mean().item()) / (Ko + 3) / 1e3
+        options["steps"] = Ko
+
     ffn = None if args.no_ffn or world > 1 else measure_ffn(args, M, torch, stream)
     small = None if world > 1 or not args.small_workloads else measure_small(args, M, torch, stream)
     quant = None if world > 1 or not args.quant_modes else measure_quant(args, M, torch, stream, wl)
@@ -836,6 +882,7 @@ def run_ours(args):
                 "streams": "H2D, compute and D2H on three streams, double-buffered",
                 "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h},
         "two_phase_combine": two_phase,
+        "dispatch_options": options,
         "ffn_variant": ffn,
         "small_workloads": small,
         "quant_dispatch": quant,

@@ -22,24 +22,26 @@
 
 namespace crs {
 
-// Ready flags, called by thread 0 right after the first barrier of token i:
+// Ready flags, called by warp 0 right after the first barrier of token i:
 //   * token i-1's store-plane rows: every thread passed the barrier after
 //     storing them, so a fence makes them visible before the count;
 //   * token i-2's bulk-plane rows: its bulk group is complete once at most one
-//     newer group (token i-1's) is pending; then an async-proxy fence.
+//     newer group (token i-1's) is pending (lane 0 issued them and waits);
+//     then an async-proxy fence.
 __device__ __forceinline__ void publish_earlier(const ScatterParams& p, const PickTable* tabs, int i) {
   if (i >= 1) {
-    __threadfence();
     const PickTable& a = tabs[(i - 1) % 3];
-    for (int j = 0; j < a.n_sm; ++j) publish_row(p, a.sm_seg[j]);
+    publish_rows_warp(p, a.sm_seg, a.n_sm);
   }
   if (i >= 2) {
     const PickTable& b = tabs[(i - 2) % 3];
     if (b.n_bulk > 0) {
-      bulk_wait_all<1>();
-      fence_proxy_async_global();
-      __threadfence();
-      for (int j = 0; j < b.n_bulk; ++j) publish_row(p, b.bulk_seg[j]);
+      if ((threadIdx.x & 31) == 0) {
+        bulk_wait_all<1>();
+        fence_proxy_async_global();
+      }
+      __syncwarp();
+      publish_rows_warp(p, b.bulk_seg, b.n_bulk);
     }
   }
 }
@@ -95,7 +97,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     if (warp == 0) build_picks(p, tau, s, t, tab);
     __syncthreads();
     if (s_abort) break;
-    if (p.seg_ready && tid == 0) publish_earlier(p, tabs, i);
+    if (p.seg_ready && warp == 0) publish_earlier(p, tabs, i);
     if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
     const int nb = tab.n_bulk, ns = tab.n_sm;
     if (tid == 0) {
@@ -121,19 +123,21 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
   // all bulk stores of this CTA complete before it exits
   if (p.seg_ready) {
     __syncthreads();  // every thread's stores of the last token are issued
-    if (tid == 0 && !s_abort) {
-      bulk_wait_all<0>();
-      fence_proxy_async_global();
-      __threadfence();
+    if (warp == 0 && !s_abort) {
+      if (tid == 0) {
+        bulk_wait_all<0>();
+        fence_proxy_async_global();
+      }
+      __syncwarp();
       const int last = my_n - 1;
       if (last >= 0) {
         const PickTable& a = tabs[last % 3];
-        for (int j = 0; j < a.n_sm; ++j) publish_row(p, a.sm_seg[j]);
-        for (int j = 0; j < a.n_bulk; ++j) publish_row(p, a.bulk_seg[j]);
+        publish_rows_warp(p, a.sm_seg, a.n_sm);
+        publish_rows_warp(p, a.bulk_seg, a.n_bulk);
       }
       if (last >= 1) {
         const PickTable& b = tabs[(last - 1) % 3];
-        for (int j = 0; j < b.n_bulk; ++j) publish_row(p, b.bulk_seg[j]);
+        publish_rows_warp(p, b.bulk_seg, b.n_bulk);
       }
     }
   }
@@ -188,10 +192,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
       }
     }
     __syncthreads();
-    if (p.seg_ready && tid == 0) {  // every thread's rows of this token are stored
-      __threadfence();
-      for (int k = 0; k < ns; ++k) publish_row(p, tab.sm_seg[k]);
-    }
+    // every thread's rows of this token are stored
+    if (p.seg_ready && warp == 0) publish_rows_warp(p, tab.sm_seg, ns);
     if (p.perf && tid == 0) perf_mark(p, tau);
     __syncthreads();
   }

@@ -33,6 +33,16 @@ __device__ __forceinline__ void publish_row(const ScatterParams& p, int g) {
   }
 }
 
+// Ready flags by the lanes of one warp: lane j counts row j in (a token's rows
+// lie in distinct segments, so the atomics hit distinct counters and run in
+// parallel). Every lane fences first; the caller has made the rows' stores
+// visible to this warp (a CTA barrier; for bulk copies, lane 0 waited for
+// their completion and fenced the async proxy before a __syncwarp).
+__device__ __forceinline__ void publish_rows_warp(const ScatterParams& p, const int* segs, int n) {
+  __threadfence();
+  if ((int)(threadIdx.x & 31) < n) publish_row(p, segs[threadIdx.x & 31]);
+}
+
 // Builds the destination list of token `tau` (warp 0 only) and writes the
 // per-row metadata. Returns nothing; results land in `tab`.
 __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, int s, int t, PickTable& tab) {

@@ -129,13 +129,16 @@ __device__ __forceinline__ void load_scales8(const float* srow, uint32_t v, floa
   s[4] = b.x; s[5] = b.y; s[6] = b.z; s[7] = b.w;
 }
 
-// Rows of token i-1 are complete: count them toward their segments' flags.
+// Rows of token i-1 are complete: warp 0 counts them toward their segments'
+// flags, after lane 0 (which issued the bulk copies) saw them complete.
 __device__ __forceinline__ void publish_token(const ScatterParams& p, const PickTable& a) {
-  bulk_wait_all<0>();
-  fence_proxy_async_global();
-  __threadfence();
-  for (int j = 0; j < a.n_sm; ++j) publish_row(p, a.sm_seg[j]);
-  for (int j = 0; j < a.n_bulk; ++j) publish_row(p, a.bulk_seg[j]);
+  if ((threadIdx.x & 31) == 0) {
+    bulk_wait_all<0>();
+    fence_proxy_async_global();
+  }
+  __syncwarp();
+  publish_rows_warp(p, a.sm_seg, a.n_sm);
+  publish_rows_warp(p, a.bulk_seg, a.n_bulk);
 }
 
 // Where a quantised row goes: the shared buffers q (codes) and dq (dynamic
@@ -356,8 +359,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
     if (warp == 0) build_picks(p, tau, s, t, tab);
     __syncthreads();
     if (s_abort) break;
+    if (p.seg_ready && warp == 0 && i >= 1) publish_token(p, tabs[(i - 1) & 1]);
     if (tid == 0 && i >= 1) {
-      if (p.seg_ready) publish_token(p, tabs[(i - 1) & 1]);
       if (p.perf) perf_mark(p, tau - G);
       // the previous token's source slot is free: its reads were generic loads
       // that all finished before the barrier above
@@ -435,10 +438,12 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
     }
   }
   __syncthreads();  // every thread's stores of the last token are issued
-  if (tid == 0 && !s_abort && my_n > 0) {
+  if (warp == 0 && !s_abort && my_n > 0) {
     if (p.seg_ready) publish_token(p, tabs[(my_n - 1) & 1]);
-    bulk_wait_all<0>();
-    if (p.perf) perf_mark(p, blockIdx.x + (size_t)(my_n - 1) * G);
+    if (tid == 0) {
+      bulk_wait_all<0>();
+      if (p.perf) perf_mark(p, blockIdx.x + (size_t)(my_n - 1) * G);
+    }
   }
   if (tid == 0) bulk_wait_all<0>();
   if (p.perf) {
@@ -556,10 +561,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_plain_kernel(Sc
       }
     }
     __syncthreads();
-    if (p.seg_ready && tid == 0) {  // every thread's rows of this token are stored
-      __threadfence();
-      for (int k = 0; k < ns; ++k) publish_row(p, tab.sm_seg[k]);
-    }
+    // every thread's rows of this token are stored
+    if (p.seg_ready && warp == 0) publish_rows_warp(p, tab.sm_seg, ns);
     if (p.perf && tid == 0) perf_mark(p, tau);
     __syncthreads();
   }
