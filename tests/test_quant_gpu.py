@@ -135,3 +135,26 @@ def test_quant_argument_errors():
     assert ei.value.name == "INVALID_ARG"
     M.dispatch(cfg, *args, scales=buf[4:68])
     assert M.get_device_status(ws) == 0
+
+
+@pytest.mark.parametrize("seed", range(24))
+def test_quant_random_shapes(seed):
+    """Random shapes (ragged and TMA rows, 1D / 2D masks, zero / copy experts),
+    a random quantised mode, element type and scales input, a random plane
+    policy: every routed row's codes and dynamic scales byte for byte."""
+    rng = np.random.default_rng(7000 + seed)
+    q, y, k = MODES[int(rng.integers(0, len(MODES)))]
+    W = int(rng.integers(2, 7))
+    L = int(rng.integers(1, 5))
+    K = int(rng.integers(1, min(W * L, 8) + 1))
+    h = int(rng.choice([16, 32, 48, 96, 130, 256, 384, 1000, 2048]))
+    if y == "fp4_e2m1" and h % 2:
+        h += 1
+    wl = WL.Workload(f"qrand{seed}", W, int(rng.integers(1, 24)), h, K, W * L,
+                     WL.X_BF16 if rng.random() < 0.5 else WL.X_FP16,
+                     zero_expert_num=int(rng.integers(0, 3)), copy_expert_num=int(rng.integers(0, 3)),
+                     mask_kind=int(rng.integers(0, 3)), special_p=0.2, mask_false_p=0.2,
+                     ids="zipf" if rng.random() < 0.5 else "uniform",
+                     quant_mode=q, y_dtype=y, scales_kind=k, seed=int(rng.integers(0, 2**31)))
+    policy = [M.PLANE_RULE, M.PLANE_STORES_ONLY, M.PLANE_BULK_ALL][int(rng.integers(0, 3))]
+    run(wl, plane_policy=policy, bulk_min_bytes=0 if policy == M.PLANE_RULE else None)
