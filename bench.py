@@ -711,7 +711,14 @@ def run_ours(args):
 
         Kt = max(1, min(K, 200))
         res = {}
-        for name, c in (("full_op", cfg_tp), ("comm_only", cfg_put)):
+        # the README's comparison: the classic single plane (every segment by
+        # SM stores) against the two planes
+        cfg_tp_c = M.MoeConfig.from_buffer_copy(cfg_tp)
+        cfg_tp_c.plane_policy = M.PLANE_STORES_ONLY
+        cfg_put_c = M.MoeConfig.from_buffer_copy(cfg_put)
+        cfg_put_c.plane_policy = M.PLANE_STORES_ONLY
+        for name, c in (("full_op", cfg_tp), ("comm_only", cfg_put), ("classic_full_op", cfg_tp_c),
+                        ("classic_comm_only", cfg_put_c)):
             for _ in range(3):
                 tp_call(c)
             torch.cuda.synchronize()
@@ -729,6 +736,7 @@ def run_ours(args):
         two_phase = {"full_op_ms": res["full_op"], "comm_only_ms": res["comm_only"],
                      "full_op_GBps": acct["combine"] / (res["full_op"] * 1e-3) / 1e9,
                      "comm_only_GBps": put_bytes / (res["comm_only"] * 1e-3) / 1e9,
+                     "classic_full_op_ms": res["classic_full_op"], "classic_comm_only_ms": res["classic_comm_only"],
                      "steps": Kt}
         del ws_tp
 
@@ -763,6 +771,10 @@ def run_ours(args):
             raise RuntimeError(f"device status {M.STATUS.get(st, st)} with the dispatch options")
         options["per_rank_comm_us_mean"] = float(perf.double().mean().item()) / (Ko + 3) / 1e3
         options["steps"] = Ko
+        # the page's split for dispatch: full_op = the whole call (routing +
+        # payload), comm_only = the payload kernel (puts and, when on, flags)
+        options["full_op_ms"] = options["plain_dispatch_ms"]
+        options["comm_only_ms"] = scatter_ms
 
     ffn = None if args.no_ffn or world > 1 else measure_ffn(args, M, torch, stream)
     small = None if world > 1 or not args.small_workloads else measure_small(args, M, torch, stream)

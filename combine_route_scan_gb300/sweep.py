@@ -33,6 +33,9 @@ Inputs are seeded and synthetic: x uniform in [-1000, 1000] (int32) or N(0, 1)
     python -m combine_route_scan_gb300.sweep --pes-list 2,4,8 --bs-list 8,16,32 \\
         --h-list 64,256,1024 --topk-list 2 --expert-per-pe-list 2,8 --type int32 \\
         --prof-pe all --warmup 5 --loops 50 --out-dir sweep_out
+
+``--plane-policy stores`` runs the classic single plane (every segment by SM
+stores), the README's comparison point for the two planes.
 """
 from __future__ import annotations
 
@@ -51,9 +54,11 @@ from . import moe as M
 TYPES = {"int32": torch.int32, "int32_t": torch.int32, "fp16": torch.float16, "float16_t": torch.float16,
          "bf16": torch.bfloat16, "bfloat16_t": torch.bfloat16}
 
-RANK_FIELDS = ["pes", "bs", "h", "topk", "expert_per_pe", "type", "rank", "recv_rows", "bulk_put_rows",
+PLANES = {"rule": M.PLANE_RULE, "stores": M.PLANE_STORES_ONLY, "bulk": M.PLANE_BULK_ALL}
+
+RANK_FIELDS = ["pes", "bs", "h", "topk", "expert_per_pe", "type", "planes", "rank", "recv_rows", "bulk_put_rows",
                "bulk_put_bytes", "full_op_us", "comm_only_us", "gather_us", "dispatch_us", "dispatch_comm_us"]
-SUMMARY_FIELDS = ["pes", "bs", "h", "topk", "expert_per_pe", "type", "routed_rows", "full_op_us", "comm_only_us",
+SUMMARY_FIELDS = ["pes", "bs", "h", "topk", "expert_per_pe", "type", "planes", "routed_rows", "full_op_us", "comm_only_us",
                   "gather_us", "dispatch_us", "combine_bytes", "gather_GBps", "full_op_GBps", "comm_only_GBps",
                   "dispatch_comm_us_min", "dispatch_comm_us_mean", "dispatch_comm_us_max",
                   "two_phase_matches_gather"]
@@ -75,6 +80,9 @@ def parse_args(argv=None):
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--loops", type=int, default=50)
     ap.add_argument("--seed", type=int, default=0)
+    ap.add_argument("--plane-policy", default="rule", choices=sorted(PLANES),
+                    help="rule: the README's two planes; stores: the classic single plane; bulk: every remote "
+                         "segment by bulk copies")
     ap.add_argument("--out-dir", default="sweep_out")
     return ap.parse_args(argv)
 
@@ -116,7 +124,7 @@ def mean_event_ms(fn, warmup: int, loops: int) -> float:
 def run_shape(W: int, bs: int, h: int, K: int, L: int, dtype: torch.dtype, args) -> Dict:
     E = W * L
     inp = make_inputs(W, bs, h, K, E, dtype, args.seed + 7919 * W + 131 * bs + h + 17 * K + L)
-    cfg_d = M.config(W, bs, h, K, E, dtype)
+    cfg_d = M.config(W, bs, h, K, E, dtype, plane_policy=PLANES[args.plane_policy])
     ws = M.alloc_workspace(M.config(W, bs, h, K, E, dtype, combine_mode=M.COMBINE_TWO_PHASE))
     out = M.alloc_dispatch_outputs(cfg_d, dtype)
     perf = torch.zeros(W, dtype=torch.int64, device="cuda")
@@ -138,7 +146,7 @@ def run_shape(W: int, bs: int, h: int, K: int, L: int, dtype: torch.dtype, args)
     seg_plane = torch.zeros((W, L * W), dtype=torch.uint8, device="cuda")
 
     def combine(mode, x_out, sp=None):
-        c = M.config(W, bs, h, K, E, dtype, combine_mode=mode)
+        c = M.config(W, bs, h, K, E, dtype, combine_mode=mode, plane_policy=PLANES[args.plane_policy])
         return lambda: M.combine(c, out["expand_x"], out["assist_info"], out["ep_recv_count"], inp["ids"],
                                  inp["w"], None, inp["x"], x_out, sp, ws)
 
@@ -177,7 +185,8 @@ def main(argv=None) -> int:
     summary: List[Dict] = []
     for W, bs, h, K, L in shapes(args):
         r = run_shape(W, bs, h, K, L, dtype, args)
-        key = {"pes": W, "bs": bs, "h": h, "topk": K, "expert_per_pe": L, "type": args.type}
+        key = {"pes": W, "bs": bs, "h": h, "topk": K, "expert_per_pe": L, "type": args.type,
+               "planes": args.plane_policy}
         for d in range(W):
             if ranks_wanted is not None and d not in ranks_wanted:
                 continue
