@@ -3,6 +3,12 @@
 Each .cu file compiles to its own object in parallel with nvcc, then nvcc links
 them into combine_route_scan_gb300/_build/libcrs_moe.so. The CUDA runtime is
 linked statically. No cmake.
+
+``build(checked=True)`` builds the bounds-checked variant
+(_build/checked/libcrs_moe.so, ``-DMOE_BOUNDS_CHECK``): every index a kernel
+derives from data is checked against its buffer, and a miss records
+MOE_ERR_OUT_OF_BOUNDS and skips the access. The binding loads it when the
+environment variable CRS_MOE_CHECKED is 1.
 """
 from __future__ import annotations
 
@@ -16,6 +22,8 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcrs_moe.so")
+CHECKED_DIR = os.path.join(OUT_DIR, "checked")
+CHECKED_LIB = os.path.join(CHECKED_DIR, "libcrs_moe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]
@@ -39,17 +47,18 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
-    os.makedirs(OUT_DIR, exist_ok=True)
-    if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= _inputs_mtime():
-        return LIB
+def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False) -> str:
+    out_dir, lib = (CHECKED_DIR, CHECKED_LIB) if checked else (OUT_DIR, LIB)
+    os.makedirs(out_dir, exist_ok=True)
+    if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _inputs_mtime():
+        return lib
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or [])
+    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DMOE_BOUNDS_CHECK"] if checked else [])
     if verbose:
         flags = flags + ["-Xptxas", "-v"]
 
     def compile_one(src: str) -> str:
-        obj = os.path.join(OUT_DIR, os.path.basename(src)[:-3] + ".o")
+        obj = os.path.join(out_dir, os.path.basename(src)[:-3] + ".o")
         cmd = [cc, *ARCH, *flags, "-c", src, "-o", obj]
         r = subprocess.run(cmd, capture_output=True, text=True)
         if r.returncode != 0:
@@ -60,15 +69,15 @@ def build(force: bool = False, verbose: bool = False, extra_flags=None) -> str:
 
     with cf.ThreadPoolExecutor(max_workers=max(1, min(8, os.cpu_count() or 1))) as ex:
         objs = list(ex.map(compile_one, sources()))
-    tmp = LIB + f".tmp{os.getpid()}"
+    tmp = lib + f".tmp{os.getpid()}"
     cmd = [cc, *ARCH, "-shared", "-o", tmp, *objs]
     r = subprocess.run(cmd, capture_output=True, text=True)
     if r.returncode != 0:
         raise RuntimeError(f"link failed:\n{r.stdout}\n{r.stderr}")
-    os.replace(tmp, LIB)
-    return LIB
+    os.replace(tmp, lib)
+    return lib
 
 
 if __name__ == "__main__":
     import sys
-    print(build(force=True, verbose="-v" in sys.argv))
+    print(build(force=True, verbose="-v" in sys.argv, checked="--checked" in sys.argv))

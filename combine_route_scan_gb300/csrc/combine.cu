@@ -51,7 +51,10 @@ __global__ void __launch_bounds__(kInvThreads) combine_inverse_kernel(CombinePar
       set_error(p.status, MOE_ERR_BAD_ASSIST);
       continue;
     }
-    p.inv[((size_t)s * sh.bs + t) * sh.K + k] = (int32_t)fr;
+    const long long pk = ((long long)s * sh.bs + t) * sh.K + k;
+    if (MOE_IN_BOUNDS(p.status, pk, (long long)sh.W * sh.bs * sh.K) &&
+        MOE_IN_BOUNDS(p.status, fr, (long long)sh.W * sh.A))
+      p.inv[pk] = (int32_t)fr;
   }
 }
 
@@ -220,7 +223,7 @@ __global__ void __launch_bounds__(kReduceThreads, 4) combine_reduce_kernel(Combi
     if (cls >= 0) {
       d = cls / sh.L;
       const long long row = r - (long long)d * sh.A;
-      if (row >= 0 && row < sh.A) {
+      if (row >= 0 && row < sh.A && MOE_IN_BOUNDS(p.status, r, (long long)sh.W * sh.A)) {
         src = static_cast<const uint8_t*>(p.expert_out) + r * (long long)sh.row_in;
       } else {
         set_error(p.status, MOE_ERR_BAD_ASSIST);

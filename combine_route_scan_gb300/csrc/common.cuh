@@ -23,6 +23,20 @@ __device__ __forceinline__ void set_error(int* status, int code) {
   atomicCAS(status, 0, code);
 }
 
+// Bounds checks of checked builds (-DMOE_BOUNDS_CHECK): an index outside its
+// buffer records MOE_ERR_OUT_OF_BOUNDS and the guarded access is skipped.
+// Ordinary builds compile every check to `true`.
+__device__ __forceinline__ bool in_bounds_checked(int* status, long long idx, long long n) {
+  if (idx >= 0 && idx < n) return true;
+  set_error(status, MOE_ERR_OUT_OF_BOUNDS);
+  return false;
+}
+#ifdef MOE_BOUNDS_CHECK
+#define MOE_IN_BOUNDS(status, idx, n) ::crs::in_bounds_checked((status), (long long)(idx), (long long)(n))
+#else
+#define MOE_IN_BOUNDS(status, idx, n) true
+#endif
+
 __device__ __forceinline__ uint64_t globaltimer_ns() {
   uint64_t t;
   asm volatile("mov.u64 %0, %%globaltimer;" : "=l"(t));

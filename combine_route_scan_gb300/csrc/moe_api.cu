@@ -446,6 +446,7 @@ const char* moe_status_string(int32_t status) {
     case MOE_ERR_CUDA: return "CUDA runtime error";
     case MOE_ERR_CAPACITY: return "receive capacity exceeded";
     case MOE_ERR_BAD_ASSIST: return "assist_info / ep_recv_count do not match the routing";
+    case MOE_ERR_OUT_OF_BOUNDS: return "index outside its buffer (bounds-checked build)";
     default: return "unknown status";
   }
 }

@@ -54,11 +54,11 @@ __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, 
     // position and id are independent loads: issue both before using either
     const int r = p.rank[tau * sh.K + lane];
     const int e = p.ids[tau * sh.K + lane];
-    if (r >= 0) {
+    if (r >= 0 && MOE_IN_BOUNDS(p.status, e, sh.E)) {
       const int d = e / sh.L;
       const size_t g = (size_t)e * sh.W + s;
       const long long row = (long long)p.base[g] + r;
-      if (row < sh.A) {
+      if (row < sh.A && MOE_IN_BOUNDS(p.status, (long long)d * sh.A + row, (long long)sh.W * sh.A)) {
         dst = (long long)d * sh.A + row;
         bulk = p.plane[g];
         if (p.inv) p.inv[tau * sh.K + lane] = (int32_t)dst;

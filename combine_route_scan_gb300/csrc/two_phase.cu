@@ -113,7 +113,11 @@ __global__ void __launch_bounds__(kTpThreads, 1) two_phase_kernel(CombineParams 
   for (int d = tid; d < W; d += kTpThreads) {
     long long own = 0;
     for (int le = 0; le < sh.L; ++le) own += seg_rows(p.ep_recv_count, d, LW, le * W + d);
-    const long long cnt = p.ep_recv_count[(size_t)d * LW + LW - 1];
+    long long cnt = p.ep_recv_count[(size_t)d * LW + LW - 1];
+    if (cnt < 0 || cnt > sh.A) {  // a count the routing cannot produce: report it, stay inside rank d's rows
+      set_error(p.status, MOE_ERR_BAD_ASSIST);
+      cnt = cnt < 0 ? 0 : sh.A;
+    }
     remote[d] = cnt - own;
     bprefix[d + 1] = (int)((cnt + R - 1) / R);
   }
@@ -151,16 +155,17 @@ __global__ void __launch_bounds__(kTpThreads, 1) two_phase_kernel(CombineParams 
       if (bprefix[mid] <= b) lo = mid; else hi = mid;
     }
     const int d = lo;
-    const long long cnt = p.ep_recv_count[(size_t)d * LW + LW - 1];
+    const long long cnt = min((long long)sh.A, (long long)p.ep_recv_count[(size_t)d * LW + LW - 1]);
     const long long r = (long long)(b - bprefix[d]) * R + lane;
     long long q = -1;  // window slot of this lane's row
     int bulk = 0;
-    if (lane < R && r < cnt) {
+    if (lane < R && r < cnt && MOE_IN_BOUNDS(p.status, (long long)d * sh.A + r, (long long)W * sh.A)) {
       const long long fr = (long long)d * sh.A + r;
       const int s = p.assist[fr * 3 + 0], t = p.assist[fr * 3 + 1], k = p.assist[fr * 3 + 2];
       if (s >= 0 && s < W && t >= 0 && t < sh.bs && k >= 0 && k < sh.K) {
         const int e = p.ids[((size_t)s * sh.bs + t) * sh.K + k];
-        if (e >= 0 && e < sh.E && e / sh.L == d) {
+        if (e >= 0 && e < sh.E && e / sh.L == d &&
+            MOE_IN_BOUNDS(p.status, ((long long)s * sh.bs + t) * sh.K + k, (long long)W * sh.bs * sh.K)) {
           q = ((long long)s * sh.bs + t) * sh.K + k;
           const long long rows = seg_rows(p.ep_recv_count, d, LW, (e % sh.L) * W + s);
           if (p.bulk_ok && s != d && rows > 0) {

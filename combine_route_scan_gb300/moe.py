@@ -15,11 +15,13 @@ from typing import Optional
 import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "_build", "libcrs_moe.so")
+# CRS_MOE_CHECKED=1 selects the bounds-checked build (build.build(checked=True))
+LIB_PATH = os.path.join(_HERE, "_build", *(["checked"] if os.environ.get("CRS_MOE_CHECKED") == "1" else []),
+                        "libcrs_moe.so")
 
 MOE_OK = 0
 STATUS = {0: "OK", 1: "INVALID_ARG", 2: "UNSUPPORTED", 3: "WORKSPACE", 4: "BAD_EXPERT_ID",
-          5: "MASK_ORDER", 6: "TIMEOUT", 7: "CUDA", 8: "CAPACITY", 9: "BAD_ASSIST"}
+          5: "MASK_ORDER", 6: "TIMEOUT", 7: "CUDA", 8: "CAPACITY", 9: "BAD_ASSIST", 10: "OUT_OF_BOUNDS"}
 
 MOE_I32, MOE_F16, MOE_BF16 = 0, 1, 2
 DTYPE_CODE = {torch.int32: MOE_I32, torch.float16: MOE_F16, torch.bfloat16: MOE_BF16}

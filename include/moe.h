@@ -60,6 +60,8 @@ typedef enum {
   MOE_ERR_CUDA = 7,          /* a CUDA runtime call failed */
   MOE_ERR_CAPACITY = 8,      /* a rank would receive more than A rows */
   MOE_ERR_BAD_ASSIST = 9,    /* assist_info / ep_recv_count do not match the routing */
+  MOE_ERR_OUT_OF_BOUNDS = 10, /* bounds-checked builds only (-DMOE_BOUNDS_CHECK): a kernel
+                                computed an index outside its buffer and skipped the access */
 } moe_status_t;
 
 typedef enum { MOE_I32 = 0, MOE_F16 = 1, MOE_BF16 = 2 } moe_dtype_t;

@@ -103,8 +103,8 @@ def test_quant_with_int32_is_rejected(lib):
 
 
 def test_status_strings(lib):
-    for code in range(10):
-        assert lib.status_string(code)
+    for code in range(11):
+        assert lib.status_string(code) != "unknown status"
 
 
 def test_binding_refuses_cpu_tensors(lib):
