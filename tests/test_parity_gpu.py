@@ -162,7 +162,8 @@ def test_one_expert_takes_everything():
 
 
 @pytest.mark.parametrize("W,E,bs,K,h", [(64, 1024, 16, 8, 64), (768, 768, 2, 1, 16), (32, 256, 40, 16, 128),
-                                        (8, 1024, 16, 8, 64), (16, 512, 8, 4, 32), (4, 64, 300, 4, 128)])
+                                        (8, 1024, 16, 8, 64), (16, 512, 8, 4, 32), (4, 64, 300, 4, 128),
+                                        (8, 256, 12, 32, 64), (2, 64, 9, 32, 256)])
 def test_wide_configurations(W, E, bs, K, h):
     wl = WL.Workload(f"wide_w{W}", W, bs, h, K, E, WL.X_BF16, zero_expert_num=2, copy_expert_num=2,
                      mask_kind=1, special_p=0.1, seed=W)

@@ -158,3 +158,14 @@ def test_quant_random_shapes(seed):
                      quant_mode=q, y_dtype=y, scales_kind=k, seed=int(rng.integers(0, 2**31)))
     policy = [M.PLANE_RULE, M.PLANE_STORES_ONLY, M.PLANE_BULK_ALL][int(rng.integers(0, 3))]
     run(wl, plane_policy=policy, bulk_min_bytes=0 if policy == M.PLANE_RULE else None)
+
+
+@pytest.mark.parametrize("mode", [(2, "", 3), (3, "fp8_e5m2", 3), (4, "fp4_e2m1", 0), (1, "", 2)], ids=mode_id)
+def test_quant_top32(mode):
+    """The largest top-k: 32 picks per token, a variant per pick with
+    per-expert scales, every plane policy."""
+    q, y, k = mode
+    wl = WL.Workload("qk32", 4, 12, 512, 32, 64, WL.X_BF16, mask_kind=2, mask_false_p=0.1, quant_mode=q,
+                     y_dtype=y, scales_kind=k, seed=51)
+    for policy in (M.PLANE_RULE, M.PLANE_BULK_ALL):
+        run(wl, plane_policy=policy, bulk_min_bytes=0)
