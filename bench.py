@@ -886,6 +886,9 @@ def run_ours(args):
         "graph_ms_per_step": graph_ms,
         "scatter_GBps": acct["scatter"] / (scatter_ms * 1e-3) / 1e9,
         "combine_reduce_GBps": acct["reduce"] / (reduce_ms * 1e-3) / 1e9 if reduce_ms else None,
+        "scatter_frac_of_measured_hbm": acct["scatter"] / (scatter_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
+        "combine_reduce_frac_of_measured_hbm": (acct["reduce"] / (reduce_ms * 1e-3) / 1e9 / peaks["hbm_gbs"]
+                                                if reduce_ms else None),
         "roofline": {"kernel": dom, "bound": "hbm", "achieved": achieved, "peak": peaks["hbm_gbs"], "unit": "GB/s",
                      "frac": achieved / peaks["hbm_gbs"], "traffic": traffic,
                      "algorithmic_bytes": dom_bytes, "peak_source": peaks["source"] + " copy bandwidth"},
