@@ -32,7 +32,7 @@ namespace crs {
 
 constexpr int kTpThreads = 256;
 constexpr int kTpWarps = kTpThreads / 32;
-constexpr int kTpSlot = 8192;  // bytes per staging slot of the bulk plane
+constexpr int kTpSlot = 2048;  // small slots: 32 KB of ring a CTA, four CTAs (32 warps) an SM  // bytes per staging slot of the bulk plane
 constexpr int kTpVpl = 4;      // 16-byte vectors per lane per reduce item
 
 __device__ __forceinline__ int4 ld_v4(const void* p) {
@@ -84,7 +84,7 @@ __device__ __forceinline__ long long seg_rows(const int32_t* ep, int d, int LW, 
 }
 
 template <int DT>
-__global__ void __launch_bounds__(kTpThreads, 1) two_phase_kernel(CombineParams p) {
+__global__ void __launch_bounds__(kTpThreads, 4) two_phase_kernel(CombineParams p) {
   extern __shared__ __align__(128) uint8_t tsm[];
   __shared__ __align__(8) uint64_t bars[kTpWarps][2];
   __shared__ const uint8_t* s_src[kTpWarps][32];
