@@ -361,8 +361,10 @@ template <int MODE>
 static cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
                                const FfnParams& p, cudaStream_t st, int num_sms) {
   auto kern = ffn_gemm_kernel<MODE>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kFfnSmem);
+  int per_sm = 0;  // one CTA per SM by design; the call raises the shared-memory limit once
+  const cudaError_t e = resident_blocks((const void*)kern, kFfnThreads, kFfnSmem, &per_sm);
   if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int units = p.E * p.tiles;
   const int grid = units < num_sms ? units : num_sms;
   if (grid <= 0) return cudaSuccess;

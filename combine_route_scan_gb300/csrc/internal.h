@@ -147,6 +147,12 @@ struct FfnLaunch {
   uint64_t timeout_ns;
 };
 
+// CTAs of `kernel` resident per SM with `threads` threads and `smem` bytes of
+// dynamic shared memory on the current device, after raising the kernel's
+// dynamic shared-memory limit to `smem`. Both steps are host calls of a few
+// microseconds; the answer is cached per (device, kernel, threads, smem).
+cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* per_sm);
+
 // True when the TMA scatter's shared-memory ring fits for this shape.
 bool scatter_tma_fits(const Shape& sh);
 // The quantising scatter (every quant_mode but 0) and its fit test.

@@ -5,7 +5,60 @@
 // dependent launch.
 #include <string.h>
 
+#include <mutex>
+
 #include "internal.h"
+
+namespace crs {
+
+cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* per_sm) {
+  // The dynamic shared-memory limit is state of the kernel, not of one call:
+  // it is only ever raised (to the largest size asked for so far), so a call
+  // with a smaller size never lowers it under a later, larger one.
+  struct Limit {
+    const void* kernel;
+    int dev;
+    size_t smem;
+  };
+  struct Occupancy {
+    const void* kernel;
+    int dev, threads;
+    size_t smem;
+    int per_sm;
+  };
+  static Limit limits[128];
+  static Occupancy occ[256];
+  static int n_limits = 0, n_occ = 0;
+  static std::mutex mu;
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  std::lock_guard<std::mutex> lock(mu);
+  Limit* lim = nullptr;
+  for (int i = 0; i < n_limits; ++i)
+    if (limits[i].kernel == kernel && limits[i].dev == dev) lim = &limits[i];
+  if (!lim || lim->smem < smem) {
+    e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
+    if (e != cudaSuccess) return e;
+    if (lim) lim->smem = smem;
+    else if (n_limits < 128) limits[n_limits++] = Limit{kernel, dev, smem};
+  }
+  for (int i = 0; i < n_occ; ++i) {
+    const Occupancy& t = occ[i];
+    if (t.kernel == kernel && t.dev == dev && t.threads == threads && t.smem == smem) {
+      *per_sm = t.per_sm;
+      return cudaSuccess;
+    }
+  }
+  int n = 0;
+  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&n, kernel, threads, smem);
+  if (e != cudaSuccess) return e;
+  if (n_occ < 256) occ[n_occ++] = Occupancy{kernel, dev, threads, smem, n};
+  *per_sm = n;
+  return cudaSuccess;
+}
+
+}  // namespace crs
 
 using namespace crs;
 

@@ -206,10 +206,8 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_plain_kernel(ScatterP
 template <typename KernelT>
 static cudaError_t launch_persistent(KernelT kernel, const ScatterParams& p, cudaStream_t st, int num_sms,
                                      size_t smem) {
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScatterThreads, smem);
+  const cudaError_t e = resident_blocks((const void*)kernel, kScatterThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int n_tok = p.sh.W * p.sh.bs;

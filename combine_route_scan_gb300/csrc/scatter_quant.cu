@@ -582,10 +582,8 @@ bool scatter_quant_tma_fits(const Shape& sh) { return quant_smem(sh) <= 200 * 10
 template <typename KernelT>
 static cudaError_t launch_quant_persistent(KernelT kernel, const ScatterParams& p, cudaStream_t st, int num_sms) {
   const size_t smem = quant_smem(p.sh);
-  cudaError_t e = cudaFuncSetAttribute(kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kernel, kScatterThreads, smem);
+  const cudaError_t e = resident_blocks((const void*)kernel, kScatterThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int n_tok = p.sh.W * p.sh.bs;

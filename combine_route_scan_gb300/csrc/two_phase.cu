@@ -343,10 +343,8 @@ cudaError_t launch_combine_two_phase(const CombineParams& p, cudaStream_t st, in
   void (*kern)(CombineParams) = sh.x_dtype == MOE_I32   ? two_phase_kernel<MOE_I32>
                                 : sh.x_dtype == MOE_F16 ? two_phase_kernel<MOE_F16>
                                                         : two_phase_kernel<MOE_BF16>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem);
-  if (e != cudaSuccess) return e;
   int per_sm = 0;
-  e = cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kTpThreads, smem);
+  const cudaError_t e = resident_blocks((const void*)kern, kTpThreads, smem, &per_sm);
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   // rows per warp batch: up to 32 (one per lane), fewer when the call has

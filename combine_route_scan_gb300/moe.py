@@ -103,13 +103,14 @@ def lib() -> ctypes.CDLL:
 
 
 def _ptr(t: Optional[torch.Tensor]):
+    """The tensor's device address as an int (ctypes passes it as void*)."""
     if t is None:
         return None
     if not t.is_cuda:
         raise ValueError("expected a CUDA tensor")
     if not t.is_contiguous():
         raise ValueError("expected a contiguous tensor")
-    return ctypes.c_void_p(t.data_ptr())
+    return t.data_ptr()
 
 
 def _stream(stream) -> ctypes.c_void_p:
@@ -149,7 +150,7 @@ def with_seg_ready(cfg: MoeConfig, seg_ready: torch.Tensor, ticket: int) -> MoeC
     """A copy of cfg whose dispatch stores `ticket` into seg_ready[d][le*W+s]
     once segment (le, s) of rank d is complete (uint32 CUDA tensor [W, L*W])."""
     c = MoeConfig.from_buffer_copy(cfg)
-    c.seg_ready = ctypes.c_void_p(_ptr(seg_ready).value)
+    c.seg_ready = _ptr(seg_ready)
     c.seg_ready_ticket = ticket
     return c
 
@@ -158,7 +159,7 @@ def with_performance_info(cfg: MoeConfig, perf: torch.Tensor) -> MoeConfig:
     """A copy of cfg whose dispatch adds each rank's communication time (ns)
     to perf (int64 CUDA tensor [W])."""
     c = MoeConfig.from_buffer_copy(cfg)
-    c.performance_info = ctypes.c_void_p(_ptr(perf).value)
+    c.performance_info = _ptr(perf)
     return c
 
 
