@@ -444,3 +444,16 @@ def test_row_map_follows_the_buffers():
     got_b2["assist_info"][d, 0, 1] = (got_b2["assist_info"][d, 0, 1] + 1) % wl.bs
     _, st = _combine_same_ws(wl, dev_b, got_b2, ws2)
     assert M.STATUS[st] == "BAD_ASSIST"
+
+
+def test_launch_limits_survive_smaller_shapes():
+    """A kernel's dynamic shared-memory limit only ever rises: a large row
+    shape, then a small one, then the large one again all launch and match."""
+    for h in (7168, 256, 7168, 1024):
+        wl = WL.Workload(f"lim_h{h}", 4, 8, h, 4, 16, WL.X_BF16, seed=61)
+        run_and_compare(wl)
+        wq = wl.with_(quant_mode=3, y_dtype="fp8_e4m3")
+        inp = WL.make_inputs(wq)
+        ref = O.dispatch(wq, inp)
+        got, _, _ = H.gpu_dispatch(wq, H.device_inputs(wq, inp))
+        H.compare_dispatch(wq, got, ref)
