@@ -267,6 +267,16 @@ def whole_job_gbps(step_bytes: int, steps: int, max_ms: float, world: int) -> fl
     return world * step_bytes * steps / (max_ms * 1e-3) / 1e9
 
 
+def bench_config(wl: WL.Workload, args, step_bytes: int) -> dict:
+    """The `config` object of the JSON line, the same for both arms."""
+    return {"workload": wl.name, "ep_world_size": wl.ep_world_size, "bs": wl.bs, "h": wl.h,
+            "topk": wl.topk, "moe_expert_num": wl.moe_expert_num, "zero_experts": wl.zero_expert_num,
+            "copy_experts": wl.copy_expert_num, "mask": wl.mask_kind, "quant_mode": wl.quant_mode,
+            "plane_policy": getattr(args, "plane_policy", 0), "combine": "gather",
+            "l2": f"no flush: one step moves {step_bytes / 1e6:.0f} MB (> {L2_BYTES >> 20} MiB L2)",
+            "accumulate": "fp32"}
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
@@ -296,12 +306,14 @@ def run_reference(args):
     total = sum(times)
     gbps = (b["dispatch"] + b["combine"]) * len(times) / total / 1e9
     sample = (f"{len(times)} timed oracle steps of dispatch+combine over "
-              + ("the full batch" if bs == wl.bs else f"the first {bs} of {wl.bs} tokens of every rank"))
+              + ("the full batch" if bs == wl.bs else f"the first {bs} of {wl.bs} tokens of every rank")
+              + ", single-threaded C")
+    full = algorithmic_bytes(wl, inp)
     line = {
         "impl": "reference", "metric": METRIC, "value": gbps, "unit": "GB/s", "n_gpus": args.gpus,
         "steps": args.steps, "warmup": args.warmup, "ms_per_step": total / len(times) * 1e3,
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
-        "config": {"workload": wl.name, "sample_bs": bs},
+        "config": bench_config(wl, args, full["dispatch"] + full["combine"]),
         "tokens_per_s": swl.ep_world_size * swl.bs * len(times) / total,
         "cpu_baseline": {"value": gbps, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
         "e2e": {"value": gbps, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
@@ -872,12 +884,7 @@ def run_ours(args):
         "ms_per_step": step_ms, "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
         "dtype": "bf16" if wl.x_dtype == WL.X_BF16 else ("fp16" if wl.x_dtype == WL.X_FP16 else "int32"),
         "data": "synthetic",
-        "config": {"workload": wl.name, "ep_world_size": wl.ep_world_size, "bs": wl.bs, "h": wl.h,
-                   "topk": wl.topk, "moe_expert_num": wl.moe_expert_num, "zero_experts": wl.zero_expert_num,
-                   "copy_experts": wl.copy_expert_num, "mask": wl.mask_kind, "quant_mode": wl.quant_mode,
-                   "plane_policy": args.plane_policy, "combine": "gather",
-                   "l2": f"no flush: one step moves {step_bytes / 1e6:.0f} MB (> {L2_BYTES >> 20} MiB L2)",
-                   "accumulate": "fp32"},
+        "config": bench_config(wl, args, step_bytes),
         "tokens_per_s": tokens * K / (total_ms * 1e-3),
         "frac_of_8TBps": value / world / HBM_NOMINAL_GBPS,
         "dispatch_bytes": acct["dispatch"], "combine_bytes": acct["combine"], "routed_picks": acct["P"],
