@@ -603,6 +603,23 @@ def pin_quant_static_hand():
             assert q.view(np.int8).tolist() == case["q"], (case["name"], dt, q.view(np.int8).tolist())
 
 
+def pin_quant_mx_group_hand():
+    g = golden("quant_mx_group_hand.json")
+    for case in g["cases"]:
+        for dt in ("float16", "bfloat16"):
+            x = np.zeros(case["h"], dtype=np.float32)
+            x[:len(case["x"])] = case["x"]
+            row = x.astype(np.float16) if dt == "float16" else WL.fp32_to_bf16_bits(x)
+            q, dyn = O.quantize_pick(row, case["mode"], dt, case["y"])
+            want = [int(b, 16) for b in case["q_hex"].split()]
+            assert q[:len(want)].tolist() == want, (case["name"], dt, q[:len(want)].tolist())
+            assert not q[len(want):].any(), (case["name"], dt)
+            if "dyn" in case:
+                assert dyn.tolist() == case["dyn"], (case["name"], dt)
+            else:
+                assert [f32_bits(float(v)) for v in dyn] == [int(b, 16) for b in case["dyn_bits"]], (case["name"], dt)
+
+
 def pin_quant_smooth_reduces(seed: int = 17):
     """Per-expert smoothing weights that are powers of two make x * s exact in
     bf16: quantMode 2 / 3 with smoothing for expert e must equal the plain
@@ -748,6 +765,7 @@ def run_all():
     pin_quant_exact()
     pin_minifloat_bruteforce(n=300)
     pin_quant_static_hand()
+    pin_quant_mx_group_hand()
     pin_quant_smooth_reduces()
     pin_quant_group_exact()
     pin_quant_mx_exact()

@@ -124,3 +124,7 @@ def test_mx_quant_exact():
 
 def test_quant_modes_through_dispatch():
     P.pin_quant_modes_dispatch()
+
+
+def test_mx_and_group_hand_fixture():
+    P.pin_quant_mx_group_hand()
