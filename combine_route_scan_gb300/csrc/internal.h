@@ -21,7 +21,8 @@ struct WsHeader {
   uint32_t inv_valid;                 // the inv region holds the pick -> row map of the last dispatch ...
   unsigned long long inv_assist;      // ... whose assist_info and ep_recv_count were these buffers
   unsigned long long inv_ep;
-  uint32_t pad[52];
+  uint32_t scatter_next;  // TMA scatter: next token ticket (zeroed by the routing kernel)
+  uint32_t pad[51];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 

@@ -78,11 +78,6 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   pdl_wait();
   pdl_launch_dependents();
 
-  if (s == 0 && tid == 0 && p.hdr) {  // the scatter that follows writes the pick -> row map
-    p.hdr->inv_assist = (unsigned long long)(uintptr_t)p.assist_out;
-    p.hdr->inv_ep = (unsigned long long)(uintptr_t)p.ep_recv_count;
-    p.hdr->inv_valid = 1u;
-  }
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;
   if (sh.mask_kind == 1) {
     const uint8_t* m = p.mask + (size_t)s * sh.bs;
@@ -280,6 +275,16 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
     __syncwarp();
     if (valid) keys[(size_t)t * K + k] = r;
+  }
+
+  // the scatter that follows writes the pick -> row map and hands out tokens
+  // by ticket; these stores come after every release of this CTA, so no
+  // barrier waits for them
+  if (s == 0 && tid == 0 && p.hdr) {
+    p.hdr->inv_assist = (unsigned long long)(uintptr_t)p.assist_out;
+    p.hdr->inv_ep = (unsigned long long)(uintptr_t)p.ep_recv_count;
+    p.hdr->inv_valid = 1u;
+    p.hdr->scatter_next = 0u;
   }
 
   if constexpr (CLUSTER) {

@@ -4,7 +4,8 @@
 // plain SM stores for local, small or average segments, TMA bulk copies for
 // large remote ones. (The quantised modes run in scatter_quant.cu.)
 //
-// Token-major and persistent: each CTA walks tokens blockIdx.x, +grid, ...
+// Token-major and persistent: each CTA starts with tokens blockIdx.x, +grid,
+// ... and then takes tokens from a shared ticket counter until none is left.
 // A ring of STAGES shared-memory slots is filled by TMA bulk loads
 // (cp.async.bulk global->shared, completion on an mbarrier), so every source
 // row is read from HBM exactly once however many ranks it goes to. For each
@@ -46,10 +47,26 @@ __device__ __forceinline__ void publish_earlier(const ScatterParams& p, const Pi
   }
 }
 
+// Thread 0 fills a ring slot with token `tau`: records the token, then either
+// starts the TMA load of its row or, with tau < 0 (no token left), completes
+// the slot's barrier phase by a plain arrival. Either way the barrier phase
+// publishes s_tok[slot] to the threads that wait on it.
+__device__ __forceinline__ void fill_slot(uint64_t* bar, int* s_tok, uint8_t* dst, const uint8_t* x, int tau,
+                                          uint32_t row_in) {
+  *s_tok = tau;
+  if (tau >= 0) {
+    mbar_arrive_expect_tx(bar, row_in);
+    bulk_g2s(dst, x + (size_t)tau * row_in, row_in, bar);
+  } else {
+    mbar_arrive(bar);
+  }
+}
+
 template <int STAGES>
 __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
+  __shared__ int s_tok[STAGES];  // token held by each slot, -1 once the tokens ran out
   __shared__ PickTable tabs[3];
   __shared__ int s_abort;
 
@@ -57,7 +74,6 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n_tok = sh.W * sh.bs;
   const int G = gridDim.x;
-  const int my_n = blockIdx.x < n_tok ? (n_tok - 1 - (int)blockIdx.x) / G + 1 : 0;
   const uint32_t row_in = (uint32_t)sh.row_in, row_out = (uint32_t)sh.row_out;
   const size_t slot_in = align128(row_in);
   uint8_t* xin = smem;                         // [STAGES][slot_in]
@@ -70,48 +86,60 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     s_abort = 0;
   }
   __syncthreads();
-  // Prefetch the first rows. x is never written by the routing kernel, and the
-  // routing kernel lets this grid start only after its own predecessor ended.
+  // Token hand-out (thread 0): the CTA's first STAGES tokens are blockIdx.x +
+  // i*G, prefetched before the routing ends (x is never written by the routing
+  // kernel, which lets this grid start only after its own predecessor ended);
+  // every later one is STAGES*G + a ticket from a counter shared by all CTAs,
+  // so CTAs that finish early take more tokens and the grid ends together.
+  bool exhausted = false;  // thread 0: a slot got -1, no further fills
   if (tid == 0) {
-    for (int i = 0; i < STAGES && i < my_n; ++i) {
-      const size_t tau = blockIdx.x + (size_t)i * G;
-      mbar_arrive_expect_tx(&full_bar[i], row_in);
-      bulk_g2s(xin + i * slot_in, x + tau * row_in, row_in, &full_bar[i]);
+    for (int i = 0; i < STAGES && !exhausted; ++i) {
+      const long long tau = blockIdx.x + (long long)i * G;
+      exhausted = tau >= n_tok;
+      fill_slot(&full_bar[i], &s_tok[i], xin + i * slot_in, x, exhausted ? -1 : (int)tau, row_in);
     }
   }
-  pdl_wait();  // routing results are visible from here on
+  pdl_wait();  // routing results (and the zeroed ticket counter) are visible from here on
   pdl_launch_dependents();
   if (p.perf && tid == 0) perf_begin(p);
+  // thread 0 claims each ticket one token ahead of its use, so the atomic's
+  // latency overlaps a token's stores
+  unsigned ticket = 0;
+  if (tid == 0 && !exhausted) ticket = atomicAdd(&p.hdr->scatter_next, 1u);
+  int prev_tau = -1;  // thread 0: last token handled (performance info)
 
-  for (int i = 0; i < my_n; ++i) {
-    const size_t tau = blockIdx.x + (size_t)i * G;
-    const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
+  int n_done = 0;
+  for (int i = 0;; ++i) {
     const int stage = i % STAGES;
     const uint32_t parity = (uint32_t)(i / STAGES) & 1u;
     PickTable& tab = tabs[i % 3];
     const uint8_t* row = xin + stage * slot_in;
 
-    bool ok = mbar_wait_bounded(&full_bar[stage], parity, p.status, p.timeout_ns);
+    const bool ok = mbar_wait_bounded(&full_bar[stage], parity, p.status, p.timeout_ns);
     if (!ok) s_abort = 1;
-
-    if (warp == 0) build_picks(p, tau, s, t, tab);
+    if (warp == 0) {
+      const int tw = s_tok[stage];
+      if (tw >= 0) build_picks(p, (size_t)tw, tw / sh.bs, tw % sh.bs, tab);
+    }
     __syncthreads();
-    if (s_abort) break;
+    const int tau = s_tok[stage];
+    if (tau < 0 || s_abort) break;
     if (p.seg_ready && warp == 0) publish_earlier(p, tabs, i);
-    if (p.perf && tid == 0 && i >= 1) perf_mark(p, tau - G);
+    if (p.perf && tid == 0 && i >= 1) perf_mark(p, (size_t)prev_tau);
     const int nb = tab.n_bulk, ns = tab.n_sm;
     if (tid == 0) {
       // refill the slot of the previous token once its bulk group has read it
-      const int nxt = i - 1 + STAGES;
-      if (i >= 1 && nxt < my_n) {
+      if (i >= 1 && !exhausted) {
         bulk_wait_read<0>();
         const int ps = (i - 1) % STAGES;
-        const size_t tn = blockIdx.x + (size_t)nxt * G;
-        mbar_arrive_expect_tx(&full_bar[ps], row_in);
-        bulk_g2s(xin + ps * slot_in, x + tn * row_in, row_in, &full_bar[ps]);
+        const long long tn = (long long)STAGES * G + ticket;
+        exhausted = tn >= n_tok;
+        fill_slot(&full_bar[ps], &s_tok[ps], xin + ps * slot_in, x, exhausted ? -1 : (int)tn, row_in);
+        if (!exhausted) ticket = atomicAdd(&p.hdr->scatter_next, 1u);
       }
       for (int j = 0; j < nb; ++j) bulk_s2g(out + tab.bulk_dst[j] * row_out, row, row_out);
       bulk_commit();
+      prev_tau = tau;
     }
     if (ns > 0) {
       for (uint32_t v = tid; v < row_in / 16; v += kScatterThreads) {
@@ -119,6 +147,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
         for (int j = 0; j < ns; ++j) st_v4(out + tab.sm_dst[j] * row_out + v * 16, val);
       }
     }
+    ++n_done;
   }
   // all bulk stores of this CTA complete before it exits
   if (p.seg_ready) {
@@ -129,7 +158,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
         fence_proxy_async_global();
       }
       __syncwarp();
-      const int last = my_n - 1;
+      const int last = n_done - 1;
       if (last >= 0) {
         const PickTable& a = tabs[last % 3];
         publish_rows_warp(p, a.sm_seg, a.n_sm);
@@ -143,7 +172,7 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
   }
   if (tid == 0) bulk_wait_all<0>();
   if (p.perf) {
-    if (tid == 0 && my_n > 0 && !s_abort) perf_mark(p, blockIdx.x + (size_t)(my_n - 1) * G);
+    if (tid == 0 && n_done > 0 && !s_abort) perf_mark(p, (size_t)prev_tau);
     __shared__ int s_last;
     perf_finish(p, &s_last);
   }
