@@ -99,6 +99,7 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   // together, and the keys stay in registers for walk 2.
   const bool in_regs = per_warp <= kRegIters;
   int keyr[kRegIters];
+  int locr[kRegIters];  // position among the warp's earlier picks of the same expert
   if (in_regs) {
     int raw[kRegIters];
     bool act[kRegIters];
@@ -114,6 +115,7 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     for (int j = 0; j < kRegIters; ++j) {
       if (it0 + j >= it1) {
         keyr[j] = -1;
+        locr[j] = -1;
         continue;
       }
       int key = -1;
@@ -133,9 +135,18 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
         key = -1;
       }
       keyr[j] = key;
+      // the group leader bumps the warp's counter for this expert and hands
+      // the old value to its group, so walk 2 needs no second match
       const uint32_t peers = __match_any_sync(0xffffffffu, key);
-      if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
-      __syncwarp();
+      const int leader = __ffs(peers) - 1;
+      int before = 0;
+      if (key >= 0 && lane == leader) {
+        before = wcnt[warp * E + key];
+        wcnt[warp * E + key] = before + __popc(peers);
+      }
+      __syncwarp();  // the next iteration's leaders read what this one wrote
+      before = __shfl_sync(0xffffffffu, before, leader);
+      locr[j] = key >= 0 ? before + __popc(peers & lanemask_lt()) : -1;
     }
   } else {
     for (int it = it0; it < it1; ++it) {
@@ -260,20 +271,25 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     if (it >= it1) break;
     const int t = it * G + tl;
     const bool valid = tl < G && t < sh.bs;
-    int key = -1;
+    int r = -1;
     if (in_regs) {
+      // wcnt now holds each expert's count over earlier warps
+      int key = -1, loc = -1;
 #pragma unroll
       for (int q = 0; q < kRegIters; ++q)
-        if (q == j) key = keyr[q];
-    } else if (valid) {
-      key = keys[(size_t)t * K + k];
+        if (q == j) {
+          key = keyr[q];
+          loc = locr[q];
+        }
+      if (key >= 0) r = wcnt[warp * E + key] + loc;
+    } else {
+      const int key = valid ? keys[(size_t)t * K + k] : -1;
+      const uint32_t peers = __match_any_sync(0xffffffffu, key);
+      if (key >= 0) r = wcnt[warp * E + key] + __popc(peers & lanemask_lt());
+      __syncwarp();
+      if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
+      __syncwarp();
     }
-    const uint32_t peers = __match_any_sync(0xffffffffu, key);
-    int r = -1;
-    if (key >= 0) r = wcnt[warp * E + key] + __popc(peers & lanemask_lt());
-    __syncwarp();
-    if (key >= 0 && lane == __ffs(peers) - 1) wcnt[warp * E + key] += __popc(peers);
-    __syncwarp();
     if (valid) keys[(size_t)t * K + k] = r;
   }
 
