@@ -438,6 +438,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   sp.plane = rp.plane;
   sp.sh = sh;
   sp.status = &hdr->status;
+  sp.hdr = hdr;
   sp.timeout_ns = timeout_ns(cfg);
   if (!empty && launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
   if (empty) return MOE_OK;

@@ -255,6 +255,7 @@ bool scatter_tma_fits(const Shape& sh) { return scatter_smem(sh, 2) <= 200 * 102
 cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t st, int num_sms, bool tma) {
   const Shape& sh = p.sh;
   if (sh.W * sh.bs == 0) return cudaSuccess;
+  if (p.hdr == nullptr) return cudaErrorInvalidValue;  // the token tickets live in the workspace header
   if (!tma) {
     const int grid = max(1, min(sh.W * sh.bs, num_sms * 4));
     PdlLaunch L(dim3(grid), dim3(kScatterThreads), 0, st);

@@ -71,6 +71,16 @@ def test_ffn_decode_layer_sampled_tokens():
     check(wl, inp, tokens)
 
 
+def test_ffn_many_tokens_per_scatter_cta():
+    """More tokens than the dispatch scatter's resident CTAs hold in their
+    rings, so most tokens are handed out by the workspace ticket counter."""
+    wl = WL.Workload("ffn_many", 8, 1024, 256, 2, 16, WL.X_BF16, ffn_intermediate=128, seed=24)
+    inp = WL.make_inputs(wl)
+    rng = np.random.default_rng(1)
+    tokens = np.sort(rng.choice(wl.ep_world_size * wl.bs, size=64, replace=False))
+    check(wl, inp, tokens)
+
+
 def test_ffn_deterministic():
     wl = WL.Workload("ffn_det", 4, 32, 512, 4, 16, WL.X_BF16, ffn_intermediate=256, seed=23)
     inp = WL.make_inputs(wl)
