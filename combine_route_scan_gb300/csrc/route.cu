@@ -23,21 +23,17 @@
 //
 // The per-rank scan of the W*L*W segment counts into ep_recv_count (inclusive)
 // and segment offsets (exclusive) then takes one of two forms:
-//   * W <= 16: the W CTAs run as one thread-block cluster. Each thread arrives
-//     at a split cluster barrier (release) as soon as its totals are in shared
-//     memory, does its global stores, then waits; CTA d then reads the counts
-//     of segment (le, s) of rank d once from CTA s's shared memory
-//     (distributed shared memory), arrives at a second barrier that only
-//     guards those reads, and scans rank d's L*W segments: all ranks in
-//     parallel, no global fence, no atomic. The second wait sits at the very
-//     end, so no CTA exits while another may still read its counts.
+//   * W <= 16: the W CTAs run as one thread-block cluster. Each CTA sets up a
+//     receive barrier (an mbarrier expecting L*W counts) and arrives at a
+//     cluster barrier before anything else; once its totals are known, CTA s
+//     pushes the count of segment (le, s) into CTA d's shared memory with
+//     st.async, whose completion is counted in bytes on CTA d's receive
+//     barrier. CTA d waits for its L*W counts and scans rank d's segments: all
+//     ranks in parallel, no fence, no global atomic. A last cluster barrier at
+//     the very end keeps every CTA alive until all pushes have landed.
 //   * otherwise: the last CTA to finish (completion counter in the workspace)
 //     scans all counts, tile by tile through shared memory.
-#include <cooperative_groups.h>
-
 #include "common.cuh"
-
-namespace cg = cooperative_groups;
 
 namespace crs {
 
@@ -57,13 +53,53 @@ __device__ __forceinline__ void cluster_wait_acquire() {
   asm volatile("barrier.cluster.wait.acquire.aligned;" ::: "memory");
 }
 
+// Address of the same shared-memory location in CTA `rank` of the cluster.
+__device__ __forceinline__ uint32_t cluster_map(const void* local, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(smem_u32(local)), "r"(rank));
+  return r;
+}
+// 4-byte store into another CTA's shared memory; its completion is counted
+// (4 bytes) on that CTA's mbarrier `bar` (both cluster addresses).
+__device__ __forceinline__ void st_async_u32(uint32_t addr, uint32_t v, uint32_t bar) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.u32 [%0], %1, [%2];" ::"r"(addr), "r"(v),
+               "r"(bar)
+               : "memory");
+}
+// Bounded wait on a phase of this CTA's mbarrier whose bytes other CTAs of the
+// cluster deliver (acquire at cluster scope).
+__device__ __forceinline__ bool mbar_wait_cluster(uint64_t* bar, uint32_t parity, int* status, uint64_t limit_ns) {
+  uint64_t t0 = 0;
+  for (uint32_t it = 0;; ++it) {
+    uint32_t ok;
+    asm volatile(
+        "{\n\t.reg .pred p;\n\t"
+        "mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n\t"
+        "selp.u32 %0, 1, 0, p;\n\t}"
+        : "=r"(ok)
+        : "r"(smem_u32(bar)), "r"(parity)
+        : "memory");
+    if (ok) return true;
+    if (it == 0) t0 = globaltimer_ns();
+    else if ((it & 63u) == 63u && globaltimer_ns() - t0 > limit_ns) {
+      set_error(status, MOE_ERR_TIMEOUT);
+      return false;
+    }
+  }
+}
+
+constexpr uint64_t kExchangeTimeoutNs = 2000000000ull;  // bound on the count exchange (never reached when healthy)
+
 // THREADS: 256 for sources with at most 1024 picks (every warp then has at most
 // kRegIters iterations and barriers are short), else 1024.
 template <bool CLUSTER, int THREADS>
 __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   constexpr int kRouteThreads = THREADS;
   constexpr int kRouteWarps = THREADS / 32;
-  extern __shared__ __align__(16) int32_t rsm[];  // wcnt [kRouteWarps][E], tot [E]; later the scan tiles
+  // wcnt [kRouteWarps][E], tot [E], recv [E] (cluster form: the L*W counts
+  // this rank receives, index le*W + s); later the scan tiles
+  extern __shared__ __align__(16) int32_t rsm[];
+  __shared__ __align__(8) uint64_t recv_bar;
   __shared__ long long s_scan[32];
   __shared__ long long s_total;
   __shared__ int s_last;
@@ -74,7 +110,18 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   const int G = 32 / K;  // whole tokens per warp iteration
   int32_t* wcnt = rsm;
   int32_t* tot = rsm + kRouteWarps * E;
+  int32_t* recv = tot + E;
 
+  if constexpr (CLUSTER) {
+    // the receive barrier expects one 4-byte count per (le, s) segment; every
+    // CTA's barrier is set up before any CTA passes the first cluster wait
+    if (tid == 0) {
+      mbar_init(&recv_bar, 1);
+      mbar_fence_init();
+      mbar_arrive_expect_tx(&recv_bar, (uint32_t)E * 4u);
+    }
+    cluster_arrive_relaxed();
+  }
   pdl_wait();
   pdl_launch_dependents();
 
@@ -187,10 +234,16 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     tot[e] = run;
     if (e / sh.L != s) remote += run;
   }
-  // cluster form: this thread's totals are released to the other CTAs now; the
-  // global stores below come after the arrive, so the barrier does not wait
-  // for them
-  if constexpr (CLUSTER) cluster_arrive_release();
+  // cluster form: push each total to the rank that receives the segment
+  // (e = d*L + le goes to CTA d, slot le*W + s); this thread wrote tot[e]
+  if constexpr (CLUSTER) {
+    cluster_wait_acquire();  // every receive barrier is set up
+    for (int e = tid; e < E; e += kRouteThreads) {
+      const int d = e / sh.L, le = e - d * sh.L;
+      st_async_u32(cluster_map(recv + le * sh.W + s, (uint32_t)d), (uint32_t)tot[e],
+                   cluster_map(&recv_bar, (uint32_t)d));
+    }
+  }
   {
     const long long ex = block_exclusive_scan(remote, s_scan);
     if (tid == kRouteThreads - 1) s_total = ex + remote;
@@ -225,11 +278,11 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   }
 
   if constexpr (CLUSTER) {
-    // every CTA's totals are visible once the wait passes; CTA s then scans
-    // the L*W segments (le, s') of receiving rank d = s (L*W = E <= 1024),
-    // reading each count once from CTA s''s shared memory
-    cluster_wait_acquire();
-    cg::cluster_group cluster = cg::this_cluster();
+    // CTA s scans the L*W segments (le, s') of receiving rank d = s
+    // (L*W = E <= 1024) once all of their counts have landed
+    mbar_wait_cluster(&recv_bar, 0, p.status, kExchangeTimeoutNs);
+    // all pushes into this CTA are done; the matching wait is at the very end
+    cluster_arrive_relaxed();
     const int d = s, LW = sh.L * sh.W;
     constexpr int kPer = (kRouteThreadsMax + kRouteThreads - 1) / kRouteThreads;
     // thread tid owns the contiguous segments [j0, j1) of rank d (at most kPer)
@@ -241,14 +294,9 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     for (int q = 0; q < kPer; ++q) {
       const int j = j0 + q;
       cv[q] = 0;
-      if (j < j1) {
-        const int le = j / sh.W, sp = j - le * sh.W;
-        cv[q] = cluster.map_shared_rank(tot, sp)[d * sh.L + le];
-      }
+      if (j < j1) cv[q] = recv[j];
       local += cv[q];
     }
-    // done reading other CTAs' memory; the matching wait is at the very end
-    cluster_arrive_relaxed();
     long long run = block_exclusive_scan(local, s_scan);
 #pragma unroll
     for (int q = 0; q < kPer; ++q) {
@@ -304,7 +352,7 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   }
 
   if constexpr (CLUSTER) {
-    cluster_wait_acquire();  // no CTA leaves while others may still read its counts
+    cluster_wait_acquire();  // no CTA leaves while pushes into another may be in flight
     return;
   }
 
@@ -357,8 +405,11 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
   if (tid == 0) *p.done = 0;  // ready for the next call (stream order)
 }
 
+// Dynamic shared memory of the walks: wcnt [threads/32][E], tot [E], recv [E].
+static size_t route_walk_smem(int E, int threads) { return (size_t)(threads / 32 + 2) * E * sizeof(int32_t); }
+
 static size_t route_smem(const Shape& sh, int threads) {
-  const size_t walk = (size_t)(threads / 32 + 1) * sh.E * sizeof(int32_t);
+  const size_t walk = route_walk_smem(sh.E, threads);
   const size_t scan = (size_t)sh.W * sizeof(long long) + kScanTile * sizeof(int32_t);
   return walk > scan ? walk : scan;
 }
@@ -372,7 +423,7 @@ static bool cluster_route_ok(int dev, int W, size_t smem) {
   bool good = cudaFuncSetAttribute(route_kernel<true, THREADS>, cudaFuncAttributeNonPortableClusterSizeAllowed, 1) ==
                   cudaSuccess &&
               cudaFuncSetAttribute(route_kernel<true, THREADS>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                   (int)((THREADS / 32 + 1) * 1024 * sizeof(int32_t))) == cudaSuccess;
+                                   (int)route_walk_smem(1024, THREADS)) == cudaSuccess;
   if (good) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(W);
@@ -395,7 +446,7 @@ static bool cluster_route_ok(int dev, int W, size_t smem) {
 
 template <int THREADS>
 static cudaError_t launch_route_t(const RouteParams& p, cudaStream_t st, int dev) {
-  const size_t walk = (size_t)(THREADS / 32 + 1) * p.sh.E * sizeof(int32_t);
+  const size_t walk = route_walk_smem(p.sh.E, THREADS);
   if (cluster_route_ok<THREADS>(dev, p.sh.W, walk)) {
     cudaLaunchConfig_t cfg{};
     cfg.gridDim = dim3(p.sh.W);
