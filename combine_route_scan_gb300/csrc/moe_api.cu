@@ -210,6 +210,75 @@ moe_status_t moe_get_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, i
   return MOE_OK;
 }
 
+// Which assist_info / ep_recv_count the pick -> row map in each workspace was
+// last written for, as far as this process enqueued it, so that a combine of
+// those very buffers can skip the inverse-map pass. The addresses are
+// compared, never dereferenced. A dispatch captured into a CUDA graph may be
+// replayed at any later time and overwrite the map unseen, so it marks the
+// workspace: from then on only a combine captured in the same capture
+// sequence as the dispatch (the graph replays the two in order) skips the
+// pass; every other combine on that workspace runs it, and the inverse kernel
+// itself returns at once when the routing kernel's record in the workspace
+// header shows the map already belongs to its buffers. moe_workspace_init
+// clears the mark.
+namespace {
+struct MapOwner {
+  const void* ws;
+  const void* assist;
+  const void* ep;
+  unsigned long long capture;  // capture sequence of the dispatch, 0 = not captured
+  bool graphed;                // some dispatch on this workspace was captured
+};
+std::mutex g_owner_mu;
+MapOwner g_owner[256];
+int g_owner_next = 0;
+
+// Capture sequence of `s` (0 when the stream is not capturing).
+unsigned long long capture_id(cudaStream_t s) {
+  cudaStreamCaptureStatus st = cudaStreamCaptureStatusNone;
+  unsigned long long id = 0;
+  if (cudaStreamGetCaptureInfo(s, &st, &id) != cudaSuccess) {
+    cudaGetLastError();
+    return ~0ull;  // unknown: treated as a capture that matches nothing
+  }
+  return st == cudaStreamCaptureStatusNone ? 0ull : id;
+}
+
+MapOwner* owner_slot(const void* ws) {
+  for (MapOwner& o : g_owner)
+    if (o.ws == ws) return &o;
+  MapOwner* o = &g_owner[g_owner_next];
+  g_owner_next = (g_owner_next + 1) % 256;
+  *o = MapOwner{ws, nullptr, nullptr, 0ull, false};
+  return o;
+}
+
+void set_map_owner(const void* ws, const void* assist, const void* ep, cudaStream_t s) {
+  const unsigned long long cap = capture_id(s);
+  std::lock_guard<std::mutex> lock(g_owner_mu);
+  MapOwner* o = owner_slot(ws);
+  o->assist = assist;
+  o->ep = ep;
+  o->capture = cap;
+  if (cap != 0) o->graphed = true;
+}
+
+void reset_map_owner(const void* ws) {
+  std::lock_guard<std::mutex> lock(g_owner_mu);
+  *owner_slot(ws) = MapOwner{ws, nullptr, nullptr, 0ull, false};
+}
+
+bool map_owned_by(const void* ws, const void* assist, const void* ep, cudaStream_t s) {
+  const unsigned long long cap = capture_id(s);
+  std::lock_guard<std::mutex> lock(g_owner_mu);
+  for (const MapOwner& o : g_owner)
+    if (o.ws == ws)
+      return assist != nullptr && o.assist == assist && o.ep == ep && o.capture == cap && cap != ~0ull &&
+             (cap != 0 || !o.graphed);
+  return false;
+}
+}  // namespace
+
 moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, void* stream) {
   Shape sh;
   moe_status_t st = make_shape(cfg, &sh);
@@ -219,6 +288,7 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
   if (st != MOE_OK) return st;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (cudaMemsetAsync(ws, 0, sizeof(WsHeader), s) != cudaSuccess) return MOE_ERR_CUDA;
+  reset_map_owner(ws);
   if (cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.perf_end, 0, (size_t)sh.W * 8, s) != cudaSuccess)
     return MOE_ERR_CUDA;
   if (L.flags && cudaMemsetAsync(static_cast<uint8_t*>(ws) + L.flags, 0,
@@ -308,6 +378,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
   const cudaError_t e = quant_kernel ? launch_scatter_quant(sp, s, nsm, tma) : launch_scatter(sp, s, nsm, tma);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  set_map_owner(ws, assist_info, ep_recv_count, s);  // the scatter writes the map for these buffers
   if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
   return MOE_OK;
 }
@@ -357,7 +428,10 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
   cp.seg_plane_out = seg_plane;
   if (empty) return MOE_OK;
   if (cfg->combine_mode == MOE_COMBINE_GATHER) {
-    if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
+    // the map of the dispatch that wrote these buffers on this workspace is
+    // used as it is; otherwise it is rebuilt from assist_info first
+    if (!map_owned_by(ws, assist_info, ep_recv_count, s) && launch_combine_inverse(cp, s) != cudaSuccess)
+      return MOE_ERR_CUDA;
     if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
     if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
   } else {
@@ -442,6 +516,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   sp.timeout_ns = timeout_ns(cfg);
   if (!empty && launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
   if (empty) return MOE_OK;
+  set_map_owner(ws, assist, ep, s);  // the map now belongs to this call's own buffers
 
   // 2. expert FFN on the tensor cores: h1 = silu(x Wg^T) * (x Wu^T), y = h1 Wd^T
   FfnLaunch f{};

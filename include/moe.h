@@ -24,9 +24,9 @@
  * Conventions, for every entry point:
  *   - Pointers named like arrays are DEVICE pointers (cudaMalloc or torch
  *     memory) unless the comment says host. The caller owns every buffer; the
- *     library never allocates, frees or keeps a pointer past the call (the
- *     workspace may keep buffer addresses as tags, compared but never
- *     dereferenced; see moe_combine).
+ *     library never allocates, frees or keeps a pointer past the call (it
+ *     remembers which buffers a workspace's row map was written for, as
+ *     addresses that are compared but never dereferenced; see moe_combine).
  *   - `stream` is a cudaStream_t passed as void*; NULL is the legacy stream.
  *     Every call only enqueues work and returns.
  *   - Argument errors return at once, before anything is launched.
@@ -216,13 +216,20 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
  *   seg_plane     NULL or [W][L*W] uint8: two-phase plane per segment (writer = rank d)
  * combine_mode selects the gather or the two-phase window protocol; both give
  * the same bytes.
- * Gather mode turns assist_info (row -> pick) into a pick -> row map in the
- * workspace first. A moe_dispatch on the same workspace leaves that map behind
- * and tags it with the addresses of the assist_info and ep_recv_count it wrote;
- * when this call passes the same two addresses, the map is used as it is (the
- * reduce still checks every pick it reads against assist_info, so contents
- * changed in place are reported as MOE_ERR_BAD_ASSIST). The tags are only
- * compared, never dereferenced. */
+ * Gather mode reads each routed pick's row from a pick -> row map in the
+ * workspace. moe_dispatch writes that map for the assist_info and
+ * ep_recv_count it fills and records their addresses in the workspace; the
+ * library also remembers (host side, per workspace) which two addresses the
+ * last such call enqueued. When this call passes the same two and nothing can
+ * have replaced the map since (no dispatch on this workspace was captured
+ * into a CUDA graph, or this combine is captured in the same capture as that
+ * dispatch), the map is used as it is; otherwise an inverse-map kernel first
+ * rebuilds it from assist_info, or returns at once when the workspace's
+ * record shows the map already belongs to these buffers. The reduce checks
+ * every pick's row against assist_info and ep_recv_count: contents changed in
+ * place, a pick that no row names, or a receive count above the capacity are
+ * reported as MOE_ERR_BAD_ASSIST. moe_workspace_init forgets a workspace's
+ * history. */
 moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const int32_t* assist_info,
                          const int32_t* ep_recv_count, const int32_t* expert_ids,
                          const void* expert_scales, const uint8_t* active_mask, const void* x,

@@ -425,7 +425,8 @@ def test_combine_reuses_the_dispatch_row_map(name):
 def test_row_map_follows_the_buffers():
     """Two dispatches on one workspace into different output buffers: a
     combine of the first one's buffers rebuilds its map and is still right;
-    a row map changed in place after the dispatch is reported, not used."""
+    an assist_info changed in place after the dispatch so that a pick has no
+    row is reported."""
     wl = WL.WORKLOADS["w8_bs8_h16_k2_e64_i32"]
     inp_a = WL.make_inputs(wl)
     inp_b = WL.make_inputs(wl, seed=99)
@@ -444,6 +445,52 @@ def test_row_map_follows_the_buffers():
     got_b2["assist_info"][d, 0, 1] = (got_b2["assist_info"][d, 0, 1] + 1) % wl.bs
     _, st = _combine_same_ws(wl, dev_b, got_b2, ws2)
     assert M.STATUS[st] == "BAD_ASSIST"
+
+
+def _ragged_wl():
+    return WL.Workload("ragged_h12_f16", 4, 9, 12, 3, 8, WL.X_FP16, mask_kind=2, mask_false_p=0.2, zero_expert_num=1,
+                       copy_expert_num=1, special_p=0.2, seed=41)
+
+
+@pytest.mark.parametrize("name", ["w16_bs256_h7168_k8_e256_bf16_zipf", "w8_bs32_h7168_k8_e64_f16", "ragged_h12_f16"])
+def test_graph_replays_and_eager_calls_share_a_workspace(name):
+    """A CUDA graph holding dispatch + combine of buffer set B and eager calls
+    on set A share one workspace. A replay of the graph overwrites the
+    workspace's row map unseen by the library, so an eager combine of A
+    after it must not take that map for A's; the graph's own combine follows
+    its dispatch on every replay. Both match the oracle byte for byte (ragged
+    rows take the element-wise reduce)."""
+    wl = _ragged_wl() if name == "ragged_h12_f16" else WL.WORKLOADS[name]
+    inp_a, inp_b = WL.make_inputs(wl), WL.make_inputs(wl, seed=5)
+    dev_a, dev_b = H.device_inputs(wl, inp_a), H.device_inputs(wl, inp_b)
+    cfg = H.make_cfg(wl)
+    ws = M.alloc_workspace(cfg)
+    out_b = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+    x_out_b = torch.empty((wl.ep_world_size, wl.bs, wl.h), dtype=H.TORCH_DT[wl.x_dtype], device="cuda")
+    torch.cuda.synchronize()
+    stream = torch.cuda.Stream()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=stream):
+        M.dispatch(cfg, dev_b["x"], dev_b["expert_ids"], dev_b["active_mask"], dev_b["expert_scales"],
+                   out_b["expand_x"], out_b["dynamic_scales"], out_b["assist_info"], out_b["ep_recv_count"],
+                   out_b["expand_scales"], None, ws)
+        M.combine(cfg, out_b["expand_x"], out_b["assist_info"], out_b["ep_recv_count"], dev_b["expert_ids"],
+                  dev_b["expert_scales"], dev_b["active_mask"], dev_b["x"], x_out_b, None, ws)
+
+    def ref(inp):
+        r = O.dispatch(wl, inp)
+        return O.combine(wl, r["expand_x"], r["assist_info"], r["ep_recv_count"], inp)
+
+    got_a, _, _ = H.gpu_dispatch(wl, dev_a, ws=ws)
+    graph.replay()  # B's map is now in the workspace
+    x_out_a, st = _combine_same_ws(wl, dev_a, got_a, ws)
+    assert st == 0, M.STATUS.get(st, st)
+    assert np.array_equal(H.to_host(x_out_a).view(np.uint8), ref(inp_a).view(np.uint8))
+    x_out_b.view(torch.uint8).fill_(0x5A)
+    graph.replay()
+    torch.cuda.synchronize()
+    assert M.get_device_status(ws) == 0
+    assert np.array_equal(H.to_host(x_out_b).view(np.uint8), ref(inp_b).view(np.uint8))
 
 
 def test_launch_limits_survive_smaller_shapes():
