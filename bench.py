@@ -267,13 +267,24 @@ def whole_job_gbps(step_bytes: int, steps: int, max_ms: float, world: int) -> fl
     return world * step_bytes * steps / (max_ms * 1e-3) / 1e9
 
 
+def rotation_sets(step_bytes: int) -> int:
+    """Buffer sets the timed regions rotate over: one when a step moves more
+    than four times the L2, else enough that a set's data has left the L2
+    before it is used again."""
+    return 1 if step_bytes >= 4 * L2_BYTES else int(np.ceil(4 * L2_BYTES / step_bytes))
+
+
 def bench_config(wl: WL.Workload, args, step_bytes: int) -> dict:
     """The `config` object of the JSON line, the same for both arms."""
+    n_sets = rotation_sets(step_bytes)
+    l2 = (f"no flush: one step moves {step_bytes / 1e6:.0f} MB (> 4x the {L2_BYTES >> 20} MiB L2)" if n_sets == 1 else
+          f"no flush: steps rotate over {n_sets} buffer sets of {step_bytes / 1e6:.0f} MB each "
+          f"(> 4x the {L2_BYTES >> 20} MiB L2 together)")
     return {"workload": wl.name, "ep_world_size": wl.ep_world_size, "bs": wl.bs, "h": wl.h,
             "topk": wl.topk, "moe_expert_num": wl.moe_expert_num, "zero_experts": wl.zero_expert_num,
             "copy_experts": wl.copy_expert_num, "mask": wl.mask_kind, "quant_mode": wl.quant_mode,
             "plane_policy": getattr(args, "plane_policy", 0), "combine": "gather",
-            "l2": f"no flush: one step moves {step_bytes / 1e6:.0f} MB (> {L2_BYTES >> 20} MiB L2)",
+            "l2": l2,
             "accumulate": "fp32"}
 
 
@@ -610,16 +621,26 @@ def run_ours(args):
     out = M.alloc_dispatch_outputs(cfg, tdt)
     x_out = torch.empty_like(x)
     stream = torch.cuda.current_stream()
+    # timed regions A and B rotate over independent buffer sets when one step
+    # would stay in L2 (set 0 is the one the other sections use)
+    n_sets = rotation_sets(step_bytes)
+    sets = [{"x": x, "ids": ids, "mask": mask, "scales": scales, "ws": ws, "out": out, "x_out": x_out}]
+    for _ in range(n_sets - 1):
+        sets.append({"x": x.clone(), "ids": ids.clone(), "mask": None if mask is None else mask.clone(),
+                     "scales": scales.clone(), "ws": M.alloc_workspace(cfg), "out": M.alloc_dispatch_outputs(cfg, tdt),
+                     "x_out": torch.empty_like(x)})
 
-    def step(cfg_d, cfg_c, xin=x, xo=x_out, ids_=ids, mask_=mask, scales_=scales):
-        M.dispatch(cfg_d, xin, ids_, mask_, scales_, out["expand_x"], out["dynamic_scales"], out["assist_info"],
-                   out["ep_recv_count"], out["expand_scales"], None, ws)
+    def step(cfg_d, cfg_c, b=None):
+        b = sets[0] if b is None else b
+        o = b["out"]
+        M.dispatch(cfg_d, b["x"], b["ids"], b["mask"], b["scales"], o["expand_x"], o["dynamic_scales"],
+                   o["assist_info"], o["ep_recv_count"], o["expand_scales"], None, b["ws"])
         if wl.quant_mode == 0:
-            M.combine(cfg_c, out["expand_x"], out["assist_info"], out["ep_recv_count"], ids_, scales_, mask_, xin,
-                      xo, None, ws)
+            M.combine(cfg_c, o["expand_x"], o["assist_info"], o["ep_recv_count"], b["ids"], b["scales"], b["mask"],
+                      b["x"], b["x_out"], None, b["ws"])
 
-    for _ in range(max(3, args.warmup)):
-        step(cfg, cfg)
+    for i in range(max(3, args.warmup, 2 * n_sets)):
+        step(cfg, cfg, sets[i % n_sets])
     torch.cuda.synchronize()
     st = M.get_device_status(ws)
     if st != 0:
@@ -638,7 +659,7 @@ def run_ours(args):
     h0 = time.time()
     t_start.record(stream)
     for k in range(K):
-        step(cfg, cfg)
+        step(cfg, cfg, sets[k % n_sets])
     t_end.record(stream)
     torch.cuda.synchronize()
     if world > 1:
@@ -649,29 +670,31 @@ def run_ours(args):
     h_ext = h1
     if sampler and h1 - h0 < 1.5:
         while time.time() - h0 < 1.5:
-            for _ in range(50):
-                step(cfg, cfg)
+            for i in range(50):
+                step(cfg, cfg, sets[i % n_sets])
             torch.cuda.synchronize()
         h_ext = time.time()
     total_ms = max_over_ranks(total_ms, world)
 
-    # The same K steps replayed from a CUDA graph of one step (no host launch
-    # cost per step); reported beside region A.
+    # The same steps replayed from a CUDA graph of one step per buffer set (no
+    # host launch cost per step); reported beside region A.
     graph = torch.cuda.CUDAGraph()
     with torch.cuda.graph(graph):
-        step(cfg, cfg)
+        for b in sets:
+            step(cfg, cfg, b)
     graph.replay()
     torch.cuda.synchronize()
     g0, g1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    reps = max(1, K // n_sets)
     if world > 1:
         dist.barrier()
     torch.cuda.synchronize()
     g0.record(stream)
-    for k in range(K):
+    for k in range(reps):
         graph.replay()
     g1.record(stream)
     torch.cuda.synchronize()
-    graph_ms = max_over_ranks(g0.elapsed_time(g1), world) / K
+    graph_ms = max_over_ranks(g0.elapsed_time(g1), world) / (reps * n_sets)
     del graph
 
     # Timed region B (kernel attribution): the same K steps with CUDA events the
@@ -688,13 +711,14 @@ def run_ours(args):
     torch.cuda.synchronize()
     b_start.record(stream)
     for k in range(K):
-        step(cfg_s[k], cfg_r[k])
+        step(cfg_s[k], cfg_r[k], sets[k % n_sets])
     b_end.record(stream)
     torch.cuda.synchronize()
     instrumented_ms = max_over_ranks(b_start.elapsed_time(b_end), world) / K
-    st = M.get_device_status(ws)
-    if st != 0:
-        raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the timed region")
+    for b in sets:
+        st = M.get_device_status(b["ws"])
+        if st != 0:
+            raise RuntimeError(f"device status {M.STATUS.get(st, st)} in the timed region")
 
     scatter_ms = statistics.mean(e.elapsed_ms() for e in ev_scatter)
     reduce_ms = statistics.mean(e.elapsed_ms() for e in ev_reduce) if wl.quant_mode == 0 else 0.0
@@ -827,7 +851,8 @@ def run_ours(args):
             stream.wait_event(ev_h2d[i & 1])
             if i >= 2:
                 stream.wait_event(ev_d2h[i & 1])  # step i-2's x_out has been read back
-            step(cfg, cfg, xin=b["x"], xo=b["out"], ids_=b["ids"], mask_=b["mask"], scales_=b["scales"])
+            step(cfg, cfg, {"x": b["x"], "ids": b["ids"], "mask": b["mask"], "scales": b["scales"], "ws": ws,
+                            "out": out, "x_out": b["out"]})
             ev_comp[i & 1].record(stream)
             with torch.cuda.stream(s_d2h):
                 s_d2h.wait_event(ev_comp[i & 1])
