@@ -65,6 +65,35 @@ def test_random_small(seed):
     run_and_compare(wl, plane_policy=seed % 3, bulk_min_bytes=0 if seed % 2 else O.DEFAULT_BULK_MIN_BYTES)
 
 
+@pytest.mark.parametrize("seed", range(6))
+def test_random_many_tokens_per_scatter_cta(seed):
+    """Medium random problems with short rows: far more tokens than the TMA
+    scatter's resident CTAs hold in their rings, so most tokens go out by the
+    workspace's ticket counter; Zipf or uniform routing, masks and specials;
+    dispatch and gather combine on the same workspace (the map the scatter
+    wrote) against the oracle."""
+    rng = np.random.default_rng(900 + seed)
+    W = int(rng.choice([2, 4, 8, 16]))
+    L = int(rng.choice([1, 2, 4, 8]))
+    K = int(rng.integers(1, min(W * L, 8) + 1))
+    h = int(rng.choice([8, 64, 256]))
+    dt = [WL.X_FP16, WL.X_BF16, WL.X_INT32][seed % 3]
+    bs = int(rng.integers(8192, 16385)) // W  # > 4 ring slots x 1216 CTAs (short rows: 8 CTAs a SM)
+    Z, C = int(rng.integers(0, 3)), int(rng.integers(0, 3))
+    wl = WL.Workload(f"rand_many_w{W}_l{L}_k{K}_bs{bs}_h{h}", W, bs, h, K, W * L, dt, zero_expert_num=Z,
+                     copy_expert_num=C, mask_kind=int(rng.integers(0, 3)), special_p=0.1 if Z + C else 0.0,
+                     mask_false_p=0.1, ids="zipf" if seed % 2 else "uniform", x_range=100, seed=seed + 77)
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    x_ref = O.combine(wl, ref["expand_x"], ref["assist_info"], ref["ep_recv_count"], inp)
+    dev = H.device_inputs(wl, inp)
+    got, ws, _ = H.gpu_dispatch(wl, dev)
+    H.compare_dispatch(wl, got, ref, O.dispatch_plane(wl, ref["ep_recv_count"], O.DEFAULT_BULK_MIN_BYTES))
+    x_out, st = _combine_same_ws(wl, dev, got, ws)
+    assert st == 0, M.STATUS.get(st, st)
+    assert np.array_equal(H.to_host(x_out).view(np.uint8), x_ref.view(np.uint8))
+
+
 @pytest.mark.parametrize("h,dt,q", [(12, WL.X_FP16, 0), (20, WL.X_BF16, 0), (3, WL.X_INT32, 0),
                                     (24, WL.X_FP16, 2), (40, WL.X_BF16, 2), (5, WL.X_BF16, 2)])
 def test_rows_not_multiple_of_16_bytes(h, dt, q):
