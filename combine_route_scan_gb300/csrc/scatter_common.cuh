@@ -93,6 +93,81 @@ __device__ __forceinline__ void build_picks(const ScatterParams& p, size_t tau, 
   }
 }
 
+// The loads of build_picks issued ahead of their use (warp 0, lanes < K):
+// a pick's position, expert id and weight one token ahead, its segment's
+// first row and plane, which need the id, on the next token; the list is then
+// built without waiting on memory (build_picks_from).
+struct PickAhead {
+  int r, e;    // position in the segment (-1: not routed), expert id
+  uint32_t w;  // expert_scales bits (when expand_scales is written)
+  int base;    // first row of segment e*W + s
+  int plane;   // its plane
+};
+
+__device__ __forceinline__ void pick_load_first(const ScatterParams& p, size_t tau, PickAhead& a) {
+  const int lane = threadIdx.x & 31;
+  a.r = -1;
+  a.e = -1;
+  a.w = 0u;
+  if (lane < p.sh.K) {
+    a.r = p.rank[tau * p.sh.K + lane];
+    a.e = p.ids[tau * p.sh.K + lane];
+    if (p.expand_scales) a.w = reinterpret_cast<const uint32_t*>(p.scales)[tau * p.sh.K + lane];
+  }
+}
+
+__device__ __forceinline__ void pick_load_second(const ScatterParams& p, int s, PickAhead& a) {
+  a.base = 0;
+  a.plane = 0;
+  if (a.r >= 0 && a.e >= 0 && a.e < p.sh.E) {
+    const size_t g = (size_t)a.e * p.sh.W + s;
+    a.base = p.base[g];
+    a.plane = p.plane[g];
+  }
+}
+
+// build_picks on values loaded ahead (same results, same metadata writes).
+__device__ __forceinline__ void build_picks_from(const ScatterParams& p, size_t tau, int s, int t, PickTable& tab,
+                                                 const PickAhead& a) {
+  const Shape& sh = p.sh;
+  const int lane = threadIdx.x & 31;
+  long long dst = -1;
+  int bulk = 0;
+  if (lane < sh.K && a.r >= 0 && MOE_IN_BOUNDS(p.status, a.e, sh.E)) {
+    const int d = a.e / sh.L;
+    const long long row = (long long)a.base + a.r;
+    if (row < sh.A && MOE_IN_BOUNDS(p.status, (long long)d * sh.A + row, (long long)sh.W * sh.A)) {
+      dst = (long long)d * sh.A + row;
+      bulk = a.plane;
+      if (p.inv) p.inv[tau * sh.K + lane] = (int32_t)dst;
+      int32_t* as = p.assist + dst * 3;
+      as[0] = s;
+      as[1] = t;
+      as[2] = lane;
+      if (p.expand_scales) reinterpret_cast<uint32_t*>(p.expand_scales)[dst] = a.w;
+    } else {
+      set_error(p.status, MOE_ERR_CAPACITY);
+    }
+  }
+  const uint32_t m_sm = __ballot_sync(0xffffffffu, dst >= 0 && !bulk);
+  const uint32_t m_bk = __ballot_sync(0xffffffffu, dst >= 0 && bulk);
+  const int seg = dst >= 0 ? a.e * sh.W + s : -1;
+  if (dst >= 0 && !bulk) {
+    const int j = __popc(m_sm & lanemask_lt());
+    tab.sm_dst[j] = dst;
+    tab.sm_seg[j] = seg;
+  }
+  if (dst >= 0 && bulk) {
+    const int j = __popc(m_bk & lanemask_lt());
+    tab.bulk_dst[j] = dst;
+    tab.bulk_seg[j] = seg;
+  }
+  if (lane == 0) {
+    tab.n_sm = __popc(m_sm);
+    tab.n_bulk = __popc(m_bk);
+  }
+}
+
 // Per-rank communication time (performance info): the earliest CTA start,
 // the latest row-store time per source rank, and the last CTA to finish adds
 // each rank's span to the caller's array and resets the workspace fields.

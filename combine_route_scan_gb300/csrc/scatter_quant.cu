@@ -297,7 +297,7 @@ __device__ __forceinline__ void quantize_variant(const uint8_t* row, const float
 // MODE: quantMode (1..4); DT: MOE_F16 / MOE_BF16; YT: MOE_Y_* of the output;
 // PE: per-expert scales (every pick's row is different).
 template <int MODE, int DT, int YT, bool PE>
-__global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterParams p) {
+__global__ void __launch_bounds__(kScatterThreads, (MODE != 1 && !PE) ? 5 : 0) scatter_quant_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kQStages];
   __shared__ PickTable tabs[2];
@@ -343,6 +343,18 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
 
   int nv = 0;   // variants through the shared buffers so far (selects the buffer)
   int nvr = 0;  // variants so far (selects the s_red half)
+  // warp 0: the destination-list loads of token i (both levels) and i + 1
+  // (first level), so that building a list never waits on memory. Measured on
+  // GB300 for the per-token and per-block modes (the registers it takes are
+  // capped at five CTAs per SM); the static-scale and per-expert forms,
+  // whose tokens cost little or a great deal, keep loading on the spot.
+  constexpr bool kAhead = MODE != 1 && !PE;
+  PickAhead cur{}, nxt{};
+  if (kAhead && warp == 0 && my_n > 0) {
+    pick_load_first(p, blockIdx.x, cur);
+    if (my_n > 1) pick_load_first(p, blockIdx.x + (size_t)G, nxt);
+    pick_load_second(p, (int)(blockIdx.x / sh.bs), cur);
+  }
   for (int i = 0; i < my_n; ++i) {
     const size_t tau = blockIdx.x + (size_t)i * G;
     const int s = (int)(tau / sh.bs), t = (int)(tau % sh.bs);
@@ -356,7 +368,18 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_quant_kernel(ScatterP
     // the buffer of this token's first shared variant was last read by the
     // bulk group two variants back: at most one newer group may still read
     if (tid == 0) bulk_wait_read<1>();
-    if (warp == 0) build_picks(p, tau, s, t, tab);
+    if (warp == 0) {
+      if constexpr (kAhead) {
+        build_picks_from(p, tau, s, t, tab, cur);
+        PickAhead n2{};
+        if (i + 1 < my_n) pick_load_second(p, (int)((tau + G) / sh.bs), nxt);
+        if (i + 2 < my_n) pick_load_first(p, tau + 2 * (size_t)G, n2);
+        cur = nxt;
+        nxt = n2;
+      } else {
+        build_picks(p, tau, s, t, tab);
+      }
+    }
     __syncthreads();
     if (s_abort) break;
     if (p.seg_ready && warp == 0 && i >= 1) publish_token(p, tabs[(i - 1) & 1]);
