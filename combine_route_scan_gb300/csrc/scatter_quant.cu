@@ -156,6 +156,16 @@ struct RowSink {
   int nd;
 };
 
+// Per-token int8 with per-expert smoothing for one pick, by one warp: the
+// maximum of |x * s[e]| over the row by the warp's shuffles (no CTA barrier,
+// so the warps of a CTA quantise different picks at once), then the codes
+// straight to the pick's row. Same arithmetic, same order-free maximum, same
+// bytes as the CTA-wide form.
+template <int DT>
+__device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, const float* srow, uint8_t* out,
+                                                         uint8_t* dyn, long long dst, uint32_t row_out,
+                                                         uint32_t nvec);
+
 // SINK: kShared (the shared buffers), kOne (the single destination dst[0]),
 // kMany (destinations dst[0..n)).
 enum { kShared = 0, kOne = 1, kMany = 2 };
@@ -294,10 +304,39 @@ __device__ __forceinline__ void quantize_variant(const uint8_t* row, const float
   }
 }
 
+template <int DT>
+__device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, const float* srow, uint8_t* out,
+                                                         uint8_t* dyn, long long dst, uint32_t row_out,
+                                                         uint32_t nvec) {
+  const int lane = threadIdx.x & 31;
+  float m = 0.f;
+  for (uint32_t v = lane; v < nvec; v += 32) {
+    float f[8], sc[8];
+    unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+    load_scales8(srow, v, sc);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(__fmul_rn(f[i], sc[i])));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  const float scale = __fdiv_rn(m, 127.0f);
+  uint8_t* q = out + dst * row_out;
+  for (uint32_t v = lane; v < nvec; v += 32) {
+    float f[8], sc[8];
+    unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+    load_scales8(srow, v, sc);
+    int qv[8];
+#pragma unroll
+    for (int i = 0; i < 8; ++i) qv[i] = m == 0.f ? 0 : token_q(__fmul_rn(f[i], sc[i]), scale);
+    *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
+  }
+  if (lane == 0) reinterpret_cast<float*>(dyn)[dst] = scale;
+}
+
 // MODE: quantMode (1..4); DT: MOE_F16 / MOE_BF16; YT: MOE_Y_* of the output;
 // PE: per-expert scales (every pick's row is different).
 template <int MODE, int DT, int YT, bool PE>
-__global__ void __launch_bounds__(kScatterThreads, (MODE != 1 && !PE) ? 5 : 0) scatter_quant_kernel(ScatterParams p) {
+__global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !PE)) ? 5 : 0) scatter_quant_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kQStages];
   __shared__ PickTable tabs[2];
@@ -404,7 +443,11 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE != 1 && !PE) ? 5 : 0) s
     // store-plane picks straight from registers: each pick on its own with
     // per-expert scales, else one pass for all of them when the token has no
     // bulk-plane pick (no shared buffer, no barrier)
-    if (PE) {
+    if (PE && MODE == 2) {
+      for (int j = warp; j < nsm; j += kScatterWarps)
+        quantize_pick_warp_mode2<DT>(row, p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h, out, dyn,
+                                     tab.sm_dst[j], row_out, nvec);
+    } else if (PE) {
       for (int j = 0; j < nsm; ++j) {
         const RowSink k{nullptr, nullptr, &tab.sm_dst[j], 1, out, dyn, row_out, nd};
         quantize_variant<MODE, DT, YT, kOne>(row, p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h, s0, k, nvec,
