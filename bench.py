@@ -657,10 +657,12 @@ def run_ours(args):
         dist.barrier()
     torch.cuda.synchronize()
     h0 = time.time()
+    n_launch0 = M.launch_count()
     t_start.record(stream)
     for k in range(K):
         step(cfg, cfg, sets[k % n_sets])
     t_end.record(stream)
+    n_launches = M.launch_count() - n_launch0
     torch.cuda.synchronize()
     if world > 1:
         dist.barrier()
@@ -933,7 +935,7 @@ def run_ours(args):
         "ffn_variant": ffn,
         "small_workloads": small,
         "quant_dispatch": quant,
-        "gpu_launches": K * (4 if wl.quant_mode == 0 else 2),
+        "gpu_launches": n_launches,
         "clocks": clocks,
     }
     print(json.dumps(line))

@@ -5,11 +5,18 @@
 // dependent launch.
 #include <string.h>
 
+#include <atomic>
 #include <mutex>
 
 #include "internal.h"
 
 namespace crs {
+
+namespace {
+std::atomic<uint64_t> g_launches{0};
+}
+// n more kernels were enqueued (moe_launch_count)
+void note_launches(int n) { g_launches.fetch_add((uint64_t)n, std::memory_order_relaxed); }
 
 cudaError_t resident_blocks(const void* kernel, int threads, size_t smem, int* per_sm) {
   // The dynamic shared-memory limit is state of the kernel, not of one call:
@@ -350,6 +357,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   rp.hdr = hdr;
   rp.assist_out = assist_info;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  note_launches(1);
 
   ScatterParams sp{};
   sp.cnt = rp.cnt;
@@ -378,6 +386,7 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
   const cudaError_t e = quant_kernel ? launch_scatter_quant(sp, s, nsm, tma) : launch_scatter(sp, s, nsm, tma);
   if (e != cudaSuccess) return MOE_ERR_CUDA;
+  if (!empty) note_launches(1);
   set_map_owner(ws, assist_info, ep_recv_count, s);  // the scatter writes the map for these buffers
   if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -430,10 +439,13 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
   if (cfg->combine_mode == MOE_COMBINE_GATHER) {
     // the map of the dispatch that wrote these buffers on this workspace is
     // used as it is; otherwise it is rebuilt from assist_info first
-    if (!map_owned_by(ws, assist_info, ep_recv_count, s) && launch_combine_inverse(cp, s) != cudaSuccess)
-      return MOE_ERR_CUDA;
+    if (!map_owned_by(ws, assist_info, ep_recv_count, s)) {
+      if (launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
+      note_launches(1);
+    }
     if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
     if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
+    note_launches(1);
   } else {
     cp.window = w + L.window;
     cp.flags = reinterpret_cast<uint32_t*>(w + L.flags);
@@ -444,6 +456,7 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
     cudaError_t e = launch_combine_two_phase(cp, s, nsm);
     if (e == cudaErrorNotSupported) return MOE_ERR_UNSUPPORTED;
     if (e != cudaSuccess) return MOE_ERR_CUDA;
+    note_launches(1);
   }
   if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
   return MOE_OK;
@@ -500,6 +513,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   rp.hdr = hdr;
   rp.assist_out = assist;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
+  note_launches(1);
   ScatterParams sp{};
   sp.x = x;
   sp.ids = expert_ids;
@@ -516,6 +530,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   sp.timeout_ns = timeout_ns(cfg);
   if (!empty && launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
   if (empty) return MOE_OK;
+  note_launches(1);
   set_map_owner(ws, assist, ep, s);  // the map now belongs to this call's own buffers
 
   // 2. expert FFN on the tensor cores: h1 = silu(x Wg^T) * (x Wu^T), y = h1 Wd^T
@@ -532,6 +547,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   f.status = &hdr->status;
   f.timeout_ns = timeout_ns(cfg);
   if (launch_ffn(f, s, nsm, cfg->prof_events) != cudaSuccess) return MOE_ERR_CUDA;
+  note_launches(2);
 
   // 3. combine the expert outputs
   CombineParams cp{};
@@ -549,6 +565,7 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   cp.hdr = hdr;
   // the scatter above wrote the pick -> row map: no inverse pass
   if (launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
+  note_launches(1);
   return MOE_OK;
 }
 
@@ -562,6 +579,8 @@ moe_status_t moe_get_device_status(void* ws, void* stream, int32_t* status) {
   *status = v;
   return MOE_OK;
 }
+
+uint64_t moe_launch_count(void) { return crs::g_launches.load(std::memory_order_relaxed); }
 
 const char* moe_status_string(int32_t status) {
   switch (status) {

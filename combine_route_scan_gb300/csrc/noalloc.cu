@@ -28,6 +28,10 @@
 
 #include "internal.h"
 
+namespace crs {
+void note_launches(int n);  // moe_api.cu: the library's launch count
+}
+
 namespace {
 
 constexpr long long kNoAllocMaxPicks = 262144;
@@ -128,5 +132,6 @@ extern "C" moe_status_t moe_combine_noalloc(const moe_config_t* cfg, const void*
   cp.status = status;
   if (crs::launch_combine_inverse(cp, s) != cudaSuccess) return MOE_ERR_CUDA;
   if (crs::launch_combine_reduce(cp, s, nsm) != cudaSuccess) return MOE_ERR_CUDA;
+  crs::note_launches(2);
   return MOE_OK;
 }

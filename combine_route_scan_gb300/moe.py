@@ -95,6 +95,8 @@ def lib() -> ctypes.CDLL:
         L.moe_get_device_status.argtypes = [P, P, ctypes.POINTER(ctypes.c_int32)]
         L.moe_status_string.argtypes = [ctypes.c_int32]
         L.moe_status_string.restype = ctypes.c_char_p
+        L.moe_launch_count.argtypes = []
+        L.moe_launch_count.restype = ctypes.c_uint64
         for f in ("moe_get_workspace_size", "moe_workspace_init", "moe_dispatch", "moe_combine",
                   "moe_dispatch_ffn_combine", "moe_combine_noalloc", "moe_get_device_status"):
             getattr(L, f).restype = ctypes.c_int32
@@ -223,6 +225,11 @@ def get_device_status(ws: torch.Tensor, stream=None) -> int:
 
 def status_string(code: int) -> str:
     return lib().moe_status_string(code).decode()
+
+
+def launch_count() -> int:
+    """Kernels the library has enqueued in this process so far."""
+    return int(lib().moe_launch_count())
 
 
 # ------------------------------------------------------------ allocation

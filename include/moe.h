@@ -283,6 +283,11 @@ moe_status_t moe_get_device_status(void* ws, void* stream, int32_t* status);
 /* Static text for a status code. */
 const char* moe_status_string(int32_t status);
 
+/* Kernels this library has enqueued in this process so far (host-side count
+ * of successful launches, every entry point and device; a launch captured
+ * into a CUDA graph counts once, at capture). */
+uint64_t moe_launch_count(void);
+
 #ifdef __cplusplus
 }
 #endif

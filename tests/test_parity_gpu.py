@@ -522,6 +522,29 @@ def test_graph_replays_and_eager_calls_share_a_workspace(name):
     assert np.array_equal(H.to_host(x_out_b).view(np.uint8), ref(inp_b).view(np.uint8))
 
 
+def test_launch_count_shows_the_skipped_inverse_pass():
+    """The library's own launch count: dispatch = routing + scatter; a combine
+    of the same buffers on the same workspace = the reduce alone; a combine
+    of buffers the workspace's map was not written for adds the inverse-map
+    kernel."""
+    wl = WL.WORKLOADS["w8_bs32_h7168_k8_e64_f16"]
+    inp_a, inp_b = WL.make_inputs(wl), WL.make_inputs(wl, seed=3)
+    dev_a, dev_b = H.device_inputs(wl, inp_a), H.device_inputs(wl, inp_b)
+    n0 = M.launch_count()
+    got_a, ws, _ = H.gpu_dispatch(wl, dev_a)
+    assert M.launch_count() - n0 == 2
+    n0 = M.launch_count()
+    _, st = _combine_same_ws(wl, dev_a, got_a, ws)
+    assert st == 0 and M.launch_count() - n0 == 1
+    got_b, _, _ = H.gpu_dispatch(wl, dev_b, ws=ws)
+    n0 = M.launch_count()
+    x_out, st = _combine_same_ws(wl, dev_a, got_a, ws)  # the map is B's now
+    assert st == 0 and M.launch_count() - n0 == 2
+    ref = O.dispatch(wl, inp_a)
+    x_ref = O.combine(wl, ref["expand_x"], ref["assist_info"], ref["ep_recv_count"], inp_a)
+    assert np.array_equal(H.to_host(x_out).view(np.uint8), x_ref.view(np.uint8))
+
+
 def test_launch_limits_survive_smaller_shapes():
     """A kernel's dynamic shared-memory limit only ever rises: a large row
     shape, then a small one, then the large one again all launch and match."""

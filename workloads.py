@@ -129,9 +129,12 @@ def fp32_to_bf16_bits(a: np.ndarray) -> np.ndarray:
 
     Used only to draw bf16 inputs; the samples are finite.
     """
-    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32).astype(np.uint64)
-    u = u + 0x7FFF + ((u >> 16) & 1)
-    return (u >> 16).astype(np.uint16)
+    u = np.ascontiguousarray(a, dtype=np.float32).view(np.uint32)
+    r = (u >> 16) & np.uint32(1)  # finite values: the sum below stays below 2^32
+    r += np.uint32(0x7FFF)
+    r += u
+    r >>= np.uint32(16)
+    return r.astype(np.uint16)
 
 
 def bf16_bits_to_fp32(b: np.ndarray) -> np.ndarray:
