@@ -170,7 +170,11 @@ moe_status_t moe_get_workspace_size(const moe_config_t* cfg, size_t* ws_bytes, i
 
 /* Clears the workspace header (status word, call counters, flag epoch).
  * Required once before the first call that uses a workspace, and after
- * reallocating it. Enqueued on `stream`. */
+ * reallocating it. Enqueued on `stream`.
+ * A workspace carries state from one call to the next (counters, the row map
+ * a dispatch leaves for its combine): calls that use one workspace must run
+ * one after another on the GPU (one stream, or streams ordered by events);
+ * overlapping calls need a workspace each. */
 moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_bytes, void* stream);
 
 /* Dispatch ([DISP] 接口功能: expandXOut = AllToAllV(X), quantised first when
