@@ -192,14 +192,17 @@ __device__ __forceinline__ void put_dyn(const RowSink& k, int g, T v) {
 }
 
 // Quantises the staged row (elements times srow, or s0 for a (1,) coefficient)
-// into the sink. Every thread of the CTA calls it (per-token int8 reduces the
-// row maximum through s_red with one barrier).
+// into the sink. Threads t0, t0 + nt, ... take the row's 16-byte vectors: the
+// whole CTA (t0 = threadIdx.x, nt = the CTA size), or for modes 1 and 3, whose
+// groups lie within a warp, one warp (t0 = its lane, nt = 32). Per-token int8
+// is CTA-wide only: it reduces the row maximum through s_red with a barrier.
 template <int MODE, int DT, int YT, int SINK>
 __device__ __forceinline__ void quantize_variant(const uint8_t* row, const float* srow, float s0, const RowSink& k,
-                                                 uint32_t nvec, float* s_red) {
+                                                 uint32_t nvec, float* s_red, int t0 = threadIdx.x,
+                                                 int nt = kScatterThreads) {
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
   if (MODE == 1) {
-    for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
+    for (uint32_t v = t0; v < nvec; v += nt) {
       float f[8], sc[8];
       unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
       if (srow) {
@@ -255,8 +258,8 @@ __device__ __forceinline__ void quantize_variant(const uint8_t* row, const float
     // neighbouring lanes; every lane of a warp takes part in the shuffles,
     // past-the-end lanes with zeros
     constexpr int kLanes = MODE == 3 ? 16 : 4;
-    for (uint32_t base = 0; base < nvec; base += kScatterThreads) {
-      const uint32_t v = base + tid;
+    for (uint32_t base = 0; base < nvec; base += nt) {
+      const uint32_t v = base + t0;
       const bool valid = v < nvec;
       float f[8];
       if (valid) {
@@ -443,15 +446,17 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     // store-plane picks straight from registers: each pick on its own with
     // per-expert scales, else one pass for all of them when the token has no
     // bulk-plane pick (no shared buffer, no barrier)
-    if (PE && MODE == 2) {
-      for (int j = warp; j < nsm; j += kScatterWarps)
-        quantize_pick_warp_mode2<DT>(row, p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h, out, dyn,
-                                     tab.sm_dst[j], row_out, nvec);
-    } else if (PE) {
-      for (int j = 0; j < nsm; ++j) {
-        const RowSink k{nullptr, nullptr, &tab.sm_dst[j], 1, out, dyn, row_out, nd};
-        quantize_variant<MODE, DT, YT, kOne>(row, p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h, s0, k, nvec,
-                                             s_red[nvr++ & 1]);
+    if constexpr (PE) {
+      // one store-plane pick per warp (no CTA barrier; each lane keeps many
+      // scales loads in flight)
+      for (int j = warp; j < nsm; j += kScatterWarps) {
+        const float* srow = p.qscales + (size_t)(tab.sm_seg[j] / sh.W) * sh.h;
+        if constexpr (MODE == 2) {
+          quantize_pick_warp_mode2<DT>(row, srow, out, dyn, tab.sm_dst[j], row_out, nvec);
+        } else {
+          const RowSink k{nullptr, nullptr, &tab.sm_dst[j], 1, out, dyn, row_out, nd};
+          quantize_variant<MODE, DT, YT, kOne>(row, srow, s0, k, nvec, nullptr, tid & 31, 32);
+        }
       }
     } else if (direct && nsm > 0) {
       const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
