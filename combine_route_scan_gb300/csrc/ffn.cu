@@ -21,8 +21,13 @@
 //     up); its epilogue computes h1 = bf16(silu(g) * u);
 //   * second GEMM: a unit = (expert, 2 x 128 rows of down); its epilogue writes
 //     the bf16 expert output y, which the gather combine then reduces.
-// Persistent CTAs (one per SM) walk the units; every wait is bounded and a
-// timeout leaves MOE_ERR_TIMEOUT in the status word instead of hanging.
+// Both GEMMs run in one persistent launch (one CTA per SM, all resident: a
+// cooperative launch): every CTA walks its share of the gate/up units and then
+// of the down units, and a down unit waits (bounded) until every gate/up unit
+// of its expert has stored its h1 rows, counted per expert in the workspace.
+// So the SMs that finish their gate/up share early stream down weights while
+// the last gate/up units run. Every wait is bounded and a timeout leaves
+// MOE_ERR_TIMEOUT in the status word instead of hanging.
 #include <cuda.h>
 #include <cudaTypedefs.h>
 #include <cuda_bf16.h>
@@ -49,13 +54,13 @@ enum { FFN_GATE_UP = 0, FFN_DOWN = 1 };
 
 struct FfnParams {
   const int32_t* ep;   // running receive counts [W][L*W]
-  __nv_bfloat16* out;  // h1 [W*A][I] (gate/up) or y [W*A][h] (down)
+  __nv_bfloat16* h1;   // [W*A][I]: gate/up output, down input
+  __nv_bfloat16* y;    // [W*A][h]: down output
+  uint32_t* done;      // [E] gate/up epilogue warps finished per expert (zeroed by the routing kernel)
   int W, L, E;
   long long A;
-  int K;         // reduction length: h (gate/up) or I (down)
-  int out_cols;  // row length of out
-  int tiles;     // units per expert
-  int a_rows;    // weight rows per expert: I (gate/up) or h (down)
+  int h, I;
+  int tiles_gu, tiles_dn;  // units per expert: I / 128 (gate/up), h / 256 (down)
   int* status;
   uint64_t timeout_ns;
 };
@@ -129,15 +134,23 @@ __device__ __forceinline__ uint32_t idesc_bf16(int n) {
 
 // ------------------------------------------------------------- the kernel
 
+// A unit: one expert's 2 x 128 weight rows against all of its tokens. Units
+// [0, E*tiles_gu) are gate/up (the same 128 rows of gate and of up), the rest
+// down (two 128-row slices of the down projection).
 struct Unit {
-  int e, tile, n_e;
+  int mode, e, tile, n_e, K;
   long long row0;  // flat expand row of the expert's first token
 };
 
 __device__ __forceinline__ Unit unit_of(const FfnParams& p, int u) {
   Unit x;
-  x.e = u / p.tiles;
-  x.tile = u % p.tiles;
+  const int n_gu = p.E * p.tiles_gu;
+  x.mode = u < n_gu ? FFN_GATE_UP : FFN_DOWN;
+  if (x.mode == FFN_DOWN) u -= n_gu;
+  const int tiles = x.mode == FFN_GATE_UP ? p.tiles_gu : p.tiles_dn;
+  x.e = u / tiles;
+  x.tile = u % tiles;
+  x.K = x.mode == FFN_GATE_UP ? p.h : p.I;
   const int d = x.e / p.L, le = x.e % p.L, LW = p.L * p.W;
   const int32_t* epd = p.ep + (size_t)d * LW;
   const int start = le == 0 ? 0 : epd[le * p.W - 1];
@@ -147,9 +160,32 @@ __device__ __forceinline__ Unit unit_of(const FfnParams& p, int u) {
   return x;
 }
 
-template <int MODE>
+// First weight row of tile t of a unit (rows of w_gate / w_up: expert-major
+// I rows; of w_down: expert-major h rows).
 __device__ __forceinline__ int a_row(const FfnParams& p, const Unit& u, int t) {
-  return MODE == FFN_GATE_UP ? u.e * p.a_rows + u.tile * 128 : u.e * p.a_rows + u.tile * 256 + t * 128;
+  return u.mode == FFN_GATE_UP ? u.e * p.I + u.tile * 128 : u.e * p.h + u.tile * 256 + t * 128;
+}
+
+// A down unit may start once all gate/up units of its expert have stored their
+// h1 rows: bounded acquire-spin on the expert's counter, then order those
+// generic-proxy stores before this thread's TMA (async-proxy) reads of h1.
+__device__ __forceinline__ bool wait_expert(const FfnParams& p, int e, volatile int* abort_flag) {
+  const uint64_t t0 = globaltimer_ns();
+  for (uint32_t it = 0;; ++it) {
+    uint32_t v;
+    asm volatile("ld.acquire.gpu.global.u32 %0, [%1];" : "=r"(v) : "l"(p.done + e) : "memory");
+    if (v >= 4u * (uint32_t)p.tiles_gu) break;  // every epilogue warp of every gate/up unit
+    if ((it & 63u) == 63u) {
+      if (*abort_flag) return false;
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        set_error(p.status, MOE_ERR_TIMEOUT);
+        *abort_flag = 1;
+        return false;
+      }
+    }
+  }
+  asm volatile("fence.proxy.async.global;" ::: "memory");
+  return true;
 }
 
 __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, const FfnParams& p,
@@ -169,10 +205,10 @@ __device__ __forceinline__ bool wait_or_abort(uint64_t* bar, uint32_t parity, co
   }
 }
 
-template <int MODE>
 __global__ void __launch_bounds__(kFfnThreads, 1)
-    ffn_gemm_kernel(const __grid_constant__ CUtensorMap map_a0, const __grid_constant__ CUtensorMap map_a1,
-                    const __grid_constant__ CUtensorMap map_b, FfnParams p) {
+    ffn_kernel(const __grid_constant__ CUtensorMap map_g, const __grid_constant__ CUtensorMap map_u,
+               const __grid_constant__ CUtensorMap map_x, const __grid_constant__ CUtensorMap map_d,
+               const __grid_constant__ CUtensorMap map_h, FfnParams p) {
   extern __shared__ __align__(1024) uint8_t fsm_raw[];
   __shared__ __align__(8) uint64_t full[kFfnStages], empty[kFfnStages], acc_full[2], acc_empty[2];
   __shared__ uint32_t tmem_slot;
@@ -180,10 +216,9 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint8_t* fsm = fsm_raw + ((1024u - (smem_u32(fsm_raw) & 1023u)) & 1023u);
-  const int n_units = p.E * p.tiles;
-  const int KB = p.K / kBK;
+  const int n_units = p.E * (p.tiles_gu + p.tiles_dn);
 
-  pdl_wait();  // the expert rows (and the previous GEMM's TMEM) are ready
+  pdl_wait();  // the expert rows are ready
   pdl_launch_dependents();
   if (threadIdx.x == 0) {
     for (int i = 0; i < kFfnStages; ++i) {
@@ -206,24 +241,33 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
   tc_fence_after();
   const uint32_t tmem = tmem_slot;
 
+  // Every role walks the same units: u = blockIdx.x, +grid, ... over gate/up
+  // units first, down units after, so each CTA meets its down units only once
+  // all of its own gate/up loads are issued, and CTAs whose gate/up share ran
+  // out early start on down units while others finish theirs.
   if (warp == 0) {
     if (lane == 0) {
-      // producer: B (tokens) and kT weight tiles per k-block
+      // producer: B (tokens or h1 rows) and kT weight tiles per k-block
       uint32_t it = 0;
       for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
         const Unit un = unit_of(p, u);
         const int passes = (un.n_e + kNP - 1) / kNP;
+        if (passes == 0) continue;
+        if (un.mode == FFN_DOWN && !wait_expert(p, un.e, &s_abort)) break;
+        const CUtensorMap* mb = un.mode == FFN_GATE_UP ? &map_x : &map_h;
+        const CUtensorMap* ma0 = un.mode == FFN_GATE_UP ? &map_g : &map_d;
+        const CUtensorMap* ma1 = un.mode == FFN_GATE_UP ? &map_u : &map_d;
+        const int KB = un.K / kBK;
         for (int ps = 0; ps < passes && !s_abort; ++ps) {
           for (int kb = 0; kb < KB; ++kb, ++it) {
             const uint32_t stage = it % kFfnStages, round = it / kFfnStages;
             if (round > 0 && !wait_or_abort(&empty[stage], (round - 1) & 1u, p, &s_abort)) break;
             uint8_t* st = fsm + stage * kStage;
             mbar_arrive_expect_tx(&full[stage], kStage);
-            tma_load_2d(st, &map_b, kb * kBK, (int)(un.row0 + (long long)ps * kNP), &full[stage]);
+            tma_load_2d(st, mb, kb * kBK, (int)(un.row0 + (long long)ps * kNP), &full[stage]);
 #pragma unroll
             for (int t = 0; t < kT; ++t)
-              tma_load_2d(st + kBTile + t * kATile, (MODE == FFN_GATE_UP && t == 1) ? &map_a1 : &map_a0,
-                          kb * kBK, a_row<MODE>(p, un, t), &full[stage]);
+              tma_load_2d(st + kBTile + t * kATile, t == 1 ? ma1 : ma0, kb * kBK, a_row(p, un, t), &full[stage]);
           }
         }
       }
@@ -235,6 +279,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
       for (int u = blockIdx.x; u < n_units && !s_abort; u += gridDim.x) {
         const Unit un = unit_of(p, u);
         const int passes = (un.n_e + kNP - 1) / kNP;
+        const int KB = un.K / kBK;
         for (int ps = 0; ps < passes && !s_abort; ++ps, ++acc) {
           const uint32_t buf = acc & 1u;
           if (acc >= 2 && !wait_or_abort(&acc_empty[buf], ((acc >> 1) - 1) & 1u, p, &s_abort)) break;
@@ -278,7 +323,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         const uint32_t tbase = tmem + ((uint32_t)(32 * q) << 16) + buf * (kT * kNP);
         const long long row = un.row0 + (long long)ps * kNP;
         for (int c = 0; c < chunks; ++c) {
-          if (MODE == FFN_GATE_UP) {
+          if (un.mode == FFN_GATE_UP) {
             uint32_t g[16], v[16];
             tc_ld16(tbase + c * 16, g);
             tc_ld16(tbase + kNP + c * 16, v);
@@ -289,7 +334,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
               if (n < n_rem) {
                 const float a = __uint_as_float(g[j]), b = __uint_as_float(v[j]);
                 const float h = a / (1.0f + expf(-a)) * b;
-                p.out[(row + n) * p.out_cols + un.tile * 128 + feat] = __float2bfloat16_rn(h);
+                p.h1[(row + n) * p.I + un.tile * 128 + feat] = __float2bfloat16_rn(h);
               }
             }
           } else {
@@ -302,7 +347,7 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
               for (int j = 0; j < 16; ++j) {
                 const int n = c * 16 + j;
                 if (n < n_rem)
-                  p.out[(row + n) * p.out_cols + un.tile * 256 + t * 128 + feat] =
+                  p.y[(row + n) * p.h + un.tile * 256 + t * 128 + feat] =
                       __float2bfloat16_rn(__uint_as_float(v[j]));
               }
             }
@@ -310,6 +355,15 @@ __global__ void __launch_bounds__(kFfnThreads, 1)
         }
         tc_fence_before();
         mbar_arrive(&acc_empty[buf]);
+      }
+      if (un.mode == FFN_GATE_UP && passes > 0) {
+        // this warp's h1 columns of the unit are stored: make them visible (to
+        // the async proxy too: down units read them by TMA), then count them
+        // for the expert (four warps a unit; no barrier across the warps)
+        asm volatile("fence.proxy.async.global;" ::: "memory");
+        __threadfence();
+        __syncwarp();
+        if (lane == 0) asm volatile("red.release.gpu.global.add.u32 [%0], 1;" ::"l"(p.done + un.e) : "memory");
       }
     }
   }
@@ -353,21 +407,6 @@ static bool make_map(CUtensorMap* m, const void* base, unsigned long long rows, 
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-template <int MODE>
-static cudaError_t launch_gemm(const CUtensorMap& a0, const CUtensorMap& a1, const CUtensorMap& b,
-                               const FfnParams& p, cudaStream_t st, int num_sms) {
-  auto kern = ffn_gemm_kernel<MODE>;
-  int per_sm = 0;  // one CTA per SM by design; the call raises the shared-memory limit once
-  const cudaError_t e = resident_blocks((const void*)kern, kFfnThreads, kFfnSmem, &per_sm);
-  if (e != cudaSuccess) return e;
-  if (per_sm < 1) return cudaErrorInvalidConfiguration;
-  const int units = p.E * p.tiles;
-  const int grid = units < num_sms ? units : num_sms;
-  if (grid <= 0) return cudaSuccess;
-  PdlLaunch L(dim3(grid), dim3(kFfnThreads), kFfnSmem, st);
-  return cudaLaunchKernelEx(&L.cfg, kern, a0, a1, b, p);
-}
-
 cudaError_t launch_ffn(const FfnLaunch& f, cudaStream_t st, int num_sms, void* const* prof_events) {
   const Shape& sh = f.sh;
   const unsigned long long rows = (unsigned long long)sh.W * sh.A;
@@ -379,29 +418,40 @@ cudaError_t launch_ffn(const FfnLaunch& f, cudaStream_t st, int num_sms, void* c
     return cudaErrorInvalidValue;
   FfnParams p{};
   p.ep = f.ep;
+  p.h1 = static_cast<__nv_bfloat16*>(f.h1);
+  p.y = static_cast<__nv_bfloat16*>(f.y);
+  p.done = f.done;
   p.W = sh.W;
   p.L = sh.L;
   p.E = sh.E;
   p.A = sh.A;
+  p.h = sh.h;
+  p.I = f.I;
+  p.tiles_gu = f.I / 128;
+  p.tiles_dn = sh.h / 256;
   p.status = f.status;
   p.timeout_ns = f.timeout_ns;
 
-  p.out = static_cast<__nv_bfloat16*>(f.h1);
-  p.K = sh.h;
-  p.out_cols = f.I;
-  p.tiles = f.I / 128;
-  p.a_rows = f.I;
+  int per_sm = 0;  // one CTA per SM by design; the call raises the shared-memory limit once
+  cudaError_t e = resident_blocks((const void*)ffn_kernel, kFfnThreads, kFfnSmem, &per_sm);
+  if (e != cudaSuccess) return e;
+  if (per_sm < 1) return cudaErrorInvalidConfiguration;
+  // every CTA must be resident at once (down units wait on other CTAs' gate/up
+  // units): one per SM, no more than the SMs
+  const int units = p.E * (p.tiles_gu + p.tiles_dn);
+  const int grid = units < num_sms ? units : num_sms;
+  if (grid <= 0) return cudaSuccess;
   if (prof_events && prof_events[0]) cudaEventRecord(static_cast<cudaEvent_t>(prof_events[0]), st);
-  cudaError_t e = launch_gemm<FFN_GATE_UP>(mg, mu, mx, p, st, num_sms);
+  PdlLaunch L(dim3(grid), dim3(kFfnThreads), kFfnSmem, st);
+  cudaLaunchAttribute attr[2] = {L.attr[0], {}};
+  attr[1].id = cudaLaunchAttributeCooperative;  // co-residency of all CTAs is required
+  attr[1].val.cooperative = 1;
+  L.cfg.attrs = attr;
+  L.cfg.numAttrs = 2;
+  e = cudaLaunchKernelEx(&L.cfg, ffn_kernel, mg, mu, mx, md, mh, p);
   if (e != cudaSuccess) return e;
   if (prof_events && prof_events[1]) cudaEventRecord(static_cast<cudaEvent_t>(prof_events[1]), st);
-
-  p.out = static_cast<__nv_bfloat16*>(f.y);
-  p.K = f.I;
-  p.out_cols = sh.h;
-  p.tiles = sh.h / 256;
-  p.a_rows = sh.h;
-  return launch_gemm<FFN_DOWN>(md, md, mh, p, st, num_sms);
+  return cudaSuccess;
 }
 
 }  // namespace crs

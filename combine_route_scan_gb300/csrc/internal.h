@@ -44,6 +44,7 @@ struct WsLayout {
   size_t ffn_ep;         // int32 [W][L*W]
   size_t ffn_h1;         // bf16 [W*A][I]
   size_t ffn_y;          // bf16 [W*A][h]
+  size_t ffn_done;       // uint32 [E] gate/up epilogue warps finished per expert
   size_t total;
 };
 
@@ -79,6 +80,8 @@ struct RouteParams {
   uint32_t ticket;
   WsHeader* hdr;           // records which assist_info / ep_recv_count the pick -> row map belongs to
   const int32_t* assist_out;
+  uint32_t* zero_words;    // optional: words the routing kernel clears for the kernels after it
+  int n_zero_words;
 };
 
 struct ScatterParams {
@@ -144,6 +147,7 @@ struct FfnLaunch {
   void* h1;                // [W*A][I] bf16
   void* y;                 // [W*A][h] bf16 (expert outputs)
   const int32_t* ep;       // [W][L*W] running receive counts
+  uint32_t* done;          // [E] per-expert gate/up completion counters (cleared by the routing kernel)
   int* status;
   uint64_t timeout_ns;
 };

@@ -172,6 +172,7 @@ WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
     L.ffn_ep = take(segs * 4);
     L.ffn_h1 = take(rows * (size_t)c->ffn_intermediate * 2);
     L.ffn_y = take(rows * sh.h * 2);
+    L.ffn_done = take((size_t)sh.E * 4);
   }
   L.total = off;
   return L;
@@ -512,6 +513,8 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   rp.status = &hdr->status;
   rp.hdr = hdr;
   rp.assist_out = assist;
+  rp.zero_words = reinterpret_cast<uint32_t*>(w + L.ffn_done);
+  rp.n_zero_words = sh.E;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
   note_launches(1);
   ScatterParams sp{};
@@ -544,10 +547,11 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   f.h1 = w + L.ffn_h1;
   f.y = w + L.ffn_y;
   f.ep = ep;
+  f.done = reinterpret_cast<uint32_t*>(w + L.ffn_done);
   f.status = &hdr->status;
   f.timeout_ns = timeout_ns(cfg);
   if (launch_ffn(f, s, nsm, cfg->prof_events) != cudaSuccess) return MOE_ERR_CUDA;
-  note_launches(2);
+  note_launches(1);
 
   // 3. combine the expert outputs
   CombineParams cp{};

@@ -341,6 +341,9 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     if (valid) keys[(size_t)t * K + k] = r;
   }
 
+  // counters of the kernels that follow in the same call start from zero
+  if (s == 0)
+    for (int i = tid; i < p.n_zero_words; i += kRouteThreads) p.zero_words[i] = 0u;
   // the scatter that follows writes the pick -> row map and hands out tokens
   // by ticket; these stores come after every release of this CTA, so no
   // barrier waits for them
