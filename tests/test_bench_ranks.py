@@ -72,3 +72,15 @@ def test_reference_arm_runs_on_rank_zero_only(monkeypatch, capsys):
         gpus = 2
     assert B.run_reference(A()) == 0
     assert capsys.readouterr().out == ""
+
+
+def test_rotation_sets_keep_steps_out_of_l2():
+    """Timed regions rotate over enough buffer sets that a set's data has left
+    the L2 before it is used again; a step larger than four L2s needs one."""
+    B = _bench()
+    assert B.rotation_sets(4 * B.L2_BYTES) == 1
+    assert B.rotation_sets(931_000_000) == 1
+    n = B.rotation_sets(66_000_000)
+    assert n >= 2 and n * 66_000_000 >= 4 * B.L2_BYTES and (n - 1) * 66_000_000 < 4 * B.L2_BYTES
+    cfg = B.bench_config(B.WL.WORKLOADS["w8_bs32_h7168_k8_e64_f16"], None, 66_000_000)
+    assert f"{n} buffer sets" in cfg["l2"]
