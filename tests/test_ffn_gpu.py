@@ -102,3 +102,29 @@ def test_ffn_unsupported_shapes():
         M.dispatch_ffn_combine(cfg, t, t, None, t, t, t, t, t, ws=torch.zeros(1 << 20, dtype=torch.uint8,
                                                                                device="cuda"))
     assert ei.value.name == "UNSUPPORTED"
+
+
+def test_ffn_call_replays_from_a_cuda_graph():
+    """The fused call (cooperative FFN kernel chained by programmatic
+    dependent launch) captures into a CUDA graph; replays give the eager
+    call's bytes."""
+    wl = WL.Workload("ffn_graph", 4, 32, 512, 4, 16, WL.X_BF16, ffn_intermediate=256, seed=25)
+    inp = WL.make_inputs(wl)
+    eager, _ = run_ffn(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    w = {k: H.to_dev(inp[k], WL.X_BF16) for k in ("w_gate", "w_up", "w_down")}
+    cfg = H.make_cfg(wl, ffn_intermediate=wl.ffn_intermediate)
+    ws = M.alloc_workspace(cfg)
+    x_out = torch.empty_like(dev["x"])
+    torch.cuda.synchronize()
+    graph = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(graph, stream=torch.cuda.Stream()):
+        M.dispatch_ffn_combine(cfg, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"],
+                               w["w_gate"], w["w_up"], w["w_down"], x_out, ws)
+    for _ in range(2):
+        x_out.view(torch.uint8).fill_(0x7F)
+        graph.replay()
+        torch.cuda.synchronize()
+        assert M.get_device_status(ws) == 0
+        got = WL.bf16_bits_to_fp32(H.to_host(x_out)).astype(np.float64).reshape(-1, wl.h)
+        assert np.array_equal(got, eager)
