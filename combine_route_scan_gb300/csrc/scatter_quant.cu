@@ -110,6 +110,32 @@ __device__ __forceinline__ int token_q(float v, float scale) {
   return max(-127, min(127, __float2int_rn(__fdiv_rn(v, scale))));
 }
 
+// Per-token int8 code from the reciprocal r = 1/scale (rounded once): y = v*r
+// is within 2^-23 |y| of v/scale and the IEEE quotient within half an ulp of
+// it, so y rounded to the nearest integer (adding 1.5 * 2^23 leaves it, ties to
+// even, in the low mantissa bits) is the code of the quotient unless y lies
+// within 2^-14 of a half-integer: those, and NaN, take the division. For
+// |v| <= amax and a normal scale, |y| <= 127.00003 needs no clamp. The code is
+// the low byte of the returned word.
+constexpr float kRoundShift = 12582912.0f;  // 1.5 * 2^23
+constexpr float kNearHalf = 0.5f - 0.00006103515625f;  // 0.5 - 2^-14
+__device__ __forceinline__ uint32_t token_code(float v, float scale, float rcp) {
+  const float y = __fmul_rn(v, rcp);
+  const float t = __fadd_rn(y, kRoundShift);
+  const float d = fabsf(__fsub_rn(y, __fsub_rn(t, kRoundShift)));
+  return d <= kNearHalf ? __float_as_uint(t) : (uint32_t)token_q(v, scale);
+}
+// the reciprocal form holds for a normal, finite scale (an all-zero row, a
+// subnormal or infinite scale quantise through the division)
+__device__ __forceinline__ bool token_rcp_ok(float scale) { return scale >= 1.17549435e-38f && scale <= 3.40282347e38f; }
+
+// low bytes of c[0..8) as 8 consecutive bytes
+__device__ __forceinline__ uint2 pack8_low(const uint32_t (&c)[8]) {
+  const uint32_t a = __byte_perm(__byte_perm(c[0], c[1], 0x0040), __byte_perm(c[2], c[3], 0x0040), 0x5410);
+  const uint32_t b = __byte_perm(__byte_perm(c[4], c[5], 0x0040), __byte_perm(c[6], c[7], 0x0040), 0x5410);
+  return make_uint2(a, b);
+}
+
 __device__ __forceinline__ uint2 pack8(const int (&q)[8]) {
   uint32_t a = 0, b = 0;
 #pragma unroll
@@ -191,6 +217,62 @@ __device__ __forceinline__ void put_dyn(const RowSink& k, int g, T v) {
   }
 }
 
+// Per-token int8, first pass: the maximum of |x| (times srow when smoothing)
+// over this thread's vectors of the row (the CTA's threads share them out),
+// reduced over the warp; max is order-free, so any split gives the same value.
+template <int DT>
+__device__ __forceinline__ float token_amax_warp(const uint8_t* row, const float* srow, uint32_t nvec) {
+  float m = 0.f;
+  for (uint32_t v = threadIdx.x; v < nvec; v += kScatterThreads) {
+    float f[8];
+    unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+    if (srow) {
+      float sc[8];
+      load_scales8(srow, v, sc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
+    }
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+  return m;
+}
+
+// Per-token int8, second pass: scale = amax / 127 and the codes
+// round(x / scale) clamped to [-127, 127] (all zeros for an all-zero row).
+// RCP: through the reciprocal (token_code). Measured on GB300, it pays where
+// the arithmetic bounds the kernel (per-expert smoothing: one quantisation a
+// pick) and not on the per-token form, whose HBM traffic hides the divisions.
+template <int SINK, int DT, bool RCP>
+__device__ __forceinline__ void token_codes(const uint8_t* row, const float* srow, const RowSink& k, uint32_t nvec,
+                                            float amax) {
+  const float scale = __fdiv_rn(amax, 127.0f);
+  const bool fast = RCP && token_rcp_ok(scale);
+  const float rcp = fast ? __frcp_rn(scale) : 0.f;
+  for (uint32_t v = threadIdx.x; v < nvec; v += kScatterThreads) {
+    float f[8];
+    unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
+    if (srow) {
+      float sc[8];
+      load_scales8(srow, v, sc);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
+    }
+    uint32_t c[8];
+    if (fast) {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = token_code(f[i], scale, rcp);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = amax == 0.f ? 0u : (uint32_t)token_q(f[i], scale);
+    }
+    put<SINK>(k, v * 8, pack8_low(c));
+  }
+  if (threadIdx.x == 0) put_dyn<SINK, float>(k, 0, scale);
+}
+
 // Quantises the staged row (elements times srow, or s0 for a (1,) coefficient)
 // into the sink. Threads t0, t0 + nt, ... take the row's 16-byte vectors: the
 // whole CTA (t0 = threadIdx.x, nt = the CTA size), or for modes 1 and 3, whose
@@ -217,42 +299,13 @@ __device__ __forceinline__ void quantize_variant(const uint8_t* row, const float
       put<SINK>(k, v * 8, pack8(qv));
     }
   } else if (MODE == 2) {
-    float m = 0.f;
-    for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-      float f[8];
-      unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-      if (srow) {
-        float sc[8];
-        load_scales8(srow, v, sc);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
-      }
-#pragma unroll
-      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
-    }
-#pragma unroll
-    for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    const float m = token_amax_warp<DT>(row, srow, nvec);
     if (lane == 0) s_red[warp] = m;
     __syncthreads();
     float amax = 0.f;
 #pragma unroll
     for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[w]);
-    const float scale = __fdiv_rn(amax, 127.0f);
-    for (uint32_t v = tid; v < nvec; v += kScatterThreads) {
-      float f[8];
-      unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-      if (srow) {
-        float sc[8];
-        load_scales8(srow, v, sc);
-#pragma unroll
-        for (int i = 0; i < 8; ++i) f[i] = __fmul_rn(f[i], sc[i]);
-      }
-      int qv[8];
-#pragma unroll
-      for (int i = 0; i < 8; ++i) qv[i] = amax == 0.f ? 0 : token_q(f[i], scale);
-      put<SINK>(k, v * 8, pack8(qv));
-    }
-    if (tid == 0) put_dyn<SINK, float>(k, 0, scale);
+    token_codes<SINK, DT, true>(row, srow, k, nvec, amax);
   } else {
     // a group (mode 3: 16 vectors) or block (mode 4: 4 vectors) is a run of
     // neighbouring lanes; every lane of a warp takes part in the shuffles,
@@ -323,15 +376,22 @@ __device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, con
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float scale = __fdiv_rn(m, 127.0f);
+  const bool fast = token_rcp_ok(scale);
+  const float rcp = fast ? __frcp_rn(scale) : 0.f;
   uint8_t* q = out + dst * row_out;
   for (uint32_t v = lane; v < nvec; v += 32) {
     float f[8], sc[8];
     unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
     load_scales8(srow, v, sc);
-    int qv[8];
+    uint32_t c[8];
+    if (fast) {
 #pragma unroll
-    for (int i = 0; i < 8; ++i) qv[i] = m == 0.f ? 0 : token_q(__fmul_rn(f[i], sc[i]), scale);
-    *reinterpret_cast<uint2*>(q + v * 8) = pack8(qv);
+      for (int i = 0; i < 8; ++i) c[i] = token_code(__fmul_rn(f[i], sc[i]), scale, rcp);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) c[i] = m == 0.f ? 0u : (uint32_t)token_q(__fmul_rn(f[i], sc[i]), scale);
+    }
+    *reinterpret_cast<uint2*>(q + v * 8) = pack8_low(c);
   }
   if (lane == 0) reinterpret_cast<float*>(dyn)[dst] = scale;
 }
@@ -391,6 +451,10 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
   // capped at five CTAs per SM); the static-scale and per-expert forms,
   // whose tokens cost little or a great deal, keep loading on the spot.
   constexpr bool kAhead = MODE != 1 && !PE;
+  // per-token int8 without smoothing: one CTA barrier a token (s_red
+  // alternates by token: a half is written again only after the next token's
+  // barrier, which every thread passes after reading it)
+  constexpr bool kMerge = MODE == 2 && !PE;
   PickAhead cur{}, nxt{};
   if (kAhead && warp == 0 && my_n > 0) {
     pick_load_first(p, blockIdx.x, cur);
@@ -410,6 +474,12 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     // the buffer of this token's first shared variant was last read by the
     // bulk group two variants back: at most one newer group may still read
     if (tid == 0) bulk_wait_read<1>();
+    if constexpr (kMerge) {
+      // per-token int8: the row maximum's first pass goes before the token's
+      // barrier, which then publishes the warps' maxima with the pick table
+      const float m = token_amax_warp<DT>(row, nullptr, nvec);
+      if ((tid & 31) == 0) s_red[i & 1][warp] = m;
+    }
     if (warp == 0) {
       if constexpr (kAhead) {
         build_picks_from(p, tau, s, t, tab, cur);
@@ -442,6 +512,11 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     // (a scale per 128 elements and destination) leave faster through the
     // shared buffer as 16-byte stores and coalesced scale rows
     const bool direct = nbk == 0 && YT != MOE_Y_FP4_E2M1 && MODE != 3;
+    float amax = 0.f;
+    if constexpr (kMerge) {
+#pragma unroll
+      for (int w = 0; w < kScatterWarps; ++w) amax = fmaxf(amax, s_red[i & 1][w]);
+    }
 
     // store-plane picks straight from registers: each pick on its own with
     // per-expert scales, else one pass for all of them when the token has no
@@ -460,7 +535,10 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
       }
     } else if (direct && nsm > 0) {
       const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
-      quantize_variant<MODE, DT, YT, kMany>(row, chan, s0, k, nvec, s_red[nvr++ & 1]);
+      if constexpr (kMerge)
+        token_codes<kMany, DT, false>(row, nullptr, k, nvec, amax);
+      else
+        quantize_variant<MODE, DT, YT, kMany>(row, chan, s0, k, nvec, s_red[nvr++ & 1]);
     }
 
     // variants through the shared buffers: one per bulk-plane pick (per-expert
@@ -478,7 +556,10 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
       }
       const float* srow = PE ? p.qscales + (size_t)(tab.bulk_seg[j - nsm] / sh.W) * sh.h : chan;
       const RowSink k{q, dq, nullptr, 0, out, dyn, row_out, nd};
-      quantize_variant<MODE, DT, YT, kShared>(row, srow, s0, k, nvec, s_red[nvr++ & 1]);
+      if constexpr (kMerge)
+        token_codes<kShared, DT, false>(row, nullptr, k, nvec, amax);
+      else
+        quantize_variant<MODE, DT, YT, kShared>(row, srow, s0, k, nvec, s_red[nvr++ & 1]);
       fence_proxy_async_smem();
       __syncthreads();
 

@@ -94,6 +94,60 @@ def test_quant_values_cover_the_ranges():
         H.compare_dispatch(w, got, ref)
 
 
+def _to_input_type(x: np.ndarray, dt: str) -> np.ndarray:
+    x = x.astype(np.float32)
+    return x.astype(np.float16) if dt == WL.X_FP16 else WL.fp32_to_bf16_bits(x)
+
+
+def _from_input_type(x: np.ndarray, dt: str) -> np.ndarray:
+    return x.astype(np.float32) if dt == WL.X_FP16 else WL.bf16_bits_to_fp32(x)
+
+
+@pytest.mark.parametrize("dt", [WL.X_BF16, WL.X_FP16])
+@pytest.mark.parametrize("k", [0, 3])
+def test_token_int8_ties_and_near_half_quotients(dt, k):
+    """Per-token int8 where x / scale lands on or next to half-integers, the
+    cases where rounding the quotient is most fragile. Even tokens: the row
+    maximum is 127 * 2^j, so the scale is 2^j exactly, and every other element
+    is (n + 1/2) * 2^j: exact ties, which round to even. Odd tokens: a random
+    maximum, and elements the input type's nearest value to (n + 1/2) * scale
+    for small n, so many quotients fall within 2^-14 of a half-integer
+    without being one. With smoothing each expert's scales row is one power of
+    two, which keeps the products on the same points. Bytes against the oracle."""
+    W, bs, h, E = 2, 16, 512, 8
+    wl = WL.Workload("qt", W, bs, h, 4, E, dt, quant_mode=2, scales_kind=k, seed=36)
+    inp = WL.make_inputs(wl)
+    rng = np.random.Generator(np.random.PCG64(360))
+    x = np.zeros((W, bs, h), np.float32)
+    for s in range(W):
+        for t in range(bs):
+            if t % 2 == 0:
+                j = float(rng.integers(-4, 5))
+                row = (rng.integers(-127, 127, size=h) + 0.5) * 2.0 ** j
+                row[0] = 127.0 * 2.0 ** j
+            else:
+                amax = _from_input_type(_to_input_type(np.array([rng.uniform(1.0, 100.0)]), dt), dt)[0]
+                scale = np.float32(amax) / np.float32(127.0)
+                row = (rng.integers(-4, 4, size=h) + 0.5) * np.float64(scale)
+                row[0] = amax
+            x[s, t] = row
+    inp["x"] = _to_input_type(x, dt)
+    if k == 3:
+        inp["quant_scales"] = np.repeat(2.0 ** rng.integers(-2, 3, size=(E, 1)), h, axis=1).astype(np.float32)
+
+    # the case mix really is there: quotients within 2^-14 of a half-integer
+    xf = _from_input_type(inp["x"], dt)
+    amax = np.abs(xf).max(axis=2, keepdims=True)
+    q = xf / (amax / np.float32(127.0))
+    near = np.abs(np.abs(q - np.floor(q)) - np.float32(0.5)) <= np.float32(2.0 ** -14)
+    assert near[:, 0::2].mean() > 0.9 and near[:, 1::2].sum() > 100
+
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    H.compare_dispatch(wl, got, ref)
+
+
 def test_quant_ready_flags_and_performance_info():
     """The quantising scatter publishes ready flags and per-rank times too."""
     wl = WL.Workload("qf", 4, 24, 512, 4, 16, WL.X_BF16, quant_mode=3, y_dtype="fp8_e4m3", scales_kind=3, seed=35)
