@@ -148,6 +148,46 @@ def test_token_int8_ties_and_near_half_quotients(dt, k):
     H.compare_dispatch(wl, got, ref)
 
 
+@pytest.mark.parametrize("dt", [WL.X_BF16, WL.X_FP16])
+@pytest.mark.parametrize("k", [0, 3])
+@pytest.mark.parametrize("y", ["fp8_e4m3", "fp8_e5m2"])
+def test_group_fp8_ties_and_near_midpoint_quotients(y, k, dt):
+    """Per-group FP8 where x / scale lands on or next to a midpoint of two
+    neighbouring FP8 values, the cases where rounding the quotient is most
+    fragile. Each 128-element group's maximum is fmax * 2^j (scale 2^j
+    exactly) and its other elements are (m + 1/2) * 2^(e - mbits) * 2^j, the
+    format's midpoints: exact ties. With smoothing each expert's scales row is
+    one value 1 + r * 2^-10, so the rounded products and the rounded scale
+    move every quotient a few fp32 ulps off the midpoint. Bytes against the
+    oracle."""
+    W, bs, h, E = 2, 16, 512, 8
+    fmax, mbits, e_top = (448.0, 3, 8) if y == "fp8_e4m3" else (57344.0, 2, 15)
+    wl = WL.Workload("qg", W, bs, h, 4, E, dt, quant_mode=3, y_dtype=y, scales_kind=k, seed=37)
+    inp = WL.make_inputs(wl)
+    rng = np.random.Generator(np.random.PCG64(370))
+    n_groups = h // 128
+    x = np.zeros((W, bs, h), np.float64)
+    for s in range(W):
+        for t in range(bs):
+            for g in range(n_groups):
+                j = float(rng.integers(-3, 1))
+                e = rng.integers(e_top - 6, e_top + 1, size=128)
+                m = rng.integers(2 ** mbits, 2 ** (mbits + 1), size=128)
+                mid = np.minimum((m + 0.5) * 2.0 ** (e - mbits), fmax) * rng.choice([-1.0, 1.0], size=128)
+                mid[0] = fmax
+                x[s, t, g * 128:(g + 1) * 128] = mid * 2.0 ** j
+    inp["x"] = _to_input_type(x, dt)
+    assert np.array_equal(_from_input_type(inp["x"], dt).astype(np.float64), x)  # exactly representable
+    if k == 3:
+        r = 1.0 + rng.integers(1, 1024, size=(E, 1)) * 2.0 ** -10
+        inp["quant_scales"] = np.repeat(r, h, axis=1).astype(np.float32)
+
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    got, _, _ = H.gpu_dispatch(wl, dev)
+    H.compare_dispatch(wl, got, ref)
+
+
 def test_quant_ready_flags_and_performance_info():
     """The quantising scatter publishes ready flags and per-rank times too."""
     wl = WL.Workload("qf", 4, 24, 512, 4, 16, WL.X_BF16, quant_mode=3, y_dtype="fp8_e4m3", scales_kind=3, seed=35)
