@@ -19,6 +19,8 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <atomic>
+
 #include "scatter_common.cuh"
 
 namespace crs {
@@ -261,18 +263,20 @@ static cudaError_t launch_persistent(KernelT kernel, const ScatterParams& p, cud
 
 // L2 size of the current device in bytes (cached per device; 0 if unknown).
 static long long l2_bytes_of_current_device() {
-  static long long l2[64] = {};
+  static std::atomic<long long> l2[64] = {};  // callers may be on several host threads
   int dev = 0;
   if (cudaGetDevice(&dev) != cudaSuccess || dev < 0 || dev >= 64) return 0;
-  if (l2[dev] == 0) {
+  long long b = l2[dev].load(std::memory_order_relaxed);
+  if (b == 0) {
     int v = 0;
     if (cudaDeviceGetAttribute(&v, cudaDevAttrL2CacheSize, dev) != cudaSuccess) {
       cudaGetLastError();
       return 0;
     }
-    l2[dev] = v;
+    b = v;
+    l2[dev].store(b, std::memory_order_relaxed);
   }
-  return l2[dev];
+  return b;
 }
 
 // Shared-memory budget of the TMA scatter for `stages` slots.
