@@ -187,6 +187,56 @@ struct RowSink {
 // so the warps of a CTA quantise different picks at once), then the codes
 // straight to the pick's row. Same arithmetic, same order-free maximum, same
 // bytes as the CTA-wide form.
+// MX FP8 with each 32-element block on a lane pair: a thread takes two
+// 16-byte vectors (read in an order rotated by (lane / 4) % 2, so that the
+// eight lanes of a shared-memory phase hit distinct banks), the pair's
+// maximum comes from one shuffle, and the thread's 16 bytes of codes leave by
+// one 16-byte store per destination, neighbouring threads adjacent. The even
+// lane writes the block's E8M0 byte. Same arithmetic as the vector-per-thread
+// form. Needs whole blocks (h a multiple of 32).
+template <int DT, int YT>
+__device__ __forceinline__ void quantize_mx8_half_blocks(const uint8_t* row, const RowSink& k, uint32_t nhalf) {
+  const uint32_t rot = (threadIdx.x >> 2) & 1u;
+  for (uint32_t base = 0; base < nhalf; base += kScatterThreads) {
+    const uint32_t hb = base + threadIdx.x;
+    const bool valid = hb < nhalf;  // nhalf is even: a pair is valid or not as a whole
+    int4 raw[2] = {make_int4(0, 0, 0, 0), make_int4(0, 0, 0, 0)};  // raw[j] = vector 2hb + (j ^ rot)
+    if (valid) {
+#pragma unroll
+      for (int j = 0; j < 2; ++j) raw[j] = *reinterpret_cast<const int4*>(row + (hb * 2 + (j ^ rot)) * 16);
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float f[8];
+      unpack8<DT>(raw[j], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    }
+    m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, 1));
+    if (!valid) continue;
+    const int se = mx_exponent(m, elem_emax(YT));
+    const float inv = exp2_exact(-se);
+    uint32_t w[4];  // w[2j], w[2j+1]: the codes of raw[j]
+#pragma unroll
+    for (int j = 0; j < 2; ++j) {
+      float f[8];
+      unpack8<DT>(raw[j], f);
+      uint32_t c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = cvt_fp8x2<YT>(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
+      w[2 * j] = c[0] | (c[1] << 16);
+      w[2 * j + 1] = c[2] | (c[3] << 16);
+    }
+    const int4 val = rot ? make_int4((int)w[2], (int)w[3], (int)w[0], (int)w[1])
+                         : make_int4((int)w[0], (int)w[1], (int)w[2], (int)w[3]);
+    for (int d = 0; d < k.n; ++d) {
+      st_v4(k.out + k.dst[d] * k.row_out + hb * 16, val);
+      if ((hb & 1u) == 0) k.dyn[k.dst[d] * k.nd + (hb >> 1)] = (uint8_t)(se + 127);
+    }
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, const float* srow, uint8_t* out,
                                                          uint8_t* dyn, long long dst, uint32_t row_out,
@@ -360,6 +410,78 @@ __device__ __forceinline__ void quantize_variant(const uint8_t* row, const float
   }
 }
 
+// int8 codes straight to every destination of k, two neighbouring 16-byte
+// vectors a thread (read in an order rotated by (lane / 4) % 2, so that the
+// eight lanes of a shared-memory phase hit distinct banks) and one 16-byte
+// store per destination, neighbouring threads adjacent. codes8(f, v) gives
+// the 8 code bytes of vector v from its elements f. nvec must be even.
+template <int DT, typename Codes8>
+__device__ __forceinline__ void int8_codes_pairs(const uint8_t* row, const RowSink& k, uint32_t nvec,
+                                                 Codes8 codes8) {
+  const uint32_t rot = (threadIdx.x >> 2) & 1u;
+  for (uint32_t pv = threadIdx.x; pv < nvec / 2; pv += kScatterThreads) {
+    const uint32_t va = 2 * pv + rot, vb = 2 * pv + (rot ^ 1u);
+    float f[8];
+    unpack8<DT>(*reinterpret_cast<const int4*>(row + va * 16), f);
+    const uint2 ca = codes8(f, va);
+    unpack8<DT>(*reinterpret_cast<const int4*>(row + vb * 16), f);
+    const uint2 cb = codes8(f, vb);
+    const int4 val = rot ? make_int4((int)cb.x, (int)cb.y, (int)ca.x, (int)ca.y)
+                         : make_int4((int)ca.x, (int)ca.y, (int)cb.x, (int)cb.y);
+    for (int d = 0; d < k.n; ++d) st_v4(k.out + k.dst[d] * k.row_out + pv * 16, val);
+  }
+}
+
+// MX FP4 with each 32-element block in one thread: its four 16-byte vectors
+// are read from the staged row (in an order rotated by (lane / 2) % 4, so
+// that the eight lanes of a shared-memory phase hit distinct banks), the
+// block maximum gives the E8M0 exponent, and the 16 bytes of codes leave by
+// one 16-byte store per destination, neighbouring threads' blocks adjacent.
+// Same arithmetic, element by element, as the vector-per-thread form.
+template <int DT>
+__device__ __forceinline__ void quantize_fp4_blocks(const uint8_t* row, const RowSink& k, uint32_t nblk) {
+  const uint32_t rot = (threadIdx.x >> 1) & 3u;
+  for (uint32_t b = threadIdx.x; b < nblk; b += kScatterThreads) {
+    int4 raw[4];  // raw[j] = vector 4b + ((j + rot) & 3)
+#pragma unroll
+    for (int j = 0; j < 4; ++j) raw[j] = *reinterpret_cast<const int4*>(row + (b * 4 + ((j + rot) & 3u)) * 16);
+    float m = 0.f;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      unpack8<DT>(raw[j], f);
+#pragma unroll
+      for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(f[i]));
+    }
+    const int se = mx_exponent(m, elem_emax(MOE_Y_FP4_E2M1));
+    const float inv = exp2_exact(-se);
+    uint32_t w[4];  // w[j]: the codes of raw[j]
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      float f[8];
+      unpack8<DT>(raw[j], f);
+      uint32_t c[4];
+#pragma unroll
+      for (int i = 0; i < 4; ++i) c[i] = cvt_fp4x2(__fmul_rn(f[2 * i], inv), __fmul_rn(f[2 * i + 1], inv));
+      w[j] = c[0] | (c[1] << 8) | (c[2] << 16) | (c[3] << 24);
+    }
+    // back to vector order: word v holds w[(v - rot) & 3]
+    if (rot & 1u) {
+      const uint32_t t = w[3];
+      w[3] = w[2]; w[2] = w[1]; w[1] = w[0]; w[0] = t;
+    }
+    if (rot & 2u) {
+      uint32_t t = w[0]; w[0] = w[2]; w[2] = t;
+      t = w[1]; w[1] = w[3]; w[3] = t;
+    }
+    const int4 val = make_int4((int)w[0], (int)w[1], (int)w[2], (int)w[3]);
+    for (int d = 0; d < k.n; ++d) {
+      st_v4(k.out + k.dst[d] * k.row_out + b * 16, val);
+      k.dyn[k.dst[d] * k.nd + b] = (uint8_t)(se + 127);
+    }
+  }
+}
+
 template <int DT>
 __device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, const float* srow, uint8_t* out,
                                                          uint8_t* dyn, long long dst, uint32_t row_out,
@@ -508,10 +630,16 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
       }
     }
     const int nsm = tab.n_sm, nbk = tab.n_bulk;
-    // measured on GB300: FP4 rows (4-byte codes a thread) and per-group rows
-    // (a scale per 128 elements and destination) leave faster through the
-    // shared buffer as 16-byte stores and coalesced scale rows
+    // Tokens with no bulk-plane pick store their codes straight from
+    // registers. Measured on GB300: FP4 rows with a vector a thread (4-byte
+    // codes) and per-group rows (a scale per 128 elements and destination)
+    // leave faster through the shared buffer as 16-byte stores and coalesced
+    // scale rows; MX rows of whole blocks leave fastest with a block (FP4) or
+    // half a block (FP8) a thread and 16-byte stores (direct4: FP4 47 -> 39
+    // us, MX FP8 54 -> 52 us at the bench shape), per-token int8 rows with two
+    // vectors a thread (53.2 -> 52.0 us; static int8 was 1% slower that way).
     const bool direct = nbk == 0 && YT != MOE_Y_FP4_E2M1 && MODE != 3;
+    const bool direct4 = MODE == 4 && !PE && nbk == 0 && sh.h % 32 == 0;
     float amax = 0.f;
     if constexpr (kMerge) {
 #pragma unroll
@@ -533,18 +661,38 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
           quantize_variant<MODE, DT, YT, kOne>(row, srow, s0, k, nvec, nullptr, tid & 31, 32);
         }
       }
+    } else if (direct4) {
+      if (nsm > 0) {
+        const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
+        if constexpr (YT == MOE_Y_FP4_E2M1)
+          quantize_fp4_blocks<DT>(row, k, (uint32_t)nd);
+        else
+          quantize_mx8_half_blocks<DT, YT>(row, k, (uint32_t)nd * 2);
+      }
     } else if (direct && nsm > 0) {
       const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
-      if constexpr (kMerge)
-        token_codes<kMany, DT, false>(row, nullptr, k, nvec, amax);
-      else
+      if constexpr (kMerge) {
+        if (nvec % 2 == 0) {
+          const float scale = __fdiv_rn(amax, 127.0f);
+          int8_codes_pairs<DT>(row, k, nvec, [&](const float(&f)[8], uint32_t) {
+            int qv[8];
+#pragma unroll
+            for (int i = 0; i < 8; ++i) qv[i] = amax == 0.f ? 0 : token_q(f[i], scale);
+            return pack8(qv);
+          });
+          if (tid == 0) put_dyn<kMany, float>(k, 0, scale);
+        } else {
+          token_codes<kMany, DT, false>(row, nullptr, k, nvec, amax);
+        }
+      } else {
         quantize_variant<MODE, DT, YT, kMany>(row, chan, s0, k, nvec, s_red[nvr++ & 1]);
+      }
     }
 
     // variants through the shared buffers: one per bulk-plane pick (per-expert
     // scales), or one for all picks when some go by bulk copies
     const int j0 = PE ? nsm : 0;
-    const int j1 = PE ? nsm + nbk : (!direct && nsm + nbk > 0 ? 1 : 0);
+    const int j1 = PE ? nsm + nbk : (!direct && !direct4 && nsm + nbk > 0 ? 1 : 0);
     for (int j = j0; j < j1; ++j) {
       const int qs = nv & 1;
       ++nv;
