@@ -432,6 +432,51 @@ __device__ __forceinline__ void int8_codes_pairs(const uint8_t* row, const RowSi
   }
 }
 
+// Per-group FP8 with two neighbouring vectors a thread (read in an order
+// rotated by (lane / 4) % 2 for distinct shared-memory banks): a 128-element
+// group lies on 8 aligned lanes, its maximum comes from three shuffles, the
+// thread's 16 bytes of codes leave by one 16-byte store per destination and
+// the group's first lane writes its fp32 scale. Past-the-end lanes take part
+// in the shuffles with zeros. Same arithmetic as the vector-a-thread form.
+// nvec must be even.
+template <int DT, int YT>
+__device__ __forceinline__ void quantize_group_fp8_pairs(const uint8_t* row, const RowSink& k, uint32_t nvec) {
+  const uint32_t rot = (threadIdx.x >> 2) & 1u;
+  const uint32_t npair = nvec / 2;
+  for (uint32_t base = 0; base < npair; base += kScatterThreads) {
+    const uint32_t pv = base + threadIdx.x;
+    const bool valid = pv < npair;
+    float fa[8], fb[8];  // vectors 2pv + rot and 2pv + (rot ^ 1)
+    if (valid) {
+      unpack8<DT>(*reinterpret_cast<const int4*>(row + (2 * pv + rot) * 16), fa);
+      unpack8<DT>(*reinterpret_cast<const int4*>(row + (2 * pv + (rot ^ 1u)) * 16), fb);
+    } else {
+#pragma unroll
+      for (int i = 0; i < 8; ++i) fa[i] = fb[i] = 0.f;
+    }
+    float m = 0.f;
+#pragma unroll
+    for (int i = 0; i < 8; ++i) m = fmaxf(m, fmaxf(fabsf(fa[i]), fabsf(fb[i])));
+#pragma unroll
+    for (int o = 4; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
+    if (!valid) continue;
+    const float scale = __fdiv_rn(m, fp8_max(YT));
+    uint32_t ca[4], cb[4];
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      ca[i] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(fa[2 * i], scale), __fdiv_rn(fa[2 * i + 1], scale));
+      cb[i] = m == 0.f ? 0u : cvt_fp8x2<YT>(__fdiv_rn(fb[2 * i], scale), __fdiv_rn(fb[2 * i + 1], scale));
+    }
+    const uint32_t a0 = ca[0] | (ca[1] << 16), a1 = ca[2] | (ca[3] << 16);
+    const uint32_t b0 = cb[0] | (cb[1] << 16), b1 = cb[2] | (cb[3] << 16);
+    const int4 val = rot ? make_int4((int)b0, (int)b1, (int)a0, (int)a1) : make_int4((int)a0, (int)a1, (int)b0, (int)b1);
+    for (int d = 0; d < k.n; ++d) {
+      st_v4(k.out + k.dst[d] * k.row_out + pv * 16, val);
+      if ((pv & 7u) == 0) reinterpret_cast<float*>(k.dyn)[k.dst[d] * k.nd + (pv >> 3)] = scale;
+    }
+  }
+}
+
 // MX FP4 with each 32-element block in one thread: its four 16-byte vectors
 // are read from the staged row (in an order rotated by (lane / 2) % 4, so
 // that the eight lanes of a shared-memory phase hit distinct banks), the
@@ -631,15 +676,17 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     }
     const int nsm = tab.n_sm, nbk = tab.n_bulk;
     // Tokens with no bulk-plane pick store their codes straight from
-    // registers. Measured on GB300: FP4 rows with a vector a thread (4-byte
-    // codes) and per-group rows (a scale per 128 elements and destination)
-    // leave faster through the shared buffer as 16-byte stores and coalesced
-    // scale rows; MX rows of whole blocks leave fastest with a block (FP4) or
-    // half a block (FP8) a thread and 16-byte stores (direct4: FP4 47 -> 39
-    // us, MX FP8 54 -> 52 us at the bench shape), per-token int8 rows with two
-    // vectors a thread (53.2 -> 52.0 us; static int8 was 1% slower that way).
+    // registers. Measured on GB300: with a vector a thread (8-byte stores, 4
+    // for FP4), FP4 and per-group rows leave faster through the shared buffer
+    // as 16-byte stores; with 16-byte stores from registers they leave faster
+    // still: MX rows of whole blocks with a block (FP4) or half a block (FP8)
+    // a thread (direct4: FP4 47 -> 39 us, MX FP8 54 -> 52 us at the bench
+    // shape), per-group FP8 rows with two vectors a thread (direct3: 57.5 ->
+    // 53.3 us), per-token int8 rows likewise (53.2 -> 52.0 us; static int8
+    // was 1% slower that way).
     const bool direct = nbk == 0 && YT != MOE_Y_FP4_E2M1 && MODE != 3;
     const bool direct4 = MODE == 4 && !PE && nbk == 0 && sh.h % 32 == 0;
+    const bool direct3 = MODE == 3 && !PE && nbk == 0 && nvec % 2 == 0;
     float amax = 0.f;
     if constexpr (kMerge) {
 #pragma unroll
@@ -669,6 +716,11 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
         else
           quantize_mx8_half_blocks<DT, YT>(row, k, (uint32_t)nd * 2);
       }
+    } else if (direct3) {
+      if (nsm > 0) {
+        const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
+        quantize_group_fp8_pairs<DT, YT>(row, k, nvec);
+      }
     } else if (direct && nsm > 0) {
       const RowSink k{nullptr, nullptr, tab.sm_dst, nsm, out, dyn, row_out, nd};
       if constexpr (kMerge) {
@@ -692,7 +744,7 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     // variants through the shared buffers: one per bulk-plane pick (per-expert
     // scales), or one for all picks when some go by bulk copies
     const int j0 = PE ? nsm : 0;
-    const int j1 = PE ? nsm + nbk : (!direct && !direct4 && nsm + nbk > 0 ? 1 : 0);
+    const int j1 = PE ? nsm + nbk : (!direct && !direct4 && !direct3 && nsm + nbk > 0 ? 1 : 0);
     for (int j = j0; j < j1; ++j) {
       const int qs = nv & 1;
       ++nv;

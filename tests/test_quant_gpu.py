@@ -76,15 +76,16 @@ def test_quant_decode_shape(mode):
     run(wl)
 
 
-@pytest.mark.parametrize("mode", [(2, "", 0), (4, "fp8_e4m3", 0), (4, "fp8_e5m2", 0), (4, "fp4_e2m1", 0)],
-                         ids=mode_id)
+@pytest.mark.parametrize("mode", [(2, "", 0), (3, "fp8_e4m3", 0), (3, "fp8_e5m2", 0), (4, "fp8_e4m3", 0),
+                                  (4, "fp8_e5m2", 0), (4, "fp4_e2m1", 0)], ids=mode_id)
 @pytest.mark.parametrize("h", [32, 48, 96, 1000, 2080])
 def test_quant_direct_store_shapes(mode, h):
     """Every pick on the store plane, so every token's codes leave straight
     from registers: whole MX blocks a thread (FP4) or half blocks on lane pairs
     (FP8) when h is a multiple of 32, two vectors a thread for per-token int8
-    when h / 8 is even, the vector-a-thread forms otherwise; 2080 needs a
-    second, partial pass over the CTA's threads."""
+    and per-group FP8 when h / 8 is even (partial groups below 128 and at the
+    row's end), the vector-a-thread forms or the shared buffer otherwise; 2080
+    needs a second, partial pass over the CTA's threads."""
     q, y, k = mode
     wl = WL.Workload("qd", 4, 12, h, 4, 16, WL.X_FP16 if h == 1000 else WL.X_BF16, zero_expert_num=1,
                      mask_kind=2, special_p=0.1, mask_false_p=0.1, quant_mode=q, y_dtype=y, scales_kind=k,
