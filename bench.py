@@ -11,7 +11,7 @@ zero and 4 copy experts, 2D active mask, bf16 data.
 Prints one JSON line. ``value`` is the algorithmic bytes of dispatch + combine
 moved per second (GB/s, whole job over all ranks); ``tokens_per_s`` and the
 fraction of the 8 TB/s HBM roofline ride along. ``--impl reference`` times the
-CPU oracle on the same workload instead (the reference arm).
+CPU oracle on the same workload instead, on all host cores (the reference arm).
 
 Multi-GPU (torchrun): every rank runs its own independent batch (the W
 emulated ranks live inside each GPU), no collective on the data path; weak
@@ -227,12 +227,74 @@ def time_oracle(wl: WL.Workload, inp: dict, target_s: float, max_steps: int = 20
             return t
 
 
-def subsample(wl: WL.Workload, inp: dict, bs: int):
-    """The first `bs` tokens of every rank (same routing law, smaller batch)."""
-    sub = wl.with_(bs=bs, name=wl.name + f"_first{bs}")
-    out = {k: (None if v is None else np.ascontiguousarray(v[:, :bs])) for k, v in inp.items()
+def subsample(wl: WL.Workload, inp: dict, bs: int, start: int = 0):
+    """Tokens [start, start + bs) of every rank (same routing law, smaller batch)."""
+    sub = wl.with_(bs=bs, name=wl.name + (f"_first{bs}" if start == 0 else f"_tokens{start}_{start + bs}"))
+    out = {k: (None if v is None else np.ascontiguousarray(v[:, start:start + bs])) for k, v in inp.items()
            if k in ("x", "expert_ids", "active_mask", "expert_scales")}
     return sub, out
+
+
+def host_cores() -> int:
+    """Cores this process may run on."""
+    if hasattr(os, "sched_getaffinity"):
+        return len(os.sched_getaffinity(0))
+    return os.cpu_count() or 1
+
+
+def token_slices(bs: int, n: int):
+    """`n` contiguous token ranges (at most `bs` of them) that cover [0, bs) once."""
+    n = max(1, min(n, bs))
+    return [(i * bs // n, (i + 1) * bs // n) for i in range(n)]
+
+
+def time_oracle_all_cores(wl: WL.Workload, inp: dict, target_s: float, threads: int = 0) -> dict:
+    """The unchanged oracle on every host core at once. The batch's tokens are
+    split into one contiguous slice per thread (every rank's tokens [a, b)); each
+    slice is a smaller problem of the same routing law, and each thread runs
+    dispatch + combine on its own slice over and over until `target_s` has
+    passed. ctypes lets go of the GIL inside the C calls, so the threads run in
+    parallel. Throughput = algorithmic bytes of every completed slice / the
+    time until the last thread finished its last slice."""
+    from oracle import oracle as O
+    n = threads or host_cores()
+    parts = [subsample(wl, inp, b - a, start=a) for a, b in token_slices(wl.bs, n)]
+    part_bytes = [sum(v for k, v in algorithmic_bytes(swl, sinp).items() if k in ("dispatch", "combine"))
+                  for swl, sinp in parts]
+    done = [0] * len(parts)
+    ends = [0.0] * len(parts)
+    errors = []
+    go = threading.Barrier(len(parts) + 1)
+    t0 = [0.0]
+
+    def run(i):
+        swl, sinp = parts[i]
+        try:
+            go.wait()
+            while True:
+                d = O.dispatch(swl, sinp)
+                O.combine(swl, d["expand_x"], d["assist_info"], d["ep_recv_count"], sinp)
+                done[i] += 1
+                ends[i] = time.perf_counter()
+                if ends[i] - t0[0] >= target_s:
+                    return
+        except Exception as e:  # reported by the caller
+            errors.append(e)
+
+    workers = [threading.Thread(target=run, args=(i,), daemon=True) for i in range(len(parts))]
+    for w in workers:
+        w.start()
+    t0[0] = time.perf_counter()
+    go.wait()
+    for w in workers:
+        w.join()
+    if errors:
+        raise errors[0]
+    elapsed = max(ends) - t0[0]
+    moved = sum(c * b for c, b in zip(done, part_bytes))
+    return {"bytes": moved, "seconds": elapsed, "threads": len(parts), "slices_done": sum(done),
+            "tokens_per_slice": (min(b - a for a, b in token_slices(wl.bs, n)),
+                                 max(b - a for a, b in token_slices(wl.bs, n)))}
 
 
 # ------------------------------------------------------------ distributed
@@ -288,37 +350,61 @@ def bench_config(wl: WL.Workload, args, step_bytes: int) -> dict:
             "accumulate": "fp32"}
 
 
+def oracle_step_all_cores(pool, parts) -> float:
+    """One step of the unchanged oracle on the host's cores: every token slice
+    (see time_oracle_all_cores) goes through dispatch + combine once, one slice
+    a thread; returns the wall time until the last slice is done."""
+    from oracle import oracle as O
+
+    def run(p):
+        swl, sinp = p
+        d = O.dispatch(swl, sinp)
+        O.combine(swl, d["expand_x"], d["assist_info"], d["ep_recv_count"], sinp)
+
+    t0 = time.perf_counter()
+    for f in [pool.submit(run, p) for p in parts]:
+        f.result()
+    return time.perf_counter() - t0
+
+
 def run_reference(args):
     rank, world, _ = dist_env()
     if rank != 0:
         return 0
+    from concurrent.futures import ThreadPoolExecutor
     wl = WL.WORKLOADS[args.workload]
     inp = WL.make_inputs(wl)
     from oracle import build as OB
     OB.build()
+    n = host_cores()
     # size each step so that warmup + steps end within about three minutes
-    one = time_oracle(wl, inp, 0.0, max_steps=1)[0]
     budget = 180.0
-    n = max(1, args.steps + args.warmup)
+    steps = max(1, args.steps + args.warmup)
     bs = wl.bs
-    while bs > 1 and one * (bs / wl.bs) * n > budget:
-        bs //= 2
-    swl, sinp = (wl, inp) if bs == wl.bs else subsample(wl, inp, bs)
-    from oracle import oracle as O
-    times = []
-    for i in range(args.warmup + args.steps):
-        t0 = time.perf_counter()
-        d = O.dispatch(swl, sinp)
-        O.combine(swl, d["expand_x"], d["assist_info"], d["ep_recv_count"], sinp)
-        dt = time.perf_counter() - t0
-        if i >= args.warmup:
-            times.append(dt)
-    b = algorithmic_bytes(swl, sinp)
+    with ThreadPoolExecutor(max_workers=n) as pool:
+        def parts_of(b):
+            swl, sinp = (wl, inp) if b == wl.bs else subsample(wl, inp, b)
+            return swl, sinp, [subsample(swl, sinp, e - a, start=a) for a, e in token_slices(b, n)]
+        swl, sinp, parts = parts_of(bs)
+        one = oracle_step_all_cores(pool, parts)
+        while bs > 1 and one * (bs / wl.bs) * steps > budget:
+            bs //= 2
+        if bs != wl.bs:
+            swl, sinp, parts = parts_of(bs)
+        times = []
+        for i in range(args.warmup + args.steps):
+            dt = oracle_step_all_cores(pool, parts)
+            if i >= args.warmup:
+                times.append(dt)
+    b = sum(v for p in parts for k, v in algorithmic_bytes(*p).items() if k in ("dispatch", "combine"))
     total = sum(times)
-    gbps = (b["dispatch"] + b["combine"]) * len(times) / total / 1e9
+    gbps = b * len(times) / total / 1e9
+    lo = min(e - a for a, e in token_slices(bs, n))
+    hi = max(e - a for a, e in token_slices(bs, n))
     sample = (f"{len(times)} timed oracle steps of dispatch+combine over "
               + ("the full batch" if bs == wl.bs else f"the first {bs} of {wl.bs} tokens of every rank")
-              + ", single-threaded C")
+              + f", unchanged single-threaded C on {len(parts)} threads at once, each on its own slice of "
+              + f"{lo}" + (f"-{hi}" if hi != lo else "") + " tokens of every rank")
     full = algorithmic_bytes(wl, inp)
     line = {
         "impl": "reference", "metric": METRIC, "value": gbps, "unit": "GB/s", "n_gpus": args.gpus,
@@ -326,7 +412,7 @@ def run_reference(args):
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16", "data": "synthetic",
         "config": bench_config(wl, args, full["dispatch"] + full["combine"]),
         "tokens_per_s": swl.ep_world_size * swl.bs * len(times) / total,
-        "cpu_baseline": {"value": gbps, "unit": "GB/s", "cores": 1, "kind": "oracle", "sample": sample},
+        "cpu_baseline": {"value": gbps, "unit": "GB/s", "cores": len(parts), "kind": "oracle", "sample": sample},
         "e2e": {"value": gbps, "unit": "GB/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
     }
     print(json.dumps(line))
@@ -898,6 +984,15 @@ def run_ours(args):
         cpu = {"value": step_bytes / statistics.mean(times) / 1e9, "unit": "GB/s", "cores": 1, "kind": "oracle",
                "sample": f"{len(times)} full steps (dispatch+combine over all {wl.ep_world_size * wl.bs} tokens), "
                          f"single-threaded C, mean {statistics.mean(times) * 1e3:.0f} ms/step"}
+        par = time_oracle_all_cores(wl, inp, target_s=5.0)
+        lo, hi = par["tokens_per_slice"]
+        cpu["all_cores"] = {
+            "value": par["bytes"] / par["seconds"] / 1e9, "unit": "GB/s", "cores": par["threads"],
+            "kind": "oracle",
+            "sample": f"{par['slices_done']} dispatch+combine calls of the unchanged single-threaded C oracle "
+                      f"on {par['threads']} threads at once, each on its own slice of {lo}"
+                      + (f"-{hi}" if hi != lo else "") + f" of every rank's {wl.bs} tokens, "
+                      f"{par['seconds']:.1f} s"}
 
     if rank != 0:
         if world > 1:
