@@ -497,6 +497,13 @@ def pin_ffn_tokens_compose(seed: int = 9):
     wl = WL.Workload("ffn_tiny", 2, 3, 16, 2, 4, WL.X_BF16, copy_expert_num=1,
                      zero_expert_num=1, special_p=0.3, ffn_intermediate=8, seed=seed)
     inp = WL.make_inputs(wl)
+    # plant special picks so that every kind of term appears: a copy expert
+    # (id 5) beside a routed one, a zero expert (id 4), a token of two copies
+    ids = inp["expert_ids"].copy()
+    ids[0, 0, 1] = 5
+    ids[0, 1, 0] = 4
+    ids[1, 2, :] = 5
+    inp = dict(inp, expert_ids=ids)
     toks = np.arange(wl.ep_world_size * wl.bs)
     got = O.moe_ffn_tokens(wl, inp, toks)
     xs = inp["x"].reshape(-1, wl.h)
@@ -544,6 +551,11 @@ def pin_errors():
     assert status(m1, masked) == 0
     assert status(base.with_(ep_world_size=1, moe_expert_num=4), inp) == 1
     assert status(base.with_(moe_expert_num=5), inp) == 1
+    # topk in [1, 32]
+    k32 = base.with_(topk=32, moe_expert_num=64)
+    assert status(k32, WL.make_inputs(k32)) == 0
+    k33 = base.with_(topk=33, moe_expert_num=66)
+    assert status(k33, WL.make_inputs(k33)) == 1
     assert status(base.with_(quant_mode=2), inp) == 2
     # quantisation rules: modes 1..4 take 16-bit float x; output types and the
     # scales input as the quantMode constraints say
@@ -725,6 +737,108 @@ def pin_quant_modes_dispatch(seed: int = 29):
                     assert g == codes and d["dynamic_scales"][r, row].tolist() == sbytes, (i, r, row)
 
 
+def pin_combine_rejects_inconsistent_assist(seed: int = 31):
+    """Combine takes dispatch's assist_info / ep_recv_count unchanged ([DISP]
+    约束说明: dispatch outputs go into combine as they are). Layouts that cannot
+    have come from the routing are rejected with BAD_ASSIST (9): a routed pick
+    that no row names (the last row cut off by its count), a pick named by two
+    rows, a row naming a pick that is not routed (masked, zero or copy), a row
+    naming a pick outside the batch, and a count above the capacity A."""
+    wl = WL.Workload("assist", 2, 6, 8, 2, 4, WL.X_INT32, zero_expert_num=1, copy_expert_num=1,
+                     mask_kind=2, special_p=0.25, mask_false_p=0.2, seed=seed)
+    inp = WL.make_inputs(wl)
+    d = O.dispatch(wl, inp)
+    ex, ai, erc = d["expand_x"], d["assist_info"], d["ep_recv_count"]
+    A = ai.shape[1]
+    assert O.combine(wl, ex, ai, erc, inp, raise_on_error=False)[1] == 0
+    routed = {tuple(ai[r, i].tolist()) for r in range(2) for i in range(erc[r, -1])}
+    others = [(s, t, k) for s in range(2) for t in range(wl.bs) for k in range(wl.topk)
+              if (s, t, k) not in routed]
+    assert others, "the fixture needs a pick that is not routed"
+    r = int(np.argmax(erc[:, -1]))          # a rank that holds rows
+    n = int(erc[r, -1])
+    assert 0 < n < A
+
+    def status(ai2, erc2):
+        return O.combine(wl, ex, ai2, erc2, inp, raise_on_error=False)[1]
+
+    cut = erc.copy()
+    cut[r, -1] -= 1
+    assert status(ai, cut) == 9                      # a routed pick with no row
+    grow = erc.copy()
+    grow[r, -1] += 1
+    dup = ai.copy()
+    dup[r, n] = ai[r, 0]
+    assert status(dup, grow) == 9                    # one pick, two rows
+    extra = ai.copy()
+    extra[r, n] = others[0]
+    assert status(extra, grow) == 9                  # a row for a pick that is not routed
+    outside = ai.copy()
+    outside[r, n] = (0, wl.bs, 0)
+    assert status(outside, grow) == 9                # a token outside the batch
+    over = erc.copy()
+    over[0, -1] = A + 1
+    assert status(ai, over) == 9                     # more rows than the capacity
+
+
+def pin_combine_int32_wraps():
+    """int32 data: the weighted sum is exact integer arithmetic taken modulo
+    2^32 (two's complement), like int32 arithmetic on any machine; nothing
+    saturates. Token (0, 0) has weights 1 and 3 on one row each (identity
+    expert), so its output is 4 x: 2^30 * 4 = 2^32 -> 0, (2^31 - 1) * 4 =
+    2^33 - 4 -> -4, -2^31 * 4 = -2^33 -> 0, 5 * 4 = 20. Token (1, 1) has
+    weights 1 and 1: -2^31 * 2 = -2^32 -> 0."""
+    wl = WL.Workload("wrap", 2, 2, 4, 2, 4, WL.X_INT32, seed=0)
+    ids = np.array([[[0, 2], [1, 3]], [[2, 0], [3, 1]]], dtype=np.int32)
+    x = np.zeros((2, 2, 4), dtype=np.int32)
+    x[0, 0] = [2 ** 30, 2 ** 31 - 1, -2 ** 31, 5]
+    x[0, 1] = [7, -7, 1, 0]
+    x[1, 0] = [2 ** 30, 1, -1, 2 ** 31 - 1]
+    x[1, 1] = [-2 ** 31, 3, 0, 1]
+    w = np.array([[[1, 3], [2, 2]], [[4, 0], [1, 1]]], dtype=np.int32)
+    inp = {"x": x, "expert_ids": ids, "expert_scales": w, "active_mask": None}
+    d = O.dispatch(wl, inp)
+    got = O.combine(wl, O.identity_expert(d), d["assist_info"], d["ep_recv_count"], inp)
+    tot = w.astype(object).sum(-1)
+    for s in range(2):
+        for t in range(2):
+            for j in range(4):
+                v = int(x[s, t, j]) * int(tot[s, t])
+                want = (v + 2 ** 31) % 2 ** 32 - 2 ** 31
+                assert int(got[s, t, j]) == want, (s, t, j, int(got[s, t, j]), want)
+    assert got[0, 0].tolist() == [0, -4, 0, 20] and int(got[1, 1, 0]) == 0
+
+
+def pin_mx_scale_floor():
+    """OCP MX: the shared scale X = 2^(floor(log2 amax) - emax) is stored as an
+    E8M0 byte, whose smallest value is 2^-127 (byte 0). Blocks of tiny bf16
+    values whose exponent would fall below that are clamped to 2^-127:
+      E4M3 (emax 8):  amax = 2^-120 -> 2^-128 -> clamped 2^-127, byte 0;
+                      2^-120 / 2^-127 = 128 = 1.0 * 2^7 -> code (7+7) << 3 = 0x70;
+                      1.5 * 2^-121 / 2^-127 = 96 = 1.5 * 2^6 -> (13 << 3) | 4 = 0x6C.
+      E5M2 (emax 15): amax = 2^-115 -> 2^-130 -> 2^-127, byte 0;
+                      2^-115 / 2^-127 = 4096 = 2^12 -> (12+15) << 2 = 0x6C.
+      E2M1 (emax 2):  amax = 2^-120 -> 2^-122, byte 5 (no clamp);
+                      2^-120 / 2^-122 = 4 -> code 0b110 = 6."""
+    def row(vals):
+        x = np.zeros(32, dtype=np.float32)
+        x[:len(vals)] = vals
+        return WL.fp32_to_bf16_bits(x)
+
+    q, dyn = O.quantize_pick(row([2.0 ** -120, -1.5 * 2.0 ** -121]), 4, "bfloat16", "fp8_e4m3")
+    assert dyn.tolist() == [0] and q[:2].tolist() == [0x70, 0x80 | 0x6C] and not q[2:].any()
+    q, dyn = O.quantize_pick(row([2.0 ** -115]), 4, "bfloat16", "fp8_e5m2")
+    assert dyn.tolist() == [0] and q[0] == 0x6C and not q[1:].any()
+    q, dyn = O.quantize_pick(row([2.0 ** -120]), 4, "bfloat16", "fp4_e2m1")
+    assert dyn.tolist() == [5] and q[0] == 0x06 and not q[1:].any()
+    # the exact rational model agrees on the clamped blocks
+    for fmt, v in (("fp8_e4m3", [2.0 ** -120, -1.5 * 2.0 ** -121]), ("fp8_e5m2", [2.0 ** -115])):
+        xs = WL.bf16_bits_to_fp32(row(v)).tolist()
+        codes, sb = mx_quant_exact(xs, fmt)
+        q, dyn = O.quantize_pick(row(v), 4, "bfloat16", fmt)
+        assert q.tolist() == codes and dyn.tolist() == sb
+
+
 def run_all():
     """Every pin, on the fixtures plus small and random workloads."""
     pin_dispatch_combine_hand()
@@ -773,3 +887,6 @@ def run_all():
     pin_conversions(n=4000)
     pin_swiglu_torch()
     pin_ffn_tokens_compose()
+    pin_combine_rejects_inconsistent_assist()
+    pin_combine_int32_wraps()
+    pin_mx_scale_floor()

@@ -1,6 +1,14 @@
 """Plant plausible mistakes in copies of the oracle (on the CPU) and check that
 the pins catch every one: a dropped term, a wrong index, a swapped loop, the
-wrong rounding, an off-by-one comparison."""
+wrong rounding, an off-by-one comparison, a missing consistency check.
+
+Two guards have no mutant here because no input can tell them apart: the
+dispatch capacity check (with a token's routed ids distinct, a rank receives at
+most bs * W * min(L, K) = A rows, so the check never fires) and combine's bound
+of a rank's row count by A (without it, a count above A on a rank reads the
+next rank's first rows, whose picks the duplicate check then reports with the
+same status; on the last rank it would read past the array, which no test
+may make it do)."""
 import os
 import subprocess
 import tempfile
@@ -70,6 +78,36 @@ MUTANTS = {
     "minifloat_no_subnormals": [("if (a < ldexp(1.0, emin)) e = emin;", "if (0) e = emin;")],
     "fp4_nibbles_swapped": [("q[j / 2] |= (uint8_t)(code << (4 * (j % 2)));",
                              "q[j / 2] |= (uint8_t)(code << (4 * (1 - j % 2)));")],
+    "mask_2d_transposed": [("return mask[((size_t)s * c->bs + t) * c->K + k] != 0;",
+                            "return mask[((size_t)s * c->K + k) * c->bs + t] != 0;")],
+    "mask_order_across_ranks": [("for (int s = 0; s < c->W; ++s) {\n    int seen_false = 0;",
+                                 "int seen_false = 0;\n  for (int s = 0; s < c->W; ++s) {")],
+    "copy_range_inclusive": [("if ((int64_t)e < (int64_t)c->E + c->Z + c->C) return PICK_COPY;",
+                              "if ((int64_t)e <= (int64_t)c->E + c->Z + c->C) return PICK_COPY;")],
+    "topk_33_accepted": [("c->K <= 0 || c->K > 32)", "c->K <= 0 || c->K > 33)")],
+    "expand_scales_first_pick": [("(const char*)scales + (src * K + k) * 4, 4);",
+                                  "(const char*)scales + (src * K) * 4, 4);")],
+    "segment_rows_first_rank_only": [("return (g % LW == 0) ? ep_recv_count[g]", "return (g == 0) ? ep_recv_count[g]")],
+    "dispatch_plane_counts_local": [("if (d != s)\n        for (int le = 0; le < L; ++le) remote +=",
+                                     "for (int le = 0; le < L; ++le) remote +=")],
+    "combine_duplicate_row_accepted": [("if (where[p] >= 0) { st = ORC_ERR_BAD_ASSIST; break; }",
+                                        "if (0) { st = ORC_ERR_BAD_ASSIST; break; }")],
+    "combine_missing_row_accepted": [(
+        "if (cls[k] == PICK_ROUTED && where[tok * K + k] < 0) { st = ORC_ERR_BAD_ASSIST; break; }", "")],
+    "combine_unrouted_row_accepted": [(
+        "if (cls[k] != PICK_ROUTED && where[tok * K + k] >= 0) { st = ORC_ERR_BAD_ASSIST; break; }", "")],
+    "int32_combine_saturates": [(
+        "((int32_t*)x_out)[tok * h + j] = (int32_t)(uint32_t)(uint64_t)acc;",
+        "((int32_t*)x_out)[tok * h + j] = acc > 2147483647 ? 2147483647 : "
+        "(acc < -2147483647 ? -2147483647 : (int32_t)acc);")],
+    "group_amax_signed": [("for (int j = g0; j < g1; ++j) if (fabsf(xs[j]) > amax) amax = fabsf(xs[j]);",
+                           "for (int j = g0; j < g1; ++j) if (xs[j] > amax) amax = xs[j];")],
+    "e4m3_saturates_to_nan": [("f.maxv = 448.0; f.max_code = 0x7E;", "f.maxv = 448.0; f.max_code = 0x7F;")],
+    "mx_scale_bias_128": [("((uint8_t*)dyn)[b0 / 32] = (uint8_t)(se + 127);",
+                           "((uint8_t*)dyn)[b0 / 32] = (uint8_t)(se + 128);")],
+    "mx_scale_floor_126": [("if (se < -127) se = -127;", "if (se < -126) se = -126;")],
+    "ffn_copy_weight_dropped": [("for (int j = 0; j < h; ++j) o[j] += w * bf16_to_f32(x[(size_t)tok * h + j]);",
+                                 "for (int j = 0; j < h; ++j) o[j] += bf16_to_f32(x[(size_t)tok * h + j]);")],
     "silu_sign": [("a[i] = g / (1.0 + exp(-g)) * u;", "a[i] = g / (1.0 + exp(g)) * u;")],
     "gate_up_swapped": [("g += xv[j] * bf16_to_f32(wg[", "g += xv[j] * bf16_to_f32(wu[")],
     "down_transposed": [("acc += a[i] * bf16_to_f32(wd[(size_t)j * I + i]);",
