@@ -87,13 +87,21 @@ def pick_counts(wl: WL.Workload, inp: dict) -> dict:
     return {"P": int(routed.sum()), "copy": int(copy.sum()), "tok_routed": int(routed.any(-1).sum())}
 
 
+def row_out_bytes(wl: WL.Workload) -> int:
+    """Bytes of one expand_x row: x's row unquantised, h for int8 / fp8, h / 2
+    for packed fp4."""
+    if wl.quant_mode == 0:
+        return wl.h * wl.es
+    return wl.h // 2 if wl.y_dtype == "fp4_e2m1" else wl.h
+
+
 def algorithmic_bytes(wl: WL.Workload, inp: dict) -> dict:
     """Bytes the method must move (inputs read once, outputs written once)."""
     c = pick_counts(wl, inp)
     W, bs, K, h = wl.ep_world_size, wl.bs, wl.topk, wl.h
     L = wl.moe_expert_num // W
     r_in = h * wl.es
-    r_out = wl.row_out_bytes
+    r_out = row_out_bytes(wl)
     picks = W * bs * K
     mask = 0 if inp.get("active_mask") is None else inp["active_mask"].size
     ep = W * L * W * 4
@@ -661,7 +669,7 @@ def measure_quant(args, M, torch, stream, base: WL.Workload):
         res[tag] = {"dispatch_ms": call_ms, "dispatch_GBps": acct["dispatch"] / (call_ms * 1e-3) / 1e9,
                     "scatter_ms": sc_ms, "scatter_GBps": acct["scatter"] / (sc_ms * 1e-3) / 1e9,
                     "scatter_frac_of_measured_hbm": acct["scatter"] / (sc_ms * 1e-3) / 1e9 / peaks["hbm_gbs"],
-                    "scatter_bytes": acct["scatter"], "row_out_bytes": wl.row_out_bytes, "steps": n}
+                    "scatter_bytes": acct["scatter"], "row_out_bytes": row_out_bytes(wl), "steps": n}
         del ws, outs
     return {"workload": base.name, "variants": res,
             "note": "q2_int8_s0 is the per-token int8 kernel of the plain dispatch; the others run the quantising "

@@ -43,12 +43,13 @@ def test_two_phase_rejects_counts_beyond_capacity():
     import workloads as WL
     import gpu_harness as H
     from combine_route_scan_gb300 import moe as M
+    from oracle import oracle as O
     wl = WL.WORKLOADS["w8_bs8_h16_k2_e64_f16"]
     inp = WL.make_inputs(wl)
     dev = H.device_inputs(wl, inp)
     got, _, _ = H.gpu_dispatch(wl, dev)
     ep = got["ep_recv_count"].clone()
-    ep[-1, -1] = int(wl.capacity) + 5
+    ep[-1, -1] = O.capacity(wl) + 5
     for mode in (M.COMBINE_GATHER, M.COMBINE_TWO_PHASE, M.COMBINE_PUT_ONLY):
         _, st, _ = H.gpu_combine(wl, dev, got["expand_x"], got["assist_info"], ep, combine_mode=mode,
                                  check_status=False)

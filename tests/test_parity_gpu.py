@@ -48,7 +48,10 @@ def run_and_compare(wl, inp=None, plane_policy=0, bulk_min_bytes=O.DEFAULT_BULK_
 
 
 def _tma_rows(wl):
-    return wl.h * wl.es % 16 == 0 and wl.row_out_bytes % 16 == 0
+    """Rows in and out are 16-byte multiples (x's row; int8 / fp8 codes take h
+    bytes, packed fp4 h / 2)."""
+    out = wl.h * wl.es if wl.quant_mode == 0 else (wl.h // 2 if wl.y_dtype == "fp4_e2m1" else wl.h)
+    return wl.h * wl.es % 16 == 0 and out % 16 == 0
 
 
 @pytest.mark.parametrize("name", SMALL)

@@ -69,19 +69,6 @@ class Workload:
     def es(self) -> int:
         return ES[self.x_dtype]
 
-    @property
-    def row_out_bytes(self) -> int:
-        """Bytes of one expand_x row: x's row unquantised, h for int8 / fp8,
-        h / 2 for packed fp4."""
-        if self.quant_mode == 0:
-            return self.h * self.es
-        return self.h // 2 if self.y_dtype == "fp4_e2m1" else self.h
-
-    @property
-    def capacity(self) -> int:
-        """Rows each rank's expand_x can hold: bs * W * min(L, K)."""
-        return self.bs * self.ep_world_size * min(self.local_expert_num, self.topk)
-
     def with_(self, **kw) -> "Workload":
         return dataclasses.replace(self, **kw)
 
