@@ -128,3 +128,15 @@ def test_quant_modes_through_dispatch():
 
 def test_mx_and_group_hand_fixture():
     P.pin_quant_mx_group_hand()
+
+
+def test_combine_rejects_layouts_dispatch_cannot_make():
+    P.pin_combine_rejects_inconsistent_assist()
+
+
+def test_int32_combine_wraps_modulo_2_32():
+    P.pin_combine_int32_wraps()
+
+
+def test_mx_scale_clamped_at_e8m0_floor():
+    P.pin_mx_scale_floor()
