@@ -233,7 +233,13 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
  * every pick's row against assist_info and ep_recv_count: contents changed in
  * place, a pick that no row names, or a receive count above the capacity are
  * reported as MOE_ERR_BAD_ASSIST. moe_workspace_init forgets a workspace's
- * history. */
+ * history. A caller that rewrites assist_info / ep_recv_count in place between
+ * the dispatch and this call, even with another layout that dispatch could
+ * make (rows permuted within a segment together with expert_out), must call
+ * moe_workspace_init first or pass the layout in other buffers: otherwise the
+ * dispatch's map is kept and the picks it no longer fits are reported as
+ * MOE_ERR_BAD_ASSIST. A layout that dispatch cannot make (a pick named by two
+ * rows, a row naming an unrouted pick) gives unspecified x_out. */
 moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const int32_t* assist_info,
                          const int32_t* ep_recv_count, const int32_t* expert_ids,
                          const void* expert_scales, const uint8_t* active_mask, const void* x,
