@@ -280,3 +280,85 @@ def test_quant_top32(mode):
                      y_dtype=y, scales_kind=k, seed=51)
     for policy in (M.PLANE_RULE, M.PLANE_BULK_ALL):
         run(wl, plane_policy=policy, bulk_min_bytes=0)
+
+
+# Every quantising-scatter instantiation the tests and the bench run, plus the
+# per-token int8 form without scales.
+ALL_MODES = MODES + [(2, "", 0)]
+
+
+def _resident_limit():
+    """An upper bound on the quantising scatter's resident grid: 8 CTAs of 256
+    threads per SM (2048 threads, the SM's limit)."""
+    return torch.cuda.get_device_properties(0).multi_processor_count * 8
+
+
+def _many_tokens_workload(mode, dt, seed):
+    q, y, k = mode
+    return WL.Workload("qmany", 8, 1024, 256, 4, 32, dt, zero_expert_num=2, copy_expert_num=2, mask_kind=2,
+                       special_p=0.1, mask_false_p=0.1, ids="zipf", quant_mode=q, y_dtype=y, scales_kind=k,
+                       seed=seed)
+
+
+@pytest.mark.parametrize("mode", ALL_MODES, ids=mode_id)
+@pytest.mark.parametrize("policy", ["rule", "bulk"])
+def test_quant_many_tokens_per_cta(mode, policy):
+    """8192 tokens against at most 8 CTAs per SM: every CTA of the quantising
+    scatter takes several tokens in turn, so the source-row ring reuses its
+    slots with the barrier parity flipped, warp 0 loads destination lists one
+    and two tokens ahead, the rows of token i-1 are counted while token i is
+    quantised, and the two shared quantised-row buffers alternate. Zipf
+    routing with masks and zero / copy experts; the page's rule with a zero
+    size threshold (every above-mean remote segment by bulk copies) or every
+    remote segment by bulk copies. Codes, dynamic scales, assist_info,
+    expand_scales and counts byte for byte."""
+    dt = WL.X_BF16 if policy == "rule" else WL.X_FP16
+    wl = _many_tokens_workload(mode, dt, 41 + ALL_MODES.index(mode))
+    assert wl.ep_world_size * wl.bs >= 4 * _resident_limit()
+    if policy == "rule":
+        run(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
+    else:
+        run(wl, plane_policy=M.PLANE_BULK_ALL)
+
+
+@pytest.mark.parametrize("mode", [(2, "", 0), (4, "fp4_e2m1", 0), (3, "fp8_e4m3", 3)], ids=mode_id)
+def test_quant_many_tokens_ready_flags_and_performance_info(mode):
+    """The multi-token path with ready flags and performance info on: every
+    segment flagged with the call's ticket, per-rank times positive, outputs
+    still byte-exact."""
+    wl = _many_tokens_workload(mode, WL.X_BF16, 60)
+    inp = WL.make_inputs(wl)
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    L = wl.moe_expert_num // wl.ep_world_size
+    cfg = H.make_cfg(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+    for t in out.values():
+        if t is not None:
+            t.view(torch.uint8).fill_(0xA5)
+    flags = torch.zeros((wl.ep_world_size, L * wl.ep_world_size), dtype=torch.int32, device="cuda")
+    perf = torch.zeros(wl.ep_world_size, dtype=torch.int64, device="cuda")
+    c = M.with_performance_info(M.with_seg_ready(cfg, flags, 11), perf)
+    M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
+               out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws,
+               scales=dev["quant_scales"])
+    assert M.get_device_status(ws) == 0
+    assert bool((flags == 11).all()), int((flags != 11).sum())
+    assert bool((perf > 0).all()), perf
+    H.compare_dispatch(wl, out, ref)
+
+
+@pytest.mark.parametrize("mode", [(2, "", 0), (3, "fp8_e4m3", 0), (2, "", 3), (3, "fp8_e4m3", 3), (4, "fp4_e2m1", 0)],
+                         ids=mode_id)
+def test_quant_full_size_bench_workload(mode):
+    """The bench workload (16 ranks, 256 tokens each, h 7168, top-8 of 256
+    Zipf-routed experts, 2D mask, zero and copy experts): 4096 tokens, about
+    5 per resident CTA, every routed row's codes and dynamic scales byte for
+    byte against the oracle, and the planes the page's rule gives to the
+    quantised row sizes (int8 and FP8 rows of 7168 bytes, packed FP4 of 3584:
+    no segment reaches 2 MiB) are the oracle's."""
+    q, y, k = mode
+    wl = WL.WORKLOADS["w16_bs256_h7168_k8_e256_bf16_zipf"].with_(quant_mode=q, y_dtype=y, scales_kind=k)
+    got, ref = run(wl)
+    assert np.array_equal(H.to_host(got["seg_plane"]), O.dispatch_plane(wl, ref["ep_recv_count"]))
