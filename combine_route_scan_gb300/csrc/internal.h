@@ -22,7 +22,8 @@ struct WsHeader {
   unsigned long long inv_assist;      // ... whose assist_info and ep_recv_count were these buffers
   unsigned long long inv_ep;
   uint32_t scatter_next;  // TMA scatter: next token ticket (zeroed by the routing kernel)
-  uint32_t pad[51];
+  uint32_t pe_rows;       // per-group FP8 with per-expert scales: receive rows of all ranks (the row list length)
+  uint32_t pad[50];
 };
 static_assert(sizeof(WsHeader) == 256, "header is 256 bytes");
 
@@ -38,6 +39,7 @@ struct WsLayout {
   size_t plane_c;  // uint8 [E*W]     two-phase combine plane per segment
   size_t flags;    // uint32 [W*bs*K] two-phase combine ready flags
   size_t window;   // [W*bs*K][h]     two-phase combine window
+  size_t pe_list;  // int4 [W*A]      per-group FP8 with per-expert scales: {row, token, expert, plane} of every receive row
   // moe_dispatch_ffn_combine only
   size_t ffn_expand_x;   // bf16 [W*A][h]
   size_t ffn_assist;     // int32 [W*A][3]
@@ -164,6 +166,11 @@ bool scatter_tma_fits(const Shape& sh);
 bool scatter_quant_tma_fits(const Shape& sh);
 cudaError_t launch_scatter_quant(const ScatterParams& p, cudaStream_t st, int num_sms, bool tma);
 inline bool uses_scatter_quant(const Shape& sh) { return sh.quant != 0; }
+// The expert-major payload of per-group FP8 with per-expert scales (row map kernel +
+// payload kernel); `launches` receives the number of kernels enqueued.
+bool uses_scatter_pe(const Shape& sh);
+cudaError_t launch_scatter_pe(const ScatterParams& p, const int32_t* ep_recv_count, int4* list, cudaStream_t st,
+                              int num_sms, int* launches);
 
 // Launchers (each returns the launch error, if any).
 cudaError_t launch_route(const RouteParams& p, cudaStream_t st);

@@ -160,6 +160,7 @@ WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
   L.perf_end = take((size_t)sh.W * 8);
   L.rank = take(picks * 4);
   L.inv = take(picks * 4);
+  if (c->quant_mode == 3 && c->scales_kind == MOE_SCALES_EXPERT) L.pe_list = take((size_t)sh.W * sh.A * 16);
   if (c->combine_mode != MOE_COMBINE_GATHER) {
     L.plane_c = take(segs);
     L.flags = take(picks * 4);
@@ -391,9 +392,17 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.status = &hdr->status;
   sp.timeout_ns = timeout_ns(cfg);
   if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
-  const cudaError_t e = quant_kernel ? launch_scatter_quant(sp, s, nsm, tma) : launch_scatter(sp, s, nsm, tma);
-  if (e != cudaSuccess) return MOE_ERR_CUDA;
-  if (!empty) note_launches(1);
+  if (quant_kernel && tma && uses_scatter_pe(sh)) {
+    int launched = 0;
+    const cudaError_t e =
+        launch_scatter_pe(sp, ep_recv_count, reinterpret_cast<int4*>(w + L.pe_list), s, nsm, &launched);
+    note_launches(launched);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+  } else {
+    const cudaError_t e = quant_kernel ? launch_scatter_quant(sp, s, nsm, tma) : launch_scatter(sp, s, nsm, tma);
+    if (e != cudaSuccess) return MOE_ERR_CUDA;
+    if (!empty) note_launches(1);
+  }
   set_map_owner(ws, assist_info, ep_recv_count, s);  // the scatter writes the map for these buffers
   if (record(cfg->prof_events, 1, s) != MOE_OK) return MOE_ERR_CUDA;
   return MOE_OK;
