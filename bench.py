@@ -69,6 +69,8 @@ def parse_args():
     ap.add_argument("--quant-steps", type=int, default=50)
     ap.add_argument("--only-quant", action="store_true",
                     help="time only the quantised dispatch variants (for profiling); prints their JSON")
+    ap.add_argument("--only-small", action="store_true",
+                    help="time only the small (L2-sized) workloads and their floors; prints their JSON")
     return ap.parse_args()
 
 
@@ -480,6 +482,43 @@ def measure_ffn(args, M, torch, stream):
             "steps": Kf}
 
 
+def measure_floor(torch, stream, flush, n, ops: dict) -> dict:
+    """What one GPU gives a call of this size at all, timed exactly as the
+    calls are (512 MB written before every step, CUDA events around the call):
+    the launch floor (events around one kernel that touches 16 bytes) and, per
+    operation, a plain device-to-device copy moving the operation's
+    algorithmic bytes (half read, half written)."""
+    tiny = torch.zeros(4, dtype=torch.int32, device="cuda")
+    big = max(ops.values())
+    src = torch.empty(big // 2 + 16, dtype=torch.uint8, device="cuda")
+    dst = torch.empty_like(src)
+
+    def timed(fn):
+        ts = []
+        for i in range(n + 3):
+            flush.fill_((i + 7) & 0xFF)
+            a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+            a.record(stream)
+            fn()
+            b.record(stream)
+            if i >= 3:
+                ts.append((a, b))
+        torch.cuda.synchronize()
+        return statistics.median(a.elapsed_time(b) for a, b in ts)
+
+    res = {"launch_ms": timed(lambda: tiny.add_(1)),
+           "how": "median over steps of CUDA-event times after a 512 MB write, as for the calls; the copy is "
+                  "torch's device-to-device copy_ of half the operation's algorithmic bytes"}
+    for op, nbytes in ops.items():
+        half = nbytes // 2
+        ms = timed(lambda: dst[:half].copy_(src[:half]))
+        res[f"{op}_copy_ms"] = ms
+        res[f"{op}_copy_GBps"] = 2 * half / (ms * 1e-3) / 1e9
+        res[f"{op}_copy_frac_of_8TBps"] = 2 * half / (ms * 1e-3) / 1e9 / HBM_NOMINAL_GBPS
+    del src, dst, tiny
+    return res
+
+
 def measure_small(args, M, torch, stream):
     """Workloads whose working set fits in L2: each step first writes a 512 MB
     buffer (untimed) so dispatch and combine read and write HBM, then times
@@ -538,6 +577,8 @@ def measure_small(args, M, torch, stream):
                       "combine_bytes": acct["combine"]})
         r["steps"] = n
         r["l2"] = "512 MB written before every step (untimed); median of per-call CUDA-event times"
+        r["floor"] = measure_floor(torch, stream, flush, n, {"dispatch": acct["dispatch"]} if wl.quant_mode else
+                                   {"dispatch": acct["dispatch"], "combine": acct["combine"]})
         del ws, out
         # sustained: back-to-back steps rotating over independent buffer sets,
         # enough of them that a set's data has left the L2 before it is reused
@@ -694,6 +735,9 @@ def run_ours(args):
     wl = WL.WORKLOADS[args.workload]
     if args.only_quant:
         print(json.dumps(measure_quant(args, M, torch, torch.cuda.current_stream(), wl)))
+        return 0
+    if args.only_small:
+        print(json.dumps(measure_small(args, M, torch, torch.cuda.current_stream())))
         return 0
     inp = WL.make_inputs(wl, seed=rank_seed(wl, rank))
     acct = algorithmic_bytes(wl, inp)
