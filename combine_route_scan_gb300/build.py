@@ -4,6 +4,12 @@ Each .cu file compiles to its own object in parallel with nvcc, then nvcc links
 them into combine_route_scan_gb300/_build/libcrs_moe.so. The CUDA runtime is
 linked statically. No cmake.
 
+``build(observer=True)`` builds the flag-observer test variant
+(_build/observer/libcrs_moe.so, ``-DMOE_FLAG_OBSERVER``): the dispatch payload
+grid's last CTA watches the ready flags and copies each segment the moment its
+flag is set, so that a test can check that no flag is visible before its rows.
+The binding loads it when the environment variable CRS_MOE_OBSERVER is 1.
+
 ``build(checked=True)`` builds the bounds-checked variant
 (_build/checked/libcrs_moe.so, ``-DMOE_BOUNDS_CHECK``): every index a kernel
 derives from data is checked against its buffer, and a miss records
@@ -24,6 +30,8 @@ OUT_DIR = os.path.join(HERE, "_build")
 LIB = os.path.join(OUT_DIR, "libcrs_moe.so")
 CHECKED_DIR = os.path.join(OUT_DIR, "checked")
 CHECKED_LIB = os.path.join(CHECKED_DIR, "libcrs_moe.so")
+OBSERVER_DIR = os.path.join(OUT_DIR, "observer")
+OBSERVER_LIB = os.path.join(OBSERVER_DIR, "libcrs_moe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]
@@ -47,13 +55,15 @@ def _inputs_mtime() -> float:
     return max(os.path.getmtime(f) for f in files)
 
 
-def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False) -> str:
-    out_dir, lib = (CHECKED_DIR, CHECKED_LIB) if checked else (OUT_DIR, LIB)
+def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False,
+          observer: bool = False) -> str:
+    out_dir, lib = (CHECKED_DIR, CHECKED_LIB) if checked else (OBSERVER_DIR, OBSERVER_LIB) if observer else (OUT_DIR, LIB)
     os.makedirs(out_dir, exist_ok=True)
     if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _inputs_mtime():
         return lib
     cc = nvcc()
-    flags = NVCC_FLAGS + list(extra_flags or []) + (["-DMOE_BOUNDS_CHECK"] if checked else [])
+    flags = (NVCC_FLAGS + list(extra_flags or []) + (["-DMOE_BOUNDS_CHECK"] if checked else []) +
+             (["-DMOE_FLAG_OBSERVER"] if observer else []))
     if verbose:
         flags = flags + ["-Xptxas", "-v"]
 

@@ -86,6 +86,20 @@ struct RouteParams {
   int n_zero_words;
 };
 
+#ifdef MOE_FLAG_OBSERVER
+// Test builds only (-DMOE_FLAG_OBSERVER): where the flag observer of the
+// dispatch payload kernels copies each segment the moment its ready flag shows
+// the call's ticket (see observe_flags in scatter_common.cuh).
+struct FlagObserver {
+  uint8_t* rows;                        // [W][A][row bytes], like expand_x
+  int32_t* assist;                      // [W][A][3], like assist_info
+  uint8_t* dyn;                         // like dynamic_scales (quantised modes), or null
+  unsigned long long* seen_ns;          // [E*W] %globaltimer once the segment's copy was taken
+  unsigned long long* producer_end_ns;  // latest end of a storing CTA
+  uint32_t* n_seen;                     // segments seen
+};
+#endif
+
 struct ScatterParams {
   const void* x;
   const int32_t* ids;
@@ -110,6 +124,10 @@ struct ScatterParams {
   Shape sh;
   int* status;
   uint64_t timeout_ns;
+#ifdef MOE_FLAG_OBSERVER
+  FlagObserver obs;
+  int observe;  // the grid's last CTA observes instead of storing
+#endif
 };
 
 struct CombineParams {

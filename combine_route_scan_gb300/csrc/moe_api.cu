@@ -312,6 +312,32 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
   return MOE_OK;
 }
 
+#ifdef MOE_FLAG_OBSERVER
+namespace {
+std::mutex g_observer_mu;
+bool g_observer_on = false;
+FlagObserver g_observer{};
+}  // namespace
+
+// Test builds only (not declared in include/moe.h): the next dispatches with
+// ready flags run the flag observer of their payload grid, which copies each
+// segment the moment its flag shows the call's ticket into these device
+// buffers (rows like expand_x, assist like assist_info, dyn like
+// dynamic_scales or NULL; seen_ns [E*W] and producer_end_ns, n_seen single
+// words). rows == NULL turns the observer off.
+moe_status_t moe_test_set_flag_observer(void* rows, void* assist, void* dyn, void* seen_ns, void* producer_end_ns,
+                                        void* n_seen) {
+  std::lock_guard<std::mutex> lock(g_observer_mu);
+  g_observer_on = rows != nullptr;
+  if (g_observer_on && (!assist || !seen_ns || !producer_end_ns || !n_seen || !aligned(rows, 16)))
+    return MOE_ERR_INVALID_ARG;
+  g_observer = FlagObserver{static_cast<uint8_t*>(rows), static_cast<int32_t*>(assist), static_cast<uint8_t*>(dyn),
+                            static_cast<unsigned long long*>(seen_ns),
+                            static_cast<unsigned long long*>(producer_end_ns), static_cast<uint32_t*>(n_seen)};
+  return MOE_OK;
+}
+#endif
+
 moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t* expert_ids,
                           const uint8_t* active_mask, const void* expert_scales, const float* scales,
                           void* expand_x, void* dynamic_scales, int32_t* assist_info, int32_t* ep_recv_count,
@@ -391,6 +417,16 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.sh = sh;
   sp.status = &hdr->status;
   sp.timeout_ns = timeout_ns(cfg);
+#ifdef MOE_FLAG_OBSERVER
+  {
+    std::lock_guard<std::mutex> lock(g_observer_mu);
+    // observed: 16-byte rows on the token-major kernels, flags on, at most 64
+    // segments a thread of the observing CTA
+    sp.observe = g_observer_on && cfg->seg_ready && tma && !(quant_kernel && uses_scatter_pe(sh)) &&
+                 (long long)sh.E * sh.W <= 64LL * 256 && !cfg->performance_info;
+    sp.obs = g_observer;
+  }
+#endif
   if (record(cfg->prof_events, 0, s) != MOE_OK) return MOE_ERR_CUDA;
   if (quant_kernel && tma && uses_scatter_pe(sh)) {
     int launched = 0;

@@ -86,7 +86,15 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
   const Shape sh = p.sh;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n_tok = sh.W * sh.bs;
+#ifdef MOE_FLAG_OBSERVER
+  if (p.observe && blockIdx.x == gridDim.x - 1) {
+    observe_flags(p);
+    return;
+  }
+  const int G = gridDim.x - (p.observe ? 1 : 0);
+#else
   const int G = gridDim.x;
+#endif
   const uint32_t row_in = (uint32_t)sh.row_in, row_out = (uint32_t)sh.row_out;
   const size_t slot_in = align128(row_in);
   uint8_t* xin = smem;                         // [STAGES][slot_in]
@@ -187,6 +195,9 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
     }
   }
   if (tid == 0) bulk_wait_all<0>();
+#ifdef MOE_FLAG_OBSERVER
+  observer_producer_end(p);
+#endif
   if (p.perf) {
     if (tid == 0 && n_done > 0 && !s_abort) perf_mark(p, (size_t)prev_tau);
     __shared__ int s_last;
@@ -256,6 +267,9 @@ static cudaError_t launch_persistent(KernelT kernel, const ScatterParams& p, cud
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int n_tok = p.sh.W * p.sh.bs;
+#ifdef MOE_FLAG_OBSERVER
+  if (p.observe) return launch_observed(kernel, p, st, min(n_tok, num_sms * per_sm - 1) + 1, smem);
+#endif
   const int grid = max(1, min(n_tok, num_sms * per_sm));
   PdlLaunch L(dim3(grid), dim3(kScatterThreads), smem, st);
   return cudaLaunchKernelEx(&L.cfg, kernel, p);

@@ -199,4 +199,99 @@ __device__ __forceinline__ void perf_finish(const ScatterParams& p, int* s_last)
   }
 }
 
+#ifdef MOE_FLAG_OBSERVER
+// Test builds only. The last CTA of a dispatch payload grid (launched
+// cooperatively, so it runs alongside the storing CTAs) watches every
+// segment's ready flag with acquire loads and, the moment a flag holds the
+// call's ticket, copies the segment's rows, assist_info entries and dynamic
+// scales into the observer's buffers. A flag published before its rows were
+// visible would leave rows in the copies that differ from the final output.
+// Warp w takes segments w, w + nwarps, ...; every wait is bounded by the
+// call's timeout (a segment never seen records MOE_ERR_TIMEOUT).
+__device__ __forceinline__ void observe_flags(const ScatterParams& p) {
+  const Shape& sh = p.sh;
+  const int lane = threadIdx.x & 31, nthr = blockDim.x;
+  const int nseg = sh.E * sh.W;  // at most 64 * nthr (host check)
+  const uint32_t row_out = (uint32_t)sh.row_out;
+  const int dyn_row = sh.quant == 4 ? sh.ngroups : sh.ngroups * 4;  // dynamic-scale bytes of a row
+  pdl_wait();
+  const uint64_t t0 = globaltimer_ns();
+  // thread i watches segments i, i + nthr, ... (bit k of pend: segment i + k * nthr)
+  uint64_t pend = 0;
+  for (int k = 0; k < 64; ++k)
+    if ((int)threadIdx.x + k * nthr < nseg) pend |= 1ull << k;
+  while (__any_sync(0xffffffffu, pend != 0)) {
+    // poll every pending flag with relaxed loads (all in flight together);
+    // a segment is read only after its flag is acquired below
+    int found = -1;
+    for (uint64_t m = pend; m; m &= m - 1) {
+      const int k = __ffsll((long long)m) - 1;
+      uint32_t f;
+      asm volatile("ld.relaxed.gpu.global.u32 %0, [%1];" : "=r"(f) : "l"(p.seg_ready + threadIdx.x + k * nthr) : "memory");
+      if (f == p.ticket && found < 0) {
+        found = (int)threadIdx.x + k * nthr;
+        pend &= ~(1ull << k);
+      }
+    }
+    // the warp copies every segment a lane just saw, one after another
+    for (uint32_t b = __ballot_sync(0xffffffffu, found >= 0); b; b &= b - 1) {
+      const int gs = __shfl_sync(0xffffffffu, found, __ffs(b) - 1);
+      // every lane acquires the flag itself before reading the segment
+      if (ld_acquire_gpu(p.seg_ready + gs) != p.ticket) set_error(p.status, MOE_ERR_BAD_ASSIST);
+      const int e = gs / sh.W, d = e / sh.L;
+      const long long b0 = min((long long)max(p.base[gs], 0), (long long)sh.A);
+      const long long r0 = (long long)d * sh.A + b0, n = min((long long)max(p.cnt[gs], 0), (long long)sh.A - b0);
+      const uint8_t* from = static_cast<const uint8_t*>(p.expand_x) + r0 * row_out;
+      uint8_t* to = p.obs.rows + r0 * row_out;
+      const long long bytes = n * (long long)row_out;
+      // four 16-byte loads a lane in flight, then their stores
+      for (long long o = (long long)lane * 16; o < bytes; o += 4 * 32 * 16) {
+        int4 v[4];
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (o + j * 512 < bytes) v[j] = *reinterpret_cast<const int4*>(from + o + j * 512);
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+          if (o + j * 512 < bytes) *reinterpret_cast<int4*>(to + o + j * 512) = v[j];
+      }
+      for (long long o = lane; o < n * 3; o += 32) p.obs.assist[r0 * 3 + o] = p.assist[r0 * 3 + o];
+      if (p.obs.dyn)
+        for (long long o = lane; o < n * dyn_row; o += 32)
+          p.obs.dyn[r0 * dyn_row + o] = static_cast<const uint8_t*>(p.dyn_scales)[r0 * dyn_row + o];
+      __syncwarp();
+      if (lane == 0) {
+        p.obs.seen_ns[gs] = globaltimer_ns();  // every read of the segment has returned
+        atomicAdd(p.obs.n_seen, 1u);
+      }
+    }
+    if (pend && globaltimer_ns() - t0 > p.timeout_ns) {
+      set_error(p.status, MOE_ERR_TIMEOUT);
+      pend = 0;
+    }
+  }
+}
+
+// An observed payload grid: `grid` CTAs (the storing ones and the observer)
+// as one cooperative launch, so that all of them are resident together.
+template <typename KernelT>
+static cudaError_t launch_observed(KernelT kernel, const ScatterParams& p, cudaStream_t st, int grid, size_t smem) {
+  cudaLaunchConfig_t cfg{};
+  cfg.gridDim = dim3(grid);
+  cfg.blockDim = dim3(kScatterThreads);
+  cfg.dynamicSmemBytes = smem;
+  cfg.stream = st;
+  cudaLaunchAttribute a[1];
+  a[0].id = cudaLaunchAttributeCooperative;
+  a[0].val.cooperative = 1;
+  cfg.attrs = a;
+  cfg.numAttrs = 1;
+  return cudaLaunchKernelEx(&cfg, kernel, p);
+}
+
+// A storing CTA of an observed grid ends: its time for the observer.
+__device__ __forceinline__ void observer_producer_end(const ScatterParams& p) {
+  if (p.observe && threadIdx.x == 0) atomicMax(p.obs.producer_end_ns, (unsigned long long)globaltimer_ns());
+}
+#endif
+
 }  // namespace crs

@@ -451,8 +451,16 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
   const Shape sh = p.sh;
   const int tid = threadIdx.x, warp = tid >> 5;
   const int n_tok = sh.W * sh.bs;
+#ifdef MOE_FLAG_OBSERVER
+  if (p.observe && blockIdx.x == gridDim.x - 1) {
+    observe_flags(p);
+    return;
+  }
+  const int G = gridDim.x - (p.observe ? 1 : 0);
+#else
   const int G = gridDim.x;
-  const int my_n = blockIdx.x < n_tok ? (n_tok - 1 - (int)blockIdx.x) / G + 1 : 0;
+#endif
+  const int my_n = (int)blockIdx.x < n_tok ? (n_tok - 1 - (int)blockIdx.x) / G + 1 : 0;
   const uint32_t row_in = (uint32_t)sh.row_in, row_out = (uint32_t)sh.row_out;
   const size_t slot_in = align128(row_in), slot_out = align128(row_out);
   const size_t slot_dyn = align128((size_t)sh.ngroups * 4);
@@ -673,6 +681,9 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     }
   }
   if (tid == 0) bulk_wait_all<0>();
+#ifdef MOE_FLAG_OBSERVER
+  observer_producer_end(p);
+#endif
   if (p.perf) {
     __shared__ int s_last;
     perf_finish(p, &s_last);
@@ -814,6 +825,9 @@ static cudaError_t launch_quant_persistent(KernelT kernel, const ScatterParams& 
   if (e != cudaSuccess) return e;
   if (per_sm < 1) return cudaErrorInvalidConfiguration;
   const int n_tok = p.sh.W * p.sh.bs;
+#ifdef MOE_FLAG_OBSERVER
+  if (p.observe) return launch_observed(kernel, p, st, min(n_tok, num_sms * per_sm - 1) + 1, smem);
+#endif
   const int grid = max(1, min(n_tok, num_sms * per_sm));
   PdlLaunch L(dim3(grid), dim3(kScatterThreads), smem, st);
   return cudaLaunchKernelEx(&L.cfg, kernel, p);
