@@ -207,8 +207,14 @@ __global__ void __launch_bounds__(kReduceThreads, 4) combine_reduce_kernel(Combi
   const long long item = (long long)blockIdx.x * (kReduceThreads / 32) + warp;
   pdl_wait();
   pdl_launch_dependents();
-  if (item >= (long long)sh.W * sh.bs * chunks) return;
-  const size_t tau = (size_t)(item / chunks);
+  const long long n_tok = (long long)sh.W * sh.bs;
+  if (item >= n_tok * chunks) return;
+  // last token first: the dispatch scatter hands out tokens in ascending
+  // order, so the rows of the highest tokens are the newest in L2 when this
+  // kernel starts, and are read before the reduce's own traffic evicts them
+  // (measured on GB300 at 16 ranks x 256 tokens, h 7168: reduce 78.3 -> 74.2
+  // us, dispatch + combine step 155.5 -> 150.1 us)
+  const size_t tau = (size_t)(n_tok - 1 - item / chunks);
   const int c = (int)(item % chunks);
 
   const uint8_t* src = nullptr;
