@@ -118,6 +118,7 @@ struct ScatterParams {
   uint32_t* seg_ready;     // optional ready flags
   uint32_t ticket;
   int32_t* inv;                    // pick -> flat row map (workspace), written for every routed pick
+  int stream_below;                // TMA scatter with streaming stores: tokens below this index use them
   int64_t* perf;                   // per-rank communication time (user array [W]), or null
   unsigned long long* perf_end;    // [W] workspace
   WsHeader* hdr;

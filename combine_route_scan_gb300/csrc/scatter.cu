@@ -19,6 +19,7 @@
 #include <cuda_bf16.h>
 #include <cuda_fp16.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "scatter_common.cuh"
@@ -70,11 +71,12 @@ __device__ __forceinline__ void st_v4_cs(void* p, int4 v) {
                : "memory");
 }
 
-// STREAM: the call writes far more than the L2 holds, so store-plane rows use
-// streaming stores and leave L2 early instead of as dirty lines that the next
-// kernel's loads must first write back (measured at W16 bs256 h7168: dispatch
-// + combine 156.9 -> 152.8 us); a batch whose rows fit in L2 keeps plain
-// stores, so that the consumer can still find them there.
+// STREAM: the call writes far more than the L2 holds, so store-plane rows of
+// tokens below p.stream_below use streaming stores and leave L2 early instead
+// of as dirty lines that the next kernel's loads must first write back
+// (measured at W16 bs256 h7168: dispatch + combine 156.9 -> 152.8 us); the
+// last tokens, and a batch whose rows fit in L2, keep plain stores, so that
+// the consumer can still find them there.
 template <int STAGES, bool STREAM>
 __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterParams p) {
   extern __shared__ __align__(128) uint8_t smem[];
@@ -163,10 +165,11 @@ __global__ void __launch_bounds__(kScatterThreads) scatter_tma_kernel(ScatterPar
       prev_tau = tau;
     }
     if (ns > 0) {
+      const bool cs = STREAM && tau < p.stream_below;
       for (uint32_t v = tid; v < row_in / 16; v += kScatterThreads) {
         const int4 val = *reinterpret_cast<const int4*>(row + v * 16);
         for (int j = 0; j < ns; ++j) {
-          if constexpr (STREAM) st_v4_cs(out + tab.sm_dst[j] * row_out + v * 16, val);
+          if (cs) st_v4_cs(out + tab.sm_dst[j] * row_out + v * 16, val);
           else st_v4(out + tab.sm_dst[j] * row_out + v * 16, val);
         }
       }
@@ -312,11 +315,21 @@ cudaError_t launch_scatter(const ScatterParams& p, cudaStream_t st, int num_sms,
   const bool four = scatter_smem(sh, 4) <= 110 * 1024;
   const size_t smem = scatter_smem(sh, four ? 4 : 2);
   const bool stream = (long long)sh.W * sh.bs * sh.K * sh.row_out > 2 * l2_bytes_of_current_device();
+  // the last tokens' rows, about 3/8 of the L2, keep plain stores: the
+  // combine reduce reads the highest tokens first and finds them in L2
+  // (measured on GB300 at 16 x 256 tokens, h 7168: reduce 74.4 -> 73.1 us,
+  // step 150.7 -> 149.6 us; keeping all of the L2 or none was slower)
+  ScatterParams q = p;
+  {
+    const long long per_tok = (long long)sh.K * sh.row_out;
+    const long long keep = per_tok > 0 ? l2_bytes_of_current_device() * 3 / 8 / per_tok : 0;
+    q.stream_below = (int)std::max(0LL, (long long)sh.W * sh.bs - keep);
+  }
   if (stream)
-    return four ? launch_persistent(scatter_tma_kernel<4, true>, p, st, num_sms, smem)
-                : launch_persistent(scatter_tma_kernel<2, true>, p, st, num_sms, smem);
-  return four ? launch_persistent(scatter_tma_kernel<4, false>, p, st, num_sms, smem)
-              : launch_persistent(scatter_tma_kernel<2, false>, p, st, num_sms, smem);
+    return four ? launch_persistent(scatter_tma_kernel<4, true>, q, st, num_sms, smem)
+                : launch_persistent(scatter_tma_kernel<2, true>, q, st, num_sms, smem);
+  return four ? launch_persistent(scatter_tma_kernel<4, false>, q, st, num_sms, smem)
+              : launch_persistent(scatter_tma_kernel<2, false>, q, st, num_sms, smem);
 }
 
 }  // namespace crs
