@@ -362,3 +362,30 @@ def test_quant_full_size_bench_workload(mode):
     wl = WL.WORKLOADS["w16_bs256_h7168_k8_e256_bf16_zipf"].with_(quant_mode=q, y_dtype=y, scales_kind=k)
     got, ref = run(wl)
     assert np.array_equal(H.to_host(got["seg_plane"]), O.dispatch_plane(wl, ref["ep_recv_count"]))
+
+
+@pytest.mark.parametrize("y", ["fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("policy", ["rule", "bulk"])
+def test_quant_per_expert_fp8_wide_rows(y, policy):
+    """Per-group FP8 with per-expert smoothing on rows wider than the
+    expert-major kernel holds (h 9216 > 8192 elements): the token-major
+    kernel quantises them, a warp a pick; more tokens than resident CTAs."""
+    wl = WL.Workload("qwide", 4, 256, 9216, 4, 16, WL.X_BF16, zero_expert_num=1, copy_expert_num=1, mask_kind=2,
+                     special_p=0.05, mask_false_p=0.1, ids="zipf", quant_mode=3, y_dtype=y, scales_kind=3, seed=81)
+    if policy == "rule":
+        run(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
+    else:
+        run(wl, plane_policy=M.PLANE_BULK_ALL)
+
+
+@pytest.mark.parametrize("dt", [WL.X_FP16, WL.X_BF16])
+def test_quant_per_expert_fp8_expert_major_shapes(dt):
+    """The expert-major per-group FP8 kernel at shapes that exercise its row
+    list and CTA sizing: h 8192 (16 warps, 2 vectors a thread), h 1008 (a
+    partial last group, vectors past the row's end), a run of receive rows
+    longer than one 256-entry list chunk per CTA (16 ranks x 2048 tokens),
+    fp16 and bf16 input."""
+    for h, W, bs in ((8192, 4, 64), (1008, 4, 96), (256, 16, 2048)):
+        wl = WL.Workload(f"qpe_h{h}", W, bs, h, 4, 32, dt, mask_kind=2, mask_false_p=0.1, ids="zipf",
+                         quant_mode=3, y_dtype="fp8_e4m3", scales_kind=3, seed=82 + h)
+        run(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
