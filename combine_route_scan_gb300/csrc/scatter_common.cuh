@@ -274,10 +274,11 @@ __device__ __forceinline__ void observe_flags(const ScatterParams& p) {
 // An observed payload grid: `grid` CTAs (the storing ones and the observer)
 // as one cooperative launch, so that all of them are resident together.
 template <typename KernelT>
-static cudaError_t launch_observed(KernelT kernel, const ScatterParams& p, cudaStream_t st, int grid, size_t smem) {
+static cudaError_t launch_observed(KernelT kernel, const ScatterParams& p, cudaStream_t st, int grid, size_t smem,
+                                   int threads = kScatterThreads) {
   cudaLaunchConfig_t cfg{};
   cfg.gridDim = dim3(grid);
-  cfg.blockDim = dim3(kScatterThreads);
+  cfg.blockDim = dim3(threads);
   cfg.dynamicSmemBytes = smem;
   cfg.stream = st;
   cudaLaunchAttribute a[1];
