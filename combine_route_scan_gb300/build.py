@@ -10,6 +10,12 @@ grid's last CTA watches the ready flags and copies each segment the moment its
 flag is set, so that a test can check that no flag is visible before its rows.
 The binding loads it when the environment variable CRS_MOE_OBSERVER is 1.
 
+``build(phase=True)`` builds the phase-time test variant
+(_build/phase/libcrs_moe.so, ``-DMOE_PHASE_TIMES``): every kernel records its
+earliest CTA start, its CTAs' passage of the wait for the previous kernel and
+its latest CTA end (%globaltimer) for tests/test_phase_times_gpu.py; loaded
+when CRS_MOE_PHASE is 1.
+
 ``build(checked=True)`` builds the bounds-checked variant
 (_build/checked/libcrs_moe.so, ``-DMOE_BOUNDS_CHECK``): every index a kernel
 derives from data is checked against its buffer, and a miss records
@@ -32,6 +38,8 @@ CHECKED_DIR = os.path.join(OUT_DIR, "checked")
 CHECKED_LIB = os.path.join(CHECKED_DIR, "libcrs_moe.so")
 OBSERVER_DIR = os.path.join(OUT_DIR, "observer")
 OBSERVER_LIB = os.path.join(OBSERVER_DIR, "libcrs_moe.so")
+PHASE_DIR = os.path.join(OUT_DIR, "phase")
+PHASE_LIB = os.path.join(PHASE_DIR, "libcrs_moe.so")
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
 NVCC_FLAGS = ["-O3", "-lineinfo", "-std=c++17", "-Xcompiler", "-fPIC", "--expt-relaxed-constexpr",
               "-Xptxas", "-warn-spills"]
@@ -56,14 +64,15 @@ def _inputs_mtime() -> float:
 
 
 def build(force: bool = False, verbose: bool = False, extra_flags=None, checked: bool = False,
-          observer: bool = False) -> str:
-    out_dir, lib = (CHECKED_DIR, CHECKED_LIB) if checked else (OBSERVER_DIR, OBSERVER_LIB) if observer else (OUT_DIR, LIB)
+          observer: bool = False, phase: bool = False) -> str:
+    out_dir, lib = ((CHECKED_DIR, CHECKED_LIB) if checked else (OBSERVER_DIR, OBSERVER_LIB) if observer else
+                    (PHASE_DIR, PHASE_LIB) if phase else (OUT_DIR, LIB))
     os.makedirs(out_dir, exist_ok=True)
     if not force and os.path.exists(lib) and os.path.getmtime(lib) >= _inputs_mtime():
         return lib
     cc = nvcc()
     flags = (NVCC_FLAGS + list(extra_flags or []) + (["-DMOE_BOUNDS_CHECK"] if checked else []) +
-             (["-DMOE_FLAG_OBSERVER"] if observer else []))
+             (["-DMOE_FLAG_OBSERVER"] if observer else []) + (["-DMOE_PHASE_TIMES"] if phase else []))
     if verbose:
         flags = flags + ["-Xptxas", "-v"]
 

@@ -26,10 +26,12 @@ constexpr int kReduceBatch = 8;  // picks whose loads are in flight together
 constexpr int kReduceVpl = 4;    // 16-byte vectors per lane per work item
 
 __global__ void __launch_bounds__(kInvThreads) combine_inverse_kernel(CombineParams p) {
+  MOE_PHASE_BEGIN(p, kPhaseInverse);
   const Shape sh = p.sh;
   const int d = blockIdx.y;
   const int LW = sh.L * sh.W;
   pdl_wait();
+  MOE_PHASE_PAST_WAIT();
   pdl_launch_dependents();
   // the dispatch that wrote these assist_info / ep_recv_count buffers also
   // wrote the map (the reduce still checks every pick against assist_info);
@@ -200,12 +202,14 @@ __device__ __forceinline__ void reduce_vector(const uint8_t* const* src, const u
 // loads in flight to cover HBM latency.
 template <int DT>
 __global__ void __launch_bounds__(kReduceThreads, 4) combine_reduce_kernel(CombineParams p, int chunks, int vpl) {
+  MOE_PHASE_BEGIN(p, kPhaseReduce);
   __shared__ const uint8_t* s_src[kReduceThreads / 32][32];
   __shared__ uint32_t s_w[kReduceThreads / 32][32];
   const Shape sh = p.sh;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long item = (long long)blockIdx.x * (kReduceThreads / 32) + warp;
   pdl_wait();
+  MOE_PHASE_PAST_WAIT();
   pdl_launch_dependents();
   const long long n_tok = (long long)sh.W * sh.bs;
   if (item >= n_tok * chunks) return;

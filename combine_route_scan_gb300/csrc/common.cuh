@@ -43,6 +43,37 @@ __device__ __forceinline__ uint64_t globaltimer_ns() {
   return t;
 }
 
+// ---------------------------------------------------------------- phase times
+// Test builds only (-DMOE_PHASE_TIMES): thread 0 of every CTA of a kernel
+// records, in the 4 words of the kernel's slot, the earliest CTA start and the
+// earliest CTA past griddepcontrol.wait (both kept inverted, so that
+// atomicMax keeps the minimum), the latest CTA past it, and the latest CTA end
+// (%globaltimer ns). Other builds compile the marks to nothing.
+#ifdef MOE_PHASE_TIMES
+struct PhaseScope {
+  unsigned long long* t;
+  __device__ PhaseScope(unsigned long long* base, int slot) : t(base ? base + slot * 4 : nullptr) {
+    if (t && threadIdx.x == 0) atomicMax(t + 0, ~globaltimer_ns());
+  }
+  __device__ void past_wait() {
+    if (t && threadIdx.x == 0) {
+      const unsigned long long g = globaltimer_ns();
+      atomicMax(t + 1, ~g);
+      atomicMax(t + 2, g);
+    }
+  }
+  __device__ ~PhaseScope() {
+    if (t && threadIdx.x == 0) atomicMax(t + 3, globaltimer_ns());
+  }
+};
+#define MOE_PHASE_BEGIN(params, slot) ::crs::PhaseScope moe_phase_scope((params).phase, (slot))
+#define MOE_PHASE_PAST_WAIT() moe_phase_scope.past_wait()
+#else
+#define MOE_PHASE_BEGIN(params, slot) ((void)0)
+#define MOE_PHASE_PAST_WAIT() ((void)0)
+#endif
+enum { kPhaseRoute = 0, kPhaseScatter = 1, kPhaseInverse = 2, kPhaseReduce = 3 };
+
 // ---------------------------------------------------------------- PDL
 
 // Wait until the previous kernel in the stream has completed and its memory

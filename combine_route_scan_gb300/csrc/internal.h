@@ -84,6 +84,9 @@ struct RouteParams {
   const int32_t* assist_out;
   uint32_t* zero_words;    // optional: words the routing kernel clears for the kernels after it
   int n_zero_words;
+#ifdef MOE_PHASE_TIMES
+  unsigned long long* phase;  // test builds: per-kernel phase times
+#endif
 };
 
 #ifdef MOE_FLAG_OBSERVER
@@ -129,6 +132,9 @@ struct ScatterParams {
   FlagObserver obs;
   int observe;  // the grid's last CTA observes instead of storing
 #endif
+#ifdef MOE_PHASE_TIMES
+  unsigned long long* phase;  // test builds: per-kernel phase times
+#endif
 };
 
 struct CombineParams {
@@ -155,6 +161,9 @@ struct CombineParams {
   int put_only;
   int tp_rows;             // two-phase: rows per warp batch (1..32)
   uint64_t timeout_ns;
+#ifdef MOE_PHASE_TIMES
+  unsigned long long* phase;  // test builds: per-kernel phase times
+#endif
 };
 
 // Everything the expert-FFN grouped GEMMs need.

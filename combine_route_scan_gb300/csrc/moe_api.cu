@@ -312,6 +312,21 @@ moe_status_t moe_workspace_init(const moe_config_t* cfg, void* ws, size_t ws_byt
   return MOE_OK;
 }
 
+#ifdef MOE_PHASE_TIMES
+namespace {
+std::atomic<unsigned long long*> g_phase{nullptr};
+}  // namespace
+
+// Test builds only (not declared in include/moe.h): the kernels of the next
+// calls record their phase times into `buf`, a device array of 16 words
+// (4 a kernel: routing, scatter, inverse map, reduce; see PhaseScope), which
+// the caller zeroes before a call. NULL turns the recording off.
+moe_status_t moe_test_set_phase_buffer(void* buf) {
+  g_phase.store(static_cast<unsigned long long*>(buf));
+  return MOE_OK;
+}
+#endif
+
 #ifdef MOE_FLAG_OBSERVER
 namespace {
 std::mutex g_observer_mu;
@@ -390,6 +405,9 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   rp.ticket = cfg->seg_ready_ticket;
   rp.hdr = hdr;
   rp.assist_out = assist_info;
+#ifdef MOE_PHASE_TIMES
+  rp.phase = g_phase.load();
+#endif
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
   note_launches(1);
 
@@ -417,6 +435,9 @@ moe_status_t moe_dispatch(const moe_config_t* cfg, const void* x, const int32_t*
   sp.sh = sh;
   sp.status = &hdr->status;
   sp.timeout_ns = timeout_ns(cfg);
+#ifdef MOE_PHASE_TIMES
+  sp.phase = g_phase.load();
+#endif
 #ifdef MOE_FLAG_OBSERVER
   {
     std::lock_guard<std::mutex> lock(g_observer_mu);
@@ -486,6 +507,9 @@ moe_status_t moe_combine(const moe_config_t* cfg, const void* expert_out, const 
   cp.plane_policy = cfg->plane_policy;
   cp.bulk_min_bytes = cfg->bulk_min_bytes;
   cp.timeout_ns = timeout_ns(cfg);
+#ifdef MOE_PHASE_TIMES
+  cp.phase = g_phase.load();
+#endif
   cp.seg_plane_out = seg_plane;
   if (empty) return MOE_OK;
   if (cfg->combine_mode == MOE_COMBINE_GATHER) {
@@ -564,6 +588,9 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   rp.status = &hdr->status;
   rp.hdr = hdr;
   rp.assist_out = assist;
+#ifdef MOE_PHASE_TIMES
+  rp.phase = g_phase.load();
+#endif
   rp.zero_words = reinterpret_cast<uint32_t*>(w + L.ffn_done);
   rp.n_zero_words = sh.E;
   if (launch_route(rp, s) != cudaSuccess) return MOE_ERR_CUDA;
@@ -582,6 +609,9 @@ moe_status_t moe_dispatch_ffn_combine(const moe_config_t* cfg, const void* x, co
   sp.status = &hdr->status;
   sp.hdr = hdr;
   sp.timeout_ns = timeout_ns(cfg);
+#ifdef MOE_PHASE_TIMES
+  sp.phase = g_phase.load();
+#endif
   if (!empty && launch_scatter(sp, s, nsm, tma) != cudaSuccess) return MOE_ERR_CUDA;
   if (empty) return MOE_OK;
   note_launches(1);

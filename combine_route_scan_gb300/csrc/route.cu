@@ -94,6 +94,7 @@ constexpr uint64_t kExchangeTimeoutNs = 2000000000ull;  // bound on the count ex
 // kRegIters iterations and barriers are short), else 1024.
 template <bool CLUSTER, int THREADS>
 __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
+  MOE_PHASE_BEGIN(p, kPhaseRoute);
   constexpr int kRouteThreads = THREADS;
   constexpr int kRouteWarps = THREADS / 32;
   // wcnt [kRouteWarps][E], tot [E], recv [E] (cluster form: the L*W counts
@@ -123,6 +124,7 @@ __global__ void __launch_bounds__(THREADS) route_kernel(RouteParams p) {
     cluster_arrive_relaxed();
   }
   pdl_wait();
+  MOE_PHASE_PAST_WAIT();
   pdl_launch_dependents();
 
   for (int i = tid; i < kRouteWarps * E; i += kRouteThreads) wcnt[i] = 0;

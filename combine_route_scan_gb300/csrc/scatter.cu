@@ -83,6 +83,7 @@ __device__ __forceinline__ void st_v4_cs(void* p, int4 v) {
 constexpr int kTmaThreads = 512;
 template <int STAGES, bool STREAM>
 __global__ void __launch_bounds__(kTmaThreads) scatter_tma_kernel(ScatterParams p) {
+  MOE_PHASE_BEGIN(p, kPhaseScatter);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[STAGES];
   __shared__ int s_tok[STAGES];  // token held by each slot, -1 once the tokens ran out
@@ -127,6 +128,7 @@ __global__ void __launch_bounds__(kTmaThreads) scatter_tma_kernel(ScatterParams 
     }
   }
   pdl_wait();  // routing results (and the zeroed ticket counter) are visible from here on
+  MOE_PHASE_PAST_WAIT();
   pdl_launch_dependents();
   if (p.perf && tid == 0) perf_begin(p);
   // thread 0 claims each ticket one token ahead of its use, so the atomic's

@@ -442,6 +442,7 @@ __device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, con
 // PE: per-expert scales (every pick's row is different).
 template <int MODE, int DT, int YT, bool PE>
 __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !PE)) ? 5 : 0) scatter_quant_kernel(ScatterParams p) {
+  MOE_PHASE_BEGIN(p, kPhaseScatter);
   extern __shared__ __align__(128) uint8_t smem[];
   __shared__ __align__(8) uint64_t full_bar[kQStages];
   __shared__ PickTable tabs[2];
@@ -490,6 +491,7 @@ __global__ void __launch_bounds__(kScatterThreads, (MODE == 2 || (MODE != 1 && !
     }
   }
   pdl_wait();  // routing results are visible from here on
+  MOE_PHASE_PAST_WAIT();
   pdl_launch_dependents();
   if (p.perf && tid == 0) perf_begin(p);
 

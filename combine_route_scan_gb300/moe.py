@@ -16,9 +16,11 @@ import torch
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 # CRS_MOE_CHECKED=1 selects the bounds-checked build (build.build(checked=True)),
-# CRS_MOE_OBSERVER=1 the flag-observer test build (build.build(observer=True))
+# CRS_MOE_OBSERVER=1 the flag-observer test build (build.build(observer=True)),
+# CRS_MOE_PHASE=1 the phase-time test build (build.build(phase=True))
 LIB_PATH = os.path.join(_HERE, "_build", *(["checked"] if os.environ.get("CRS_MOE_CHECKED") == "1" else
-                                           ["observer"] if os.environ.get("CRS_MOE_OBSERVER") == "1" else []),
+                                           ["observer"] if os.environ.get("CRS_MOE_OBSERVER") == "1" else
+                                           ["phase"] if os.environ.get("CRS_MOE_PHASE") == "1" else []),
                         "libcrs_moe.so")
 
 MOE_OK = 0
