@@ -109,7 +109,10 @@ __global__ void __launch_bounds__(kTmaThreads) scatter_tma_kernel(ScatterParams 
   uint8_t* out = static_cast<uint8_t*>(p.expand_x);
 
   if (tid == 0) {
-    for (int i = 0; i < STAGES; ++i) mbar_init(&full_bar[i], 1);
+    for (int i = 0; i < STAGES; ++i) {
+      mbar_init(&full_bar[i], 1);
+      s_tok[i] = -1;  // slots past the end of the tokens are never filled
+    }
     mbar_fence_init();
     s_abort = 0;
   }
@@ -136,7 +139,6 @@ __global__ void __launch_bounds__(kTmaThreads) scatter_tma_kernel(ScatterParams 
   unsigned ticket = 0;
   if (tid == 0 && !exhausted) ticket = atomicAdd(&p.hdr->scatter_next, 1u);
   int prev_tau = -1;  // thread 0: last token handled (performance info)
-
   int n_done = 0;
   for (int i = 0;; ++i) {
     const int stage = i % STAGES;
