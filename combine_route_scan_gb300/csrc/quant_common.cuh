@@ -189,4 +189,45 @@ __device__ __forceinline__ void unpack8x2(int4 v, f32x2 (&o)[4]) {
   }
 }
 
+// The per-token int8 codes of one 8-element vector through the IEEE division
+// (the rare vectors whose reciprocal form is undecided), out of line so that
+// the main path carries none of its instructions.
+static __device__ __noinline__ uint2 token_codes_div8(f32x2 v0, f32x2 v1, f32x2 v2, f32x2 v3, float scale, float amax) {
+  const f32x2 v[4] = {v0, v1, v2, v3};
+  int qv[8];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    float lo, hi;
+    f2_split(v[i], lo, hi);
+    qv[2 * i] = amax == 0.f ? 0 : token_q(lo, scale);
+    qv[2 * i + 1] = amax == 0.f ? 0 : token_q(hi, scale);
+  }
+  return pack8(qv);
+}
+
+// Per-token int8 codes of 8 products v through the reciprocal r = fl(1/scale):
+// rounding y = v * r to an integer (adding 1.5 * 2^23, the code then in the
+// low byte) gives the code of the IEEE quotient unless y lies within 2^-14 of
+// a half-integer (the argument at token_code); one test for the vector, whose
+// rare failures take the division.
+__device__ __forceinline__ uint2 token_codes8(const f32x2 (&v)[4], float scale, float amax, bool fast, f32x2 rcp2) {
+  const f32x2 shift2 = f2_pack(kRoundShift, kRoundShift);
+  uint32_t c[8];
+  float dm = 0.f;
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const f32x2 y = f2_mul(v[i], rcp2);
+    const f32x2 t = f2_add(y, shift2);
+    const f32x2 d = f2_sub(y, f2_sub(t, shift2));
+    float dl, dh, tl, th;
+    f2_split(d, dl, dh);
+    f2_split(t, tl, th);
+    dm = fmax_abs3(dm, dl, dh);
+    c[2 * i] = __float_as_uint(tl);
+    c[2 * i + 1] = __float_as_uint(th);
+  }
+  if (!(fast && dm <= kNearHalf)) return token_codes_div8(v[0], v[1], v[2], v[3], scale, amax);
+  return pack8_low(c);
+}
+
 }  // namespace crs

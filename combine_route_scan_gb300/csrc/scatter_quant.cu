@@ -407,33 +407,44 @@ __device__ __forceinline__ void quantize_pick_warp_mode2(const uint8_t* row, con
                                                          uint8_t* dyn, long long dst, uint32_t row_out,
                                                          uint32_t nvec) {
   const int lane = threadIdx.x & 31;
-  float m = 0.f;
+  // products v = x * s as fp32 pairs (packed multiplies), x from the staged
+  // row and s from the expert's scales row, recomputed in the second pass
+  auto products = [&](uint32_t v, f32x2 (&p)[4]) {
+    f32x2 xp[4];
+    unpack8x2<DT>(*reinterpret_cast<const int4*>(row + v * 16), xp);
+    const ulonglong2 a = __ldg(reinterpret_cast<const ulonglong2*>(srow) + 2 * v);
+    const ulonglong2 b = __ldg(reinterpret_cast<const ulonglong2*>(srow) + 2 * v + 1);
+    p[0] = f2_mul(xp[0], a.x);
+    p[1] = f2_mul(xp[1], a.y);
+    p[2] = f2_mul(xp[2], b.x);
+    p[3] = f2_mul(xp[3], b.y);
+  };
+  float m0 = 0.f, m1 = 0.f;
   for (uint32_t v = lane; v < nvec; v += 32) {
-    float f[8], sc[8];
-    unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-    load_scales8(srow, v, sc);
-#pragma unroll
-    for (int i = 0; i < 8; ++i) m = fmaxf(m, fabsf(__fmul_rn(f[i], sc[i])));
+    f32x2 p[4];
+    products(v, p);
+    float a0, a1, b0, b1;
+    f2_split(p[0], a0, a1);
+    f2_split(p[1], b0, b1);
+    m0 = fmax_abs3(m0, a0, a1);
+    m1 = fmax_abs3(m1, b0, b1);
+    f2_split(p[2], a0, a1);
+    f2_split(p[3], b0, b1);
+    m0 = fmax_abs3(m0, a0, a1);
+    m1 = fmax_abs3(m1, b0, b1);
   }
+  float m = fmaxf(m0, m1);
 #pragma unroll
   for (int o = 16; o > 0; o >>= 1) m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, o));
   const float scale = __fdiv_rn(m, 127.0f);
   const bool fast = token_rcp_ok(scale);
   const float rcp = fast ? __frcp_rn(scale) : 0.f;
+  const f32x2 rcp2 = f2_pack(rcp, rcp);
   uint8_t* q = out + dst * row_out;
   for (uint32_t v = lane; v < nvec; v += 32) {
-    float f[8], sc[8];
-    unpack8<DT>(*reinterpret_cast<const int4*>(row + v * 16), f);
-    load_scales8(srow, v, sc);
-    uint32_t c[8];
-    if (fast) {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = token_code(__fmul_rn(f[i], sc[i]), scale, rcp);
-    } else {
-#pragma unroll
-      for (int i = 0; i < 8; ++i) c[i] = m == 0.f ? 0u : (uint32_t)token_q(__fmul_rn(f[i], sc[i]), scale);
-    }
-    *reinterpret_cast<uint2*>(q + v * 8) = pack8_low(c);
+    f32x2 p[4];
+    products(v, p);
+    *reinterpret_cast<uint2*>(q + v * 8) = token_codes8(p, scale, m, fast, rcp2);
   }
   if (lane == 0) reinterpret_cast<float*>(dyn)[dst] = scale;
 }
