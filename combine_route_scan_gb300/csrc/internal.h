@@ -39,7 +39,7 @@ struct WsLayout {
   size_t plane_c;  // uint8 [E*W]     two-phase combine plane per segment
   size_t flags;    // uint32 [W*bs*K] two-phase combine ready flags
   size_t window;   // [W*bs*K][h]     two-phase combine window
-  size_t pe_list;  // int4 [W*A]      per-group FP8 with per-expert scales: {row, token, expert, plane} of every receive row
+  size_t pe_list;  // int4 [W*A]      per-token int8 / per-group FP8 with per-expert scales: {row, token, expert, plane} of every receive row
   // moe_dispatch_ffn_combine only
   size_t ffn_expand_x;   // bf16 [W*A][h]
   size_t ffn_assist;     // int32 [W*A][3]

@@ -160,7 +160,7 @@ WsLayout make_layout(const moe_config_t* c, const Shape& sh) {
   L.perf_end = take((size_t)sh.W * 8);
   L.rank = take(picks * 4);
   L.inv = take(picks * 4);
-  if (c->quant_mode == 3 && c->scales_kind == MOE_SCALES_EXPERT) L.pe_list = take((size_t)sh.W * sh.A * 16);
+  if ((c->quant_mode == 2 || c->quant_mode == 3) && c->scales_kind == MOE_SCALES_EXPERT) L.pe_list = take((size_t)sh.W * sh.A * 16);
   if (c->combine_mode != MOE_COMBINE_GATHER) {
     L.plane_c = take(segs);
     L.flags = take(picks * 4);

@@ -162,6 +162,11 @@ __device__ __forceinline__ f32x2 f2_sub(f32x2 a, f32x2 b) {
   asm("sub.rn.f32x2 %0, %1, %2;" : "=l"(d) : "l"(a), "l"(b));
   return d;
 }
+__device__ __forceinline__ f32x2 f2_fma(f32x2 a, f32x2 b, f32x2 c) {
+  f32x2 d;
+  asm("fma.rn.f32x2 %0, %1, %2, %3;" : "=l"(d) : "l"(a), "l"(b), "l"(c));
+  return d;
+}
 // max(a, |b|, |c|) and min(a, |b|, |c|), one three-input instruction each
 __device__ __forceinline__ float fmax_abs3(float a, float b, float c) {
   float d;

@@ -15,7 +15,7 @@ ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
 SELECTION = [
     ("tests/test_parity_gpu.py", "random_small or empty_batch or ready_flags or two_phase_matches or reuses "
                                  "or row_map or performance_info or one_expert or all_masked"),
-    ("tests/test_quant_gpu.py", "small_tma_rows or ragged or bulk_plane or random_shapes "
+    ("tests/test_quant_gpu.py", "small_tma_rows or ragged or bulk_plane or random_shapes or expert_major "
                                "or (many_tokens_per_cta and (q2_int8_s3 or q3_fp8_e4m3_s0 or q3_fp8_e4m3_s3 or q4_fp4_e2m1_s0))"),
     ("tests/test_ffn_gpu.py", "small_all_tokens or several_token_passes"),
 ]

@@ -21,6 +21,8 @@ if torch.cuda.is_available():
 # (quant_mode, expand type, scales kind)
 MODES = [(1, "", 1), (1, "", 2), (1, "", 3), (2, "", 3), (3, "fp8_e4m3", 0), (3, "fp8_e5m2", 0),
          (3, "fp8_e4m3", 3), (4, "fp8_e4m3", 0), (4, "fp8_e5m2", 0), (4, "fp4_e2m1", 0)]
+# the modes with per-expert smoothing and a data-dependent scale (the expert-major kernel)
+PE_MODES = [(2, "", 3), (3, "fp8_e4m3", 3), (3, "fp8_e5m2", 3)]
 
 
 def mode_id(m):
@@ -205,6 +207,72 @@ def test_group_fp8_ties_and_near_midpoint_quotients(y, k, dt):
     H.compare_dispatch(wl, got, ref)
 
 
+def _fragile_rows(wl, inp, rng):
+    """Every other token a row whose quotients sit on or next to rounding
+    boundaries of the quantisation (exact half-integers for per-token int8 with
+    power-of-two smoothing rows; FP8 midpoints moved a few fp32 ulps by
+    smoothing rows 1 + r * 2^-10 for per-group FP8); the other tokens keep
+    their random values."""
+    W, bs, h, E, dt = wl.ep_world_size, wl.bs, wl.h, wl.moe_expert_num, wl.x_dtype
+    x = _from_input_type(inp["x"], dt).astype(np.float64).reshape(W, bs, h)
+    for s in range(W):
+        for t in range(0, bs, 2):
+            if wl.quant_mode == 2:
+                j = float(rng.integers(-4, 5))
+                row = (rng.integers(-127, 127, size=h) + 0.5) * 2.0 ** j
+                row[0] = 127.0 * 2.0 ** j
+            else:
+                fmax, mbits, e_top = (448.0, 3, 8) if wl.y_dtype == "fp8_e4m3" else (57344.0, 2, 15)
+                row = np.empty(h)
+                for g0 in range(0, h, 128):
+                    n = min(128, h - g0)
+                    e = rng.integers(e_top - 6, e_top + 1, size=n)
+                    m = rng.integers(2 ** mbits, 2 ** (mbits + 1), size=n)
+                    mid = np.minimum((m + 0.5) * 2.0 ** (e - mbits), fmax) * rng.choice([-1.0, 1.0], size=n)
+                    mid[0] = fmax
+                    row[g0:g0 + n] = mid * 2.0 ** float(rng.integers(-3, 1))
+            x[s, t] = row
+    inp["x"] = _to_input_type(x, dt)
+    if wl.quant_mode == 2:
+        inp["quant_scales"] = np.repeat(2.0 ** rng.integers(-2, 3, size=(E, 1)), h, axis=1).astype(np.float32)
+    else:
+        r = 1.0 + rng.integers(1, 1024, size=(E, 1)) * 2.0 ** -10
+        inp["quant_scales"] = np.repeat(r, h, axis=1).astype(np.float32)
+
+
+@pytest.mark.parametrize("mode", PE_MODES, ids=mode_id)
+@pytest.mark.parametrize("policy", ["rule", "bulk"])
+def test_quant_per_expert_deferred_exact_codes(mode, policy):
+    """The expert-major kernel's exact path: rows whose quotients sit on
+    rounding boundaries make most of their threads queue for the IEEE
+    division after the CTA's last row, enough to overflow the queue (every
+    row from there recomputed whole), mixed with random rows; store and bulk
+    planes, ready flags and per-rank times on. Bytes against the oracle, every
+    segment's flag set, status OK."""
+    q, y, k = mode
+    wl = WL.Workload("qdx", 4, 256, 2048, 4, 32, WL.X_BF16, mask_kind=2, mask_false_p=0.1, ids="zipf",
+                     quant_mode=q, y_dtype=y, scales_kind=k, seed=88)
+    inp = WL.make_inputs(wl)
+    _fragile_rows(wl, inp, np.random.Generator(np.random.PCG64(880)))
+    ref = O.dispatch(wl, inp)
+    dev = H.device_inputs(wl, inp)
+    L = wl.moe_expert_num // wl.ep_world_size
+    cfg = H.make_cfg(wl, plane_policy=M.PLANE_RULE if policy == "rule" else M.PLANE_BULK_ALL,
+                     bulk_min_bytes=0 if policy == "rule" else M.BULK_MIN_BYTES)
+    ws = M.alloc_workspace(cfg)
+    out = M.alloc_dispatch_outputs(cfg, H.TORCH_DT[wl.x_dtype])
+    flags = torch.zeros((wl.ep_world_size, L * wl.ep_world_size), dtype=torch.int32, device="cuda")
+    perf = torch.zeros(wl.ep_world_size, dtype=torch.int64, device="cuda")
+    c = M.with_performance_info(M.with_seg_ready(cfg, flags, 9), perf)
+    M.dispatch(c, dev["x"], dev["expert_ids"], dev["active_mask"], dev["expert_scales"], out["expand_x"],
+               out["dynamic_scales"], out["assist_info"], out["ep_recv_count"], out["expand_scales"], None, ws,
+               scales=dev["quant_scales"])
+    assert M.get_device_status(ws) == 0
+    assert bool((flags == 9).all())
+    assert bool((perf >= 0).all())
+    H.compare_dispatch(wl, out, ref)
+
+
 def test_quant_ready_flags_and_performance_info():
     """The quantising scatter publishes ready flags and per-rank times too."""
     wl = WL.Workload("qf", 4, 24, 512, 4, 16, WL.X_BF16, quant_mode=3, y_dtype="fp8_e4m3", scales_kind=3, seed=35)
@@ -364,28 +432,34 @@ def test_quant_full_size_bench_workload(mode):
     assert np.array_equal(H.to_host(got["seg_plane"]), O.dispatch_plane(wl, ref["ep_recv_count"]))
 
 
-@pytest.mark.parametrize("y", ["fp8_e4m3", "fp8_e5m2"])
+@pytest.mark.parametrize("mode", PE_MODES, ids=mode_id)
 @pytest.mark.parametrize("policy", ["rule", "bulk"])
-def test_quant_per_expert_fp8_wide_rows(y, policy):
-    """Per-group FP8 with per-expert smoothing on rows wider than the
-    expert-major kernel holds (h 9216 > 8192 elements): the token-major
-    kernel quantises them, a warp a pick; more tokens than resident CTAs."""
-    wl = WL.Workload("qwide", 4, 256, 9216, 4, 16, WL.X_BF16, zero_expert_num=1, copy_expert_num=1, mask_kind=2,
-                     special_p=0.05, mask_false_p=0.1, ids="zipf", quant_mode=3, y_dtype=y, scales_kind=3, seed=81)
+def test_quant_per_expert_wide_rows(mode, policy):
+    """Per-token int8 and per-group FP8 with per-expert smoothing on rows wider
+    than the expert-major kernel holds (h 16640 > 15360 elements): the
+    token-major kernel quantises them, a warp a pick; more tokens than
+    resident CTAs."""
+    q, y, k = mode
+    wl = WL.Workload("qwide", 4, 256, 16640, 4, 16, WL.X_BF16, zero_expert_num=1, copy_expert_num=1, mask_kind=2,
+                     special_p=0.05, mask_false_p=0.1, ids="zipf", quant_mode=q, y_dtype=y, scales_kind=k, seed=81)
     if policy == "rule":
         run(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
     else:
         run(wl, plane_policy=M.PLANE_BULK_ALL)
 
 
+@pytest.mark.parametrize("mode", PE_MODES, ids=mode_id)
 @pytest.mark.parametrize("dt", [WL.X_FP16, WL.X_BF16])
-def test_quant_per_expert_fp8_expert_major_shapes(dt):
-    """The expert-major per-group FP8 kernel at shapes that exercise its row
-    list and CTA sizing: h 8192 (16 warps, 2 vectors a thread), h 1008 (a
-    partial last group, vectors past the row's end), a run of receive rows
-    longer than one 256-entry list chunk per CTA (16 ranks x 2048 tokens),
-    fp16 and bf16 input."""
-    for h, W, bs in ((8192, 4, 64), (1008, 4, 96), (256, 16, 2048)):
+def test_quant_per_expert_expert_major_shapes(mode, dt):
+    """The expert-major kernel (per-token int8 and per-group FP8 with
+    per-expert smoothing) at shapes that exercise its row list and CTA
+    sizing: h 9216 (9 warps, 4 vectors a thread), h 8192 (8 warps), h 1008
+    (one warp, a partial last group, vectors past the row's end), a run of
+    receive rows longer than one 256-entry list chunk per CTA (16 ranks x 2048
+    tokens), fp16 and bf16 input; bulk plane for every remote segment above
+    zero bytes."""
+    q, y, k = mode
+    for h, W, bs in ((9216, 4, 64), (8192, 4, 64), (1008, 4, 96), (256, 16, 2048)):
         wl = WL.Workload(f"qpe_h{h}", W, bs, h, 4, 32, dt, mask_kind=2, mask_false_p=0.1, ids="zipf",
-                         quant_mode=3, y_dtype="fp8_e4m3", scales_kind=3, seed=82 + h)
+                         quant_mode=q, y_dtype=y, scales_kind=k, seed=82 + h)
         run(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
