@@ -453,13 +453,14 @@ def test_quant_per_expert_wide_rows(mode, policy):
 def test_quant_per_expert_expert_major_shapes(mode, dt):
     """The expert-major kernel (per-token int8 and per-group FP8 with
     per-expert smoothing) at shapes that exercise its row list and CTA
-    sizing: h 9216 (9 warps, 4 vectors a thread), h 8192 (8 warps), h 1008
+    sizing: h 15360 (the widest row it takes: 15 warps and the producer, 512
+    threads), h 9216 (9 warps, 4 vectors a thread), h 8192 (8 warps), h 1008
     (one warp, a partial last group, vectors past the row's end), a run of
     receive rows longer than one 256-entry list chunk per CTA (16 ranks x 2048
     tokens), fp16 and bf16 input; bulk plane for every remote segment above
     zero bytes."""
     q, y, k = mode
-    for h, W, bs in ((9216, 4, 64), (8192, 4, 64), (1008, 4, 96), (256, 16, 2048)):
+    for h, W, bs in ((15360, 2, 64), (9216, 4, 64), (8192, 4, 64), (1008, 4, 96), (256, 16, 2048)):
         wl = WL.Workload(f"qpe_h{h}", W, bs, h, 4, 32, dt, mask_kind=2, mask_false_p=0.1, ids="zipf",
                          quant_mode=q, y_dtype=y, scales_kind=k, seed=82 + h)
         run(wl, plane_policy=M.PLANE_RULE, bulk_min_bytes=0)
