@@ -7,6 +7,7 @@ from __future__ import annotations
 
 import os
 import subprocess
+import threading
 
 HERE = os.path.dirname(os.path.abspath(__file__))
 SRC = os.path.join(HERE, "moe_oracle.c")
@@ -18,7 +19,8 @@ def build(force: bool = False) -> str:
     os.makedirs(OUT_DIR, exist_ok=True)
     if not force and os.path.exists(LIB) and os.path.getmtime(LIB) >= os.path.getmtime(SRC):
         return LIB
-    tmp = LIB + f".tmp{os.getpid()}"
+    # unique per process and thread: concurrent first builds never share a file
+    tmp = LIB + f".tmp{os.getpid()}.{threading.get_ident()}"
     cmd = ["gcc", "-O2", "-std=gnu11", "-ffp-contract=off", "-fno-fast-math", "-Wall",
            "-fPIC", "-shared", "-o", tmp, SRC, "-lm"]
     subprocess.run(cmd, check=True)

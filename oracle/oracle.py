@@ -8,6 +8,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import threading
 from typing import Optional
 
 import numpy as np
@@ -35,6 +36,7 @@ class OrcCfg(ctypes.Structure):
 
 _lib = None
 _lib_path_override = None
+_lib_lock = threading.Lock()
 
 
 def use_library(path: Optional[str]) -> None:
@@ -48,35 +50,41 @@ def use_library(path: Optional[str]) -> None:
 def lib():
     global _lib
     if _lib is None:
-        path = _lib_path_override or _build.build()
-        L = ctypes.CDLL(path)
-        P = ctypes.c_void_p
-        C = ctypes.POINTER(OrcCfg)
-        L.orc_check_cfg.argtypes = [C]
-        L.orc_capacity.argtypes = [C]
-        L.orc_capacity.restype = ctypes.c_int64
-        L.orc_dispatch.argtypes = [C, P, P, P, P, P, P, P, P, P, P]
-        L.orc_combine.argtypes = [C, P, P, P, P, P, P, P, P]
-        L.orc_combine_plane.argtypes = [C, P, P]
-        L.orc_dispatch_plane.argtypes = [C, P, P]
-        L.orc_swiglu_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
-                                      P, P, P, P, P, P]
-        L.orc_moe_ffn_tokens.argtypes = [C, ctypes.c_int, ctypes.c_int64, P, P, P, P, P, P, P, P, P]
-        L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
-        L.orc_f32_to_bf16.restype = ctypes.c_uint16
-        L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
-        L.orc_bf16_to_f32.restype = ctypes.c_float
-        L.orc_f32_to_fp16.argtypes = [ctypes.c_float]
-        L.orc_f32_to_fp16.restype = ctypes.c_uint16
-        L.orc_fp16_to_f32.argtypes = [ctypes.c_uint16]
-        L.orc_fp16_to_f32.restype = ctypes.c_float
-        L.orc_quantize_row.argtypes = [C, P, P]
-        L.orc_quantize_row.restype = ctypes.c_float
-        L.orc_f32_to_minifloat.argtypes = [ctypes.c_float, ctypes.c_int]
-        L.orc_f32_to_minifloat.restype = ctypes.c_uint8
-        L.orc_quantize_pick.argtypes = [C, P, ctypes.c_int32, P, P, P]
-        _lib = L
+        with _lib_lock:  # the tests call the oracle from thread pools
+            if _lib is None:
+                _lib = _load()
     return _lib
+
+
+def _load():
+    path = _lib_path_override or _build.build()
+    L = ctypes.CDLL(path)
+    P = ctypes.c_void_p
+    C = ctypes.POINTER(OrcCfg)
+    L.orc_check_cfg.argtypes = [C]
+    L.orc_capacity.argtypes = [C]
+    L.orc_capacity.restype = ctypes.c_int64
+    L.orc_dispatch.argtypes = [C, P, P, P, P, P, P, P, P, P, P]
+    L.orc_combine.argtypes = [C, P, P, P, P, P, P, P, P]
+    L.orc_combine_plane.argtypes = [C, P, P]
+    L.orc_dispatch_plane.argtypes = [C, P, P]
+    L.orc_swiglu_rows.argtypes = [ctypes.c_int, ctypes.c_int, ctypes.c_int, ctypes.c_int64,
+                                  P, P, P, P, P, P]
+    L.orc_moe_ffn_tokens.argtypes = [C, ctypes.c_int, ctypes.c_int64, P, P, P, P, P, P, P, P, P]
+    L.orc_f32_to_bf16.argtypes = [ctypes.c_float]
+    L.orc_f32_to_bf16.restype = ctypes.c_uint16
+    L.orc_bf16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_bf16_to_f32.restype = ctypes.c_float
+    L.orc_f32_to_fp16.argtypes = [ctypes.c_float]
+    L.orc_f32_to_fp16.restype = ctypes.c_uint16
+    L.orc_fp16_to_f32.argtypes = [ctypes.c_uint16]
+    L.orc_fp16_to_f32.restype = ctypes.c_float
+    L.orc_quantize_row.argtypes = [C, P, P]
+    L.orc_quantize_row.restype = ctypes.c_float
+    L.orc_f32_to_minifloat.argtypes = [ctypes.c_float, ctypes.c_int]
+    L.orc_f32_to_minifloat.restype = ctypes.c_uint8
+    L.orc_quantize_pick.argtypes = [C, P, ctypes.c_int32, P, P, P]
+    return L
 
 
 class OracleError(RuntimeError):
