@@ -361,11 +361,11 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
   __shared__ __align__(16) int4 s_list[2][kPeChunk];
   __shared__ __align__(16) int4 s_desc[kPeStages];          // the clamped list entry of each staged row
   __shared__ __align__(16) float s_part[2][kPeMaxWarps];    // per-token int8: warp maxima, by row parity
-  __shared__ float s_gm[MODE == 3 ? 2 : 1][kPeMaxGroups];   // per-group FP8: group maxima, by row parity
+  __shared__ float s_gm[MODE == 3 ? 4 : 1][kPeMaxGroups];   // per-group FP8: group maxima, by row % 4
   __shared__ __align__(16) int4 s_fixq[kPeFixCap];         // queued threads: {row, thread, row maximum}
   __shared__ int s_nfix;                                    // entries queued (may exceed the capacity)
   __shared__ int s_ovf;                                     // the first row whose entry did not fit
-  __shared__ int s_rowfix[2];                               // the row of this parity queued a thread
+  __shared__ int s_rowfix[4];                               // the row (by row % 4) queued a thread
   __shared__ __align__(8) uint64_t full_bar[kPeStages];
   __shared__ __align__(8) uint64_t list_bar[2];
   __shared__ int s_abort;  // written anywhere, read only right after a CTA barrier
@@ -397,7 +397,7 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
     s_abort = 0;
     s_nfix = 0;
     s_ovf = 0x7fffffff;
-    s_rowfix[0] = s_rowfix[1] = 0;
+    s_rowfix[0] = s_rowfix[1] = s_rowfix[2] = s_rowfix[3] = 0;
   }
   if (tid < kPeStages) s_desc[tid] = make_int4(0, 0, 0, 0);  // in range even if a wait times out
   if (tid < 2 * kPeMaxWarps) (&s_part[0][0])[tid] = 0.f;
@@ -458,6 +458,51 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
     xo[m] = vok[m] ? vidx[m] * 16u : 0u;
   }
 
+  // per-group FP8: the codes of one row from its products v, to q (the row in
+  // global memory, or the shared buffer of a bulk row)
+  auto fp8_row = [&](int i, uint8_t* q, bool bulk, const f32x2 (&v)[kPeVpt][4]) {
+    // a 128-element group is 4 neighbouring threads: the maximum over this
+    // thread's 32 elements, then two shuffles
+    float gm = 0.f;
+#pragma unroll
+    for (int m = 0; m < kPeVpt; ++m) {
+#pragma unroll
+      for (int k = 0; k < 4; ++k) {
+        float a, b;
+        f2_split(v[m][k], a, b);
+        gm = fmax_abs3(gm, a, b);
+      }
+    }
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
+    gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
+    if ((tid & 3) == 0 && vok[0]) s_gm[i & 3][tid >> 2] = gm;
+    f32x2 rh2, rl2;
+    pe_brackets(gm, kF, rh2, rl2);
+    uint2 c[kPeVpt];
+    uint32_t diff = 0;
+#pragma unroll
+    for (int m = 0; m < kPeVpt; ++m) {
+      const uint32_t d = pe_fp8_codes<YT>(v[m], rh2, rl2, c[m]);
+      diff |= vok[m] ? d : 0u;
+    }
+    if (!pe_fast(gm) || diff != 0u) {  // rare: zero codes for an all-zero group, else recomputed after the last row
+      if (gm == 0.f) {
+#pragma unroll
+        for (int m = 0; m < kPeVpt; ++m) c[m] = make_uint2(0u, 0u);
+      } else if (vok[0] || vok[2]) {  // the thread holds a vector of the row
+        pe_queue(s_fixq, &s_nfix, &s_ovf, &s_rowfix[i & 3], i, tid, 0.f);
+      }
+    }
+    // vectors vidx[2p], vidx[2p] + 1 are registers 2p, 2p + 1
+#pragma unroll
+    for (int m = 0; m < kPeVpt; m += 2) {
+      if (vok[m + 1]) {
+        if (bulk) put16<true>(q, vidx[m], c[m], c[m + 1]); else put16<false>(q, vidx[m], c[m], c[m + 1]);
+      } else if (vok[m]) {
+        if (bulk) put8<true>(q, vidx[m], c[m]); else put8<false>(q, vidx[m], c[m]);
+      }
+    }
+  };
   f32x2 sc[kPeVpt][4];  // this thread's part of the scales row of expert cur_e
   int cur_e = -1;
   int nb = 0;         // rows through the shared buffers so far
@@ -468,7 +513,8 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
     int4 en;
     f32x2 v[kPeVpt][4];
     if (!producer) {
-      if (!mbar_wait_bounded(&full_bar[st], phase, p.status, p.timeout_ns)) s_abort = 1;
+      const bool landed = mbar_wait_bounded(&full_bar[st], phase, p.status, p.timeout_ns);
+      if (!landed) s_abort = 1;
       en = s_desc[st];
       if (en.z != cur_e) {
         pe_load_scales(p.qscales + (size_t)en.z * sh.h, vidx, vok, sc);
@@ -498,6 +544,11 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
         }
         const float wm = warp_max_nonneg(fmaxf(m0, m1));
         if (lane == 0) s_part[i & 1][warp] = wm;
+      } else if (en.w == 0 && landed) {
+        // per-group FP8, store plane: the codes need no other warp's values,
+        // so they leave before the barrier (a row whose slot never landed is
+        // not stored)
+        fp8_row(i, out + (long long)en.x * row_out, false, v);
       }
     } else {
       en = s_desc[st];  // written by this warp's lane 0 rows ago
@@ -505,8 +556,9 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
       if (en.w != 0 && leader) bulk_wait_read<1>();
     }
     const bool bulk = en.w != 0;
-    // row i's slot is read, every thread's stores of row i-1 are issued, the
-    // warp maxima of row i and the group maxima and queue of row i-1 are visible
+    // row i's slot is read, every thread's stores of row i-1 (per-group FP8
+    // store plane: of row i) are issued, the warp maxima of row i and the
+    // group maxima and queue of row i-1 are visible
     __syncthreads();
     if (s_abort) break;
     const long long dst = en.x;
@@ -538,9 +590,9 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
       if (i >= 1) {
         // row i-1's ready flag and time, unless it queued a thread (then they
         // follow its exact codes after the last row)
-        const bool later = s_rowfix[(i - 1) & 1] != 0 || i - 1 >= s_ovf;
+        const bool later = s_rowfix[(i - 1) & 3] != 0 || i - 1 >= s_ovf;
         __syncwarp();
-        if (lane == 0) s_rowfix[(i - 1) & 1] = 0;
+        if (lane == 0) s_rowfix[(i - 1) & 3] = 0;
         if (leader && !later) {
           if (p.seg_ready) {
             if (pen.w != 0) {
@@ -554,7 +606,7 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
         }
         // the group scales of row i-1, from its group maxima
         if (MODE == 3) {
-          for (int g = lane; g < nd; g += 32) dyn[(long long)pen.x * nd + g] = __fdiv_rn(s_gm[(i - 1) & 1][g], kF);
+          for (int g = lane; g < nd; g += 32) dyn[(long long)pen.x * nd + g] = __fdiv_rn(s_gm[(i - 1) & 3][g], kF);
         }
       }
       if (MODE == 2 && leader) dyn[dst] = __fdiv_rn(amax, 127.0f);
@@ -573,7 +625,7 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
 #pragma unroll
         for (int m = 0; m < kPeVpt; ++m) c[m] = make_uint2(0u, 0u);
       } else if (!pe_fast(amax) || diff != 0u) {  // rare: recomputed exactly after the last row
-        pe_queue(s_fixq, &s_nfix, &s_ovf, &s_rowfix[i & 1], i, tid, amax);
+        pe_queue(s_fixq, &s_nfix, &s_ovf, &s_rowfix[i & 3], i, tid, amax);
       }
       if (bulk) {
 #pragma unroll
@@ -584,48 +636,8 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
         for (int m = 0; m < kPeVpt; ++m)
           if (vok[m]) put8<false>(q, tid + m * nthr, c[m]);
       }
-    } else {
-      // a 128-element group is 4 neighbouring threads: the maximum over this
-      // thread's 32 elements, then two shuffles
-      float gm = 0.f;
-#pragma unroll
-      for (int m = 0; m < kPeVpt; ++m) {
-#pragma unroll
-        for (int k = 0; k < 4; ++k) {
-          float a, b;
-          f2_split(v[m][k], a, b);
-          gm = fmax_abs3(gm, a, b);
-        }
-      }
-      gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 1));
-      gm = fmaxf(gm, __shfl_xor_sync(0xffffffffu, gm, 2));
-      if ((tid & 3) == 0 && vok[0]) s_gm[i & 1][tid >> 2] = gm;
-      f32x2 rh2, rl2;
-      pe_brackets(gm, kF, rh2, rl2);
-      uint2 c[kPeVpt];
-      uint32_t diff = 0;
-#pragma unroll
-      for (int m = 0; m < kPeVpt; ++m) {
-        const uint32_t d = pe_fp8_codes<YT>(v[m], rh2, rl2, c[m]);
-        diff |= vok[m] ? d : 0u;
-      }
-      if (!pe_fast(gm) || diff != 0u) {  // rare: zero codes for an all-zero group, else recomputed after the last row
-        if (gm == 0.f) {
-#pragma unroll
-          for (int m = 0; m < kPeVpt; ++m) c[m] = make_uint2(0u, 0u);
-        } else if (vok[0] || vok[2]) {  // the thread holds a vector of the row
-          pe_queue(s_fixq, &s_nfix, &s_ovf, &s_rowfix[i & 1], i, tid, 0.f);
-        }
-      }
-      // vectors vidx[2p], vidx[2p] + 1 are registers 2p, 2p + 1
-#pragma unroll
-      for (int m = 0; m < kPeVpt; m += 2) {
-        if (vok[m + 1]) {
-          if (bulk) put16<true>(q, vidx[m], c[m], c[m + 1]); else put16<false>(q, vidx[m], c[m], c[m + 1]);
-        } else if (vok[m]) {
-          if (bulk) put8<true>(q, vidx[m], c[m]); else put8<false>(q, vidx[m], c[m]);
-        }
-      }
+    } else if (bulk) {
+      fp8_row(i, q, true, v);
     }
     if (bulk) {
       ++nb;
@@ -645,7 +657,7 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
   const bool ran = n_run > 0 && !s_abort;
   if (producer && ran) {
     if (MODE == 3) {
-      for (int g = lane; g < nd; g += 32) dyn[(long long)pen.x * nd + g] = __fdiv_rn(s_gm[(n_run - 1) & 1][g], kF);
+      for (int g = lane; g < nd; g += 32) dyn[(long long)pen.x * nd + g] = __fdiv_rn(s_gm[(n_run - 1) & 3][g], kF);
     }
   }
   if (leader) {  // the bulk rows have landed: the exact codes below overwrite theirs
@@ -678,7 +690,7 @@ __global__ void __launch_bounds__(kPeMaxThreads + 32, 1) scatter_pe_kernel(Scatt
       }
       if (p.perf) perf_mark(p, (size_t)en.y);
     };
-    if (s_rowfix[(n_run - 1) & 1] == 0 && n_run - 1 < ovf) publish(pen);
+    if (s_rowfix[(n_run - 1) & 3] == 0 && n_run - 1 < ovf) publish(pen);
     int last = -1;
     for (int k = 0; k < nq; ++k) {
       const int r = s_fixq[k].x;
