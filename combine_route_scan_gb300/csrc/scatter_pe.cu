@@ -30,8 +30,9 @@
 //     on the bits of non-negative floats, whose unsigned order is their
 //     numeric order). Per-group FP8: thread tid takes the 32 elements
 //     32 tid .. 32 tid + 31, a quarter of a 128-element group, so a group's
-//     maximum takes two shuffles and its codes leave as 16-byte stores. The
-//     barrier a row frees the ring slot. The producer warp also writes the
+//     maximum takes two shuffles and its codes leave as 16-byte stores, for
+//     a store-plane row before the row's barrier (they need no other warp's
+//     values). The barrier a row frees the ring slot. The producer warp also writes the
 //     dynamic scales (so that one warp, not every lane, carries those
 //     divisions) and publishes ready flags and times.
 //
