@@ -25,7 +25,9 @@ def test_checked_build_runs_the_parity_selection():
     from combine_route_scan_gb300 import build as B
     lib = B.build(checked=True)
     assert os.path.exists(lib)
-    env = dict(os.environ, CRS_MOE_CHECKED="1")
+    # the child loads this build alone, whatever build the parent selected
+    env = {k: v for k, v in os.environ.items() if k not in ("CRS_MOE_CHECKED", "CRS_MOE_OBSERVER", "CRS_MOE_PHASE")}
+    env["CRS_MOE_CHECKED"] = "1"
     probe = subprocess.run([sys.executable, "-c", "from combine_route_scan_gb300 import moe; print(moe.lib()._name)"],
                            cwd=ROOT, env=env, capture_output=True, text=True, timeout=120)
     assert probe.returncode == 0 and os.path.join("_build", "checked") in probe.stdout, probe.stdout + probe.stderr

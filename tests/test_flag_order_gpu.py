@@ -23,7 +23,9 @@ def test_flags_never_precede_their_rows():
     from combine_route_scan_gb300 import build as B
     lib = B.build(observer=True)
     assert os.path.exists(lib)
-    env = dict(os.environ, CRS_MOE_OBSERVER="1")
+    # the child loads this build alone, whatever build the parent selected
+    env = {k: v for k, v in os.environ.items() if k not in ("CRS_MOE_CHECKED", "CRS_MOE_OBSERVER", "CRS_MOE_PHASE")}
+    env["CRS_MOE_OBSERVER"] = "1"
     r = subprocess.run([sys.executable, "-m", "pytest", "tests/flag_observer_cases.py", "-q", "-x", "-s", "-m", "gpu",
                         "-p", "no:cacheprovider"], cwd=ROOT, env=env, capture_output=True, text=True, timeout=900)
     assert r.returncode == 0, f"{r.stdout[-4000:]}\n{r.stderr[-2000:]}"
